@@ -1,0 +1,313 @@
+"""CPU oracle for the paged LATENT (absorbed-MLA) attention operator.
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path may import this
+module: only the tests, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` use it.
+
+It is a plain, slow, obviously-correct restatement of what the operator
+computes, in float64 numpy, sharing no code with the CUDA path. Sources (the
+onnx-runtime-ep-cuda ``paged_attention.rs`` page and the PR pages around it):
+
+* token -> (sequence, absolute position): ``paged_attention.rs`` device
+  helper ``locate_token`` (first sequence whose cumulative end exceeds the
+  token; position = past + offset inside the sequence).
+* partial RoPE on channels ``[rotary_offset, rotary_offset + rotary_dim)``:
+  ``paged_attention.rs`` helper ``rope_channel`` (non-interleaved: the first
+  half rotates with -sin against the partner half channels away, the second
+  half with +sin; interleaved: even/odd neighbours).
+* write phase: ``paged_attention.rs`` ``write_impl`` and the module doc
+  "Write phase" (post-RoPE row rounded to the cache dtype and stored at
+  ``key_cache[slot]``; slot -1 skips).
+* read phase: ``paged_attention.rs`` ``attn_impl`` and the module doc "Read
+  phase" (causal keys 0..=pos, window skip when pos-j > window, score =
+  scale * q.k then softcap*tanh(s/softcap), softmax, V = leading
+  v_head_size channels of the same latent row, output rounded to dtype,
+  zero when no key is visible).
+* softmax form: PR #1978 review ("online-softmax ... algebraically identical
+  to the oracle's two-pass"); this oracle is the two-pass form.
+
+Precision: every value is converted exactly to float64; RoPE, dot products,
+softmax and the weighted sum are evaluated in float64 and only the stored
+results (cache rows, outputs) are rounded, round-to-nearest-even, to the
+operator dtype. The pages' own oracle accumulates in f32; float64 only
+tightens the reference.
+
+Pins (tests/test_oracle_pins.py): the rounding routine against torch and
+numpy casts, RoPE against complex multiplication and the relative-position
+identity, the attention against a naive contiguous dense attention, against
+decomposed multi-head latent attention, placement invariance under a
+permuted block table, untouched cache rows for slot -1, and closed-form
+special cases.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BF16 = "bf16"
+F16 = "f16"
+
+
+# ---------------------------------------------------------------------------
+# Number formats
+# ---------------------------------------------------------------------------
+
+def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Exact widening of bf16/f16 bit patterns (uint16) to float64."""
+    bits = np.asarray(bits, dtype=np.uint16)
+    if dtype == BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype == F16:
+        return bits.view(np.float16).astype(np.float64)
+    raise ValueError(dtype)
+
+
+_FMT = {
+    # mantissa bits, minimum normal exponent, largest finite value
+    BF16: (7, -126, float.fromhex("0x1.fep127")),
+    F16: (10, -14, 65504.0),
+}
+
+
+def round_f64_to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values to the nearest bf16/f16 value, ties to even,
+    overflowing to +-inf, and return the bit patterns (uint16).
+
+    The rounding is done directly from float64 (no intermediate float32):
+    with e = max(floor(log2|x|), emin) the representable spacing is
+    2^(e - mantissa_bits); x / spacing is an exact float64 and
+    ``np.rint`` rounds it half-to-even."""
+    mant, emin, maxv = _FMT[dtype]
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        _, ex = np.frexp(ax)           # ax = m * 2^ex, m in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, emin)
+    spacing = np.ldexp(1.0, (e - mant).astype(np.int64))
+    with np.errstate(invalid="ignore", over="ignore"):
+        r = np.rint(x / spacing) * spacing
+    r = np.where(np.isfinite(x), r, x)
+    r = np.where(np.abs(r) > maxv, np.copysign(np.inf, x), r)
+    if dtype == BF16:
+        return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    return r.astype(np.float16).view(np.uint16)
+
+
+def round_f64(x: np.ndarray, dtype: str) -> np.ndarray:
+    """Round float64 values to the dtype and widen back to float64."""
+    return bits_to_f64(round_f64_to_bits(x, dtype), dtype)
+
+
+# ---------------------------------------------------------------------------
+# Token location and RoPE
+# ---------------------------------------------------------------------------
+
+def locate_token(t: int, cumseq: np.ndarray, past: np.ndarray):
+    """(sequence b, absolute position) of global token t: b is the first
+    sequence whose cumulative end cumseq[b+1] exceeds t; the position is
+    past[b] plus t's offset inside that sequence. Tokens outside
+    [0, cumseq[B]) are rejected (the pages fall back to sequence 0; the
+    operator contract requires cumseq[B] == T)."""
+    B = len(past)
+    for b in range(B):
+        if t < int(cumseq[b + 1]):
+            if t < int(cumseq[b]):
+                raise ValueError("cumulative_sequence_length is not monotone")
+            return b, int(past[b]) + (t - int(cumseq[b]))
+    raise ValueError(f"token {t} lies beyond cumulative_sequence_length[B]")
+
+
+def rope_row(x: np.ndarray, pos: int, rotary_offset: int, rotary_dim: int,
+             cos_tab: np.ndarray, sin_tab: np.ndarray, interleaved: bool) -> np.ndarray:
+    """Partial RoPE of one head row (float64) at absolute position ``pos``.
+
+    Channels outside [ro, ro+rd) are returned unchanged. Inside, with
+    half = rd/2 and c_i, s_i = cos_tab[pos, i], sin_tab[pos, i]:
+
+    * non-interleaved: channel ro+i (i < half) pairs with ro+i+half,
+      out[ro+i] = x[ro+i] c_i - x[ro+i+half] s_i and
+      out[ro+i+half] = x[ro+i+half] c_i + x[ro+i] s_i;
+    * interleaved: channel ro+2i pairs with ro+2i+1,
+      out[ro+2i] = x[ro+2i] c_i - x[ro+2i+1] s_i and
+      out[ro+2i+1] = x[ro+2i+1] c_i + x[ro+2i] s_i.
+    """
+    out = np.array(x, dtype=np.float64, copy=True)
+    if rotary_dim == 0:
+        return out
+    half = rotary_dim // 2
+    c = cos_tab[pos, :half]
+    s = sin_tab[pos, :half]
+    seg = out[rotary_offset:rotary_offset + rotary_dim]
+    if interleaved:
+        a = seg[0::2].copy()
+        b = seg[1::2].copy()
+        seg[0::2] = a * c - b * s
+        seg[1::2] = b * c + a * s
+    else:
+        a = seg[:half].copy()
+        b = seg[half:].copy()
+        seg[:half] = a * c - b * s
+        seg[half:] = b * c + a * s
+    return out
+
+
+# ---------------------------------------------------------------------------
+# The paged cache: one latent row per slot (slot = block * bs + offset)
+# ---------------------------------------------------------------------------
+
+class F64Cache:
+    """Cache rows held exactly in float64 (no rounding on store)."""
+
+    def __init__(self, rows: np.ndarray):
+        self.rows = np.array(rows, dtype=np.float64, copy=True)
+
+    @property
+    def num_rows(self) -> int:
+        return self.rows.shape[0]
+
+    def get(self, idx) -> np.ndarray:
+        return self.rows[idx]
+
+    def put(self, slot: int, row: np.ndarray):
+        self.rows[slot] = row
+
+
+class BitsCache:
+    """Cache rows held as bf16/f16 bit patterns; a store rounds the float64
+    row to the dtype, a load widens exactly."""
+
+    def __init__(self, bits: np.ndarray, dtype: str):
+        self.bits = np.array(bits, dtype=np.uint16, copy=True)
+        self.dtype = dtype
+
+    @property
+    def num_rows(self) -> int:
+        return self.bits.shape[0]
+
+    def get(self, idx) -> np.ndarray:
+        return bits_to_f64(self.bits[idx], self.dtype)
+
+    def put(self, slot: int, row: np.ndarray):
+        self.bits[slot] = round_f64_to_bits(row, self.dtype)
+
+
+# ---------------------------------------------------------------------------
+# The operator: write phase, then read phase
+# ---------------------------------------------------------------------------
+
+def _check_geometry(p: dict):
+    hs, vhs = p["head_size"], p["v_head_size"] or p["head_size"]
+    assert 1 <= vhs <= hs
+    assert p["rotary_offset"] + p["rotary_dim"] <= hs
+    return hs, vhs
+
+
+def latent_write(key, cos_tab: np.ndarray, sin_tab: np.ndarray, slot_mapping: np.ndarray,
+                 cumseq: np.ndarray, past: np.ndarray, cache, p: dict):
+    """Write phase. ``key`` maps a token index to its float64 latent row
+    (an array ``[T, hs]`` or a callable); ``cache`` is an F64Cache or
+    BitsCache and is updated in place.
+
+    For every token t, in order: skip when slot_mapping[t] < 0; otherwise
+    apply partial RoPE to key[t] at the token's absolute position and store
+    the row (rounded to the cache dtype by the cache) at row
+    slot_mapping[t]."""
+    _check_geometry(p)
+    get_key = key if callable(key) else (lambda t: key[t])
+    for t in range(len(slot_mapping)):
+        slot = int(slot_mapping[t])
+        if slot < 0:
+            continue
+        if slot >= cache.num_rows:
+            raise ValueError(f"slot {slot} outside the cache")
+        _, pos = locate_token(t, cumseq, past)
+        cache.put(slot, rope_row(get_key(t), pos, p["rotary_offset"], p["rotary_dim"],
+                                 cos_tab, sin_tab, bool(p["rotary_interleaved"])))
+    return cache
+
+
+def visible_keys(pos: int, window: int):
+    """Causal keys 0..=pos, minus those with pos - j > window when the
+    window is enabled (window >= 0)."""
+    lo = 0 if window < 0 else max(0, pos - window)
+    return range(lo, pos + 1)
+
+
+def cache_row_index(b: int, j: int, block_table: np.ndarray, block_size: int,
+                    num_blocks: int) -> int:
+    """Row of logical key j of sequence b: block_table[b, j // bs] is the
+    physical block, j % bs the offset inside it."""
+    phys = int(block_table[b, j // block_size])
+    if not 0 <= phys < num_blocks:
+        raise ValueError(f"block_table[{b}, {j // block_size}] = {phys} is not a block")
+    return phys * block_size + j % block_size
+
+
+def latent_attend_token(t: int, q_row: np.ndarray, cache, cos_tab: np.ndarray,
+                        sin_tab: np.ndarray, cumseq: np.ndarray, past: np.ndarray,
+                        block_table: np.ndarray, p: dict) -> np.ndarray:
+    """Read phase for token t, all heads: returns float64 ``[H, vhs]``.
+    ``q_row`` is the token's float64 query row ``[H*hs]``.
+
+    q_h = RoPE(q_row[h*hs:(h+1)*hs]) (kept in float64), K_j the cache row of
+    visible key j, s_hj = scale * q_h . K_j, then
+    s_hj = softcap * tanh(s_hj / softcap) when softcap > 0, a two-pass
+    softmax over j, and out_h = sum_j p_hj K_j[:vhs] / sum_j p_hj; zero
+    when no key is visible."""
+    hs, vhs = _check_geometry(p)
+    H = p["num_heads"]
+    bs = p["block_size"]
+    num_blocks = cache.num_rows // bs
+    b, pos = locate_token(t, cumseq, past)
+    q = np.stack([rope_row(q_row[h * hs:(h + 1) * hs], pos, p["rotary_offset"],
+                           p["rotary_dim"], cos_tab, sin_tab,
+                           bool(p["rotary_interleaved"])) for h in range(H)])
+    keys = list(visible_keys(pos, p["local_window_size"]))
+    if not keys:
+        return np.zeros((H, vhs))
+    rows = [cache_row_index(b, j, block_table, bs, num_blocks) for j in keys]
+    K = cache.get(rows)                               # [n, hs]
+    s = (q @ K.T) * p["scale"]                        # [H, n]
+    if p["softcap"] > 0.0:
+        s = p["softcap"] * np.tanh(s / p["softcap"])
+    m = s.max(axis=1, keepdims=True)
+    w = np.exp(s - m)
+    den = w.sum(axis=1, keepdims=True)
+    return (w @ K[:, :vhs]) / den
+
+
+def latent_attend(query, cache, cos_tab, sin_tab, cumseq, past, block_table, p,
+                  tokens=None) -> np.ndarray:
+    """Read phase for the listed tokens (default: all). ``query`` maps a
+    token index to its float64 row (an array ``[T, H*hs]`` or a callable).
+    Returns float64 ``[len(tokens), H, vhs]``."""
+    get_q = query if callable(query) else (lambda t: query[t])
+    tokens = range(int(cumseq[-1])) if tokens is None else tokens
+    return np.stack([latent_attend_token(int(t), get_q(int(t)), cache, cos_tab, sin_tab,
+                                         cumseq, past, block_table, p) for t in tokens])
+
+
+# ---------------------------------------------------------------------------
+# Bit-level entry point (operator dtype in, operator dtype out)
+# ---------------------------------------------------------------------------
+
+def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cumseq, past,
+                      block_table, slot_mapping, p: dict, tokens=None):
+    """Write then read, on uint16 bit arrays of the operator dtype.
+
+    Shapes: query ``[T, H*hs]``, key ``[T, hs]``, cache
+    ``[num_blocks, bs, 1, hs]`` (any shape with hs last), cos/sin
+    ``[rows, rd/2]``. The read phase sees the cache after the write.
+    Returns (new cache bits in the input's shape, output bits
+    ``[len(tokens), H*vhs]``, output float64 before rounding)."""
+    dt = p["dtype"]
+    hs, _ = _check_geometry(p)
+    shape = cache_bits.shape
+    cache = BitsCache(np.asarray(cache_bits).reshape(-1, hs), dt)
+    cos_tab = bits_to_f64(cos_bits, dt)
+    sin_tab = bits_to_f64(sin_bits, dt)
+    latent_write(lambda t: bits_to_f64(key_bits[t], dt), cos_tab, sin_tab,
+                 np.asarray(slot_mapping), cumseq, past, cache, p)
+    out = latent_attend(lambda t: bits_to_f64(query_bits[t], dt), cache, cos_tab, sin_tab,
+                        cumseq, past, block_table, p, tokens)
+    out = out.reshape(out.shape[0], -1)
+    return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out

@@ -1,0 +1,68 @@
+"""Plant plausible mistakes in a copy of the oracle and check that the pins
+catch each one. The copy is built from the oracle's source text with one
+substitution and loaded as a separate module; the real oracle is untouched.
+"""
+import importlib.util
+import inspect
+import types
+
+import pytest
+
+from oracle import pa_oracle
+import tests.test_oracle_pins as pins
+
+MUTANTS = {
+    "rope_first_half_sign": ("seg[:half] = a * c - b * s", "seg[:half] = a * c + b * s"),
+    "rope_second_half_sign": ("seg[half:] = b * c + a * s", "seg[half:] = b * c - a * s"),
+    "rope_interleaved_sign": ("seg[0::2] = a * c - b * s", "seg[0::2] = a * c + b * s"),
+    "rope_wrong_position": ("c = cos_tab[pos, :half]", "c = cos_tab[max(pos - 1, 0), :half]"),
+    "window_off_by_one": ("max(0, pos - window)", "max(0, pos - window + 1)"),
+    "causal_excludes_self": ("return range(lo, pos + 1)", "return range(lo, max(pos, lo + 1))"),
+    "softcap_dropped": ('s = p["softcap"] * np.tanh(s / p["softcap"])', "pass"),
+    "softcap_before_scale": ('s = (q @ K.T) * p["scale"]', 's = (q @ K.T)'),
+    "value_wrong_channels": ("(w @ K[:, :vhs])", "(w @ K[:, hs - vhs:])"),
+    "block_offset_wrong": ("return phys * block_size + j % block_size",
+                           "return phys * block_size + (j + 1) % block_size"),
+    "position_ignores_past": ("return b, int(past[b]) + (t - int(cumseq[b]))",
+                              "return b, (t - int(cumseq[b]))"),
+    "rounding_truncates": ("r = np.rint(x / spacing) * spacing",
+                           "r = np.trunc(x / spacing) * spacing"),
+    "slot_minus_one_written": ("if slot < 0:\n            continue",
+                               "if slot < -1:\n            continue"),
+    "softmax_not_normalised": ("return (w @ K[:, :vhs]) / den", "return (w @ K[:, :vhs])"),
+}
+
+PINS = [
+    lambda: pins.test_round_bf16_matches_torch_cast(),
+    lambda: pins.test_round_f16_matches_numpy_cast(),
+    lambda: pins.test_rope_is_complex_rotation(0),
+    lambda: pins.test_rope_is_complex_rotation(1),
+    lambda: pins.test_rope_relative_position(0),
+    lambda: pins.test_attention_matches_naive_contiguous(0.0, -1),
+    lambda: pins.test_attention_matches_naive_contiguous(1.5, -1),
+    lambda: pins.test_attention_matches_naive_contiguous(0.0, 3),
+    lambda: pins.test_absorbed_equals_decomposed_mla(128, 32, 32, 64, 3),
+    lambda: pins.test_slot_minus_one_leaves_cache_untouched(),
+    lambda: pins.test_two_key_softcap_closed_form(),
+]
+
+
+def _mutant(old, new):
+    src = inspect.getsource(pa_oracle)
+    assert src.count(old) == 1, old
+    mod = types.ModuleType("pa_oracle_mutant")
+    exec(compile(src.replace(old, new), "pa_oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    mod = _mutant(*MUTANTS[name])
+    monkeypatch.setattr(pins, "O", mod)
+    caught = []
+    for pin in PINS:
+        try:
+            pin()
+        except Exception as e:  # AssertionError, or the mutant breaking outright
+            caught.append(type(e).__name__)
+    assert caught, f"no pin caught mutant {name}"
