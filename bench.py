@@ -1,0 +1,512 @@
+"""Benchmark of the paged LATENT attention operator on one node.
+
+One step = one pass of the whole operator over one synthetic batch: the
+write phase (RoPE + paged scatter of the new latent rows), the decode phase
+(split-KV attention + log-sum-exp combine) and, for mixed batches, the
+prefill phase. The default workload is GLM-style dense MLA decode (bf16,
+H=64, latent 192 / value 128 / rotary 64 at offset 128, batch 32, one new
+token per sequence, contexts uniform in [1024, 8192], bs=64).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl reference] [--portable]
+
+Timing: W untimed steps, then K timed steps bracketed by a barrier and a
+device synchronise; each step is timed with CUDA events on the launching
+stream and L2 is flushed (a write of 2x the L2 size) before every step,
+outside the events. Under torchrun each rank runs its own seeded batch
+(weak scaling, no collective on the data path) and the max over ranks is
+reported. `value` is algorithmic latent-cache bytes per second (TB/s);
+`e2e` is the same metric through the operator object with the step's inputs
+copied host->device from pinned memory and the output copied back inside
+the timed region. `--impl reference` times the CPU oracle on the same
+workload instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("paged-MLA decode latent-cache TB/s & TFLOP/s vs roofline; prefill TFLOP/s "
+          "(1 GB300)")
+UNIT = "TB/s"
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work of a workload (each visible cache row counted once)
+# ---------------------------------------------------------------------------
+
+def algorithmic_work(w, seqs=None, tokens=None, include_write=True):
+    """Bytes and FLOPs of the operator on a workload, counting each cache
+    row a sequence's queries can see once, plus Q, O, the cos/sin rows, the
+    block-table entries, the key rows read and the cache rows written.
+    FLOPs = (2*hs + 2*vhs) per (visible key, head). ``seqs`` restricts the
+    read phase to those sequences, ``tokens`` to those tokens."""
+    el = 2
+    H, hs, vhs, bs = w.num_heads, w.head_size, w.v_head_size, w.block_size
+    win = w.local_window_size
+    cs = w.cumseq.tolist()
+    seqs = range(w.num_seqs) if seqs is None else seqs
+    tok_set = None if tokens is None else set(int(t) for t in tokens)
+    cache_rows = flops = q_rows = bt_entries = 0
+    for b in seqs:
+        lo_t, hi_t = cs[b], cs[b + 1]
+        toks = [t for t in range(lo_t, hi_t) if tok_set is None or t in tok_set]
+        if not toks:
+            continue
+        P = w.past_lens[b]
+        first_lo = None
+        last_pos = None
+        for t in toks:
+            pos = P + t - lo_t
+            lo = 0 if win < 0 else max(0, pos - win)
+            flops += (pos + 1 - lo) * H * (2 * hs + 2 * vhs)
+            first_lo = lo if first_lo is None else min(first_lo, lo)
+            last_pos = pos if last_pos is None else max(last_pos, pos)
+        span = last_pos + 1 - first_lo
+        cache_rows += span
+        bt_entries += last_pos // bs - first_lo // bs + 1
+        q_rows += len(toks)
+    read_bytes = (cache_rows * hs * el + q_rows * H * hs * el + q_rows * H * vhs * el +
+                  q_rows * w.rotary_dim * el + bt_entries * 4)
+    write_bytes = 0
+    if include_write:
+        n_written = int((w.slot_mapping >= 0).sum())
+        write_bytes = (w.num_tokens * hs * el + n_written * hs * el +
+                       w.num_tokens * (w.rotary_dim * el + 4))
+    return dict(bytes=read_bytes + write_bytes, read_bytes=read_bytes, flops=flops,
+                cache_rows=cache_rows, tokens=q_rows)
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        return parse_clocks(self.path)
+
+
+def parse_clocks(path: str):
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    try:
+        lines = open(path).read().strip().splitlines()
+    except Exception:
+        return None
+    for ln in lines:
+        parts = [p.strip() for p in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            mx.append(float(parts[2]))
+        except ValueError:
+            continue
+        for n, v in zip(names, parts[5:9]):
+            if v.lower().startswith("active"):
+                reasons.add(n)
+    if not sm:
+        return None
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+            "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Multi-rank helpers (also exercised on CPU with gloo in the tests)
+# ---------------------------------------------------------------------------
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own independent batch (weak scaling)."""
+    return base_seed + 1000 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# Oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+
+def time_oracle(w, budget_s: float, tokens_order=None):
+    """Runs the CPU oracle's read phase token by token (after its write phase
+    over the whole batch) until ``budget_s`` of wall time is used. Returns
+    (seconds, algorithmic bytes of the sampled work, tokens done)."""
+    import numpy as np
+    from oracle import pa_oracle as O
+    from paged_latent_attention_cache_gb300 import workloads as W
+    p = W.oracle_params(w)
+    dt = p["dtype"]
+    hs = w.head_size
+    t0 = time.perf_counter()
+    cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
+    cos_t, sin_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt), O.bits_to_f64(W.to_bits(w.sin_cache), dt)
+    kb, qb = W.to_bits(w.key), W.to_bits(w.query)
+    cumseq, past, bt = w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy()
+    O.latent_write(lambda t: O.bits_to_f64(kb[t], dt), cos_t, sin_t, w.slot_mapping.numpy(),
+                   cumseq, past, cache, p)
+    done = []
+    order = list(range(w.num_tokens)) if tokens_order is None else tokens_order
+    for t in order:
+        out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
+                                    past, bt, p)
+        O.round_f64_to_bits(out, dt)
+        done.append(t)
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    sec = time.perf_counter() - t0
+    work = algorithmic_work(w, tokens=done)
+    return sec, work, len(done)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def build_workload(name: str, seed_offset: int):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    fn = W.WORKLOADS[name]
+    import inspect
+    default_seed = inspect.signature(fn).parameters["seed"].default
+    return fn(seed=default_seed + seed_offset)
+
+
+def count_launches(step_fn):
+    """Kernels of this library launched by one step, counted by the torch
+    profiler (CUPTI); None if the profiler is unavailable."""
+    import torch
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step_fn()
+            torch.cuda.synchronize()
+        n = 0
+        for e in prof.events():
+            name = e.name or ""
+            if ("pa::" in name or "_ZN2pa" in name) and "kernel" in name:
+                n += 1
+        return n
+    except Exception:
+        return None
+
+
+def run_gpu_arm(args, rank, world, device):
+    import torch
+    from paged_latent_attention_cache_gb300 import build as _build
+    _build.build()
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+
+    w = build_workload(args.workload, rank_seed(0, rank) if world > 1 else 0)
+    d = w.to(device)
+    op = PagedLatentAttention.from_workload(w, device=device, portable=args.portable)
+    out = torch.empty(w.num_tokens, w.num_heads * w.v_head_size, dtype=w.dtype, device=device)
+    cache = d.key_cache
+    nd = w.num_decode_seqs
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
+        if ev is not None:
+            ev[1].record(stream)
+        if nd > 0:
+            op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                      d.block_table, out, 0, nd)
+        if ev is not None:
+            ev[2].record(stream)
+        if nd < w.num_seqs:
+            op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                       d.block_table, out, nd, w.num_seqs)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    launches_per_step = count_launches(step)
+    if op.error_flags() != 0:
+        raise RuntimeError(f"device error flags {op.error_flags():#x}")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    gpu_index = device.index
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[device.index])
+        except ValueError:
+            pass
+    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+    sampler = ClockSampler(gpu_index, os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv"))
+    time.sleep(0.3)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize(device)
+    barrier(device)
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    write_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    pre_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    ms_per_step = reduce_max(sum(step_ms) / K, device)
+
+    # End to end through the operator object: H2D of the step's inputs from
+    # pinned memory, the three phases, D2H of the output.
+    host = {k: getattr(w, k).pin_memory() for k in
+            ("query", "key", "cumseq", "past", "block_table", "slot_mapping")}
+    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        op.forward(dev_in["query"], dev_in["key"], cache, d.cos_cache, d.sin_cache,
+                   dev_in["cumseq"], dev_in["past"], dev_in["block_table"],
+                   dev_in["slot_mapping"], nd, out=out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize(device)
+    e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    barrier(device)
+    for i in range(K):
+        flush.zero_()
+        e2e_evs[i][0].record(stream)
+        e2e_step()
+        e2e_evs[i][1].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_evs) / K, device)
+    if op.error_flags() != 0:
+        raise RuntimeError(f"device error flags {op.error_flags():#x}")
+
+    work = algorithmic_work(w)
+    dec_work = algorithmic_work(w, seqs=range(nd), include_write=False)
+    pre_work = algorithmic_work(w, seqs=range(nd, w.num_seqs), include_write=False)
+    total_bytes = work["bytes"] * world
+    value = total_bytes / (ms_per_step * 1e-3) / 1e12
+    tflops = work["flops"] * world / (ms_per_step * 1e-3) / 1e12
+    res = dict(w=w, work=work, dec_work=dec_work, pre_work=pre_work, value=value,
+               tflops=tflops, ms_per_step=ms_per_step, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+               clocks=clocks, wall=wall, launches=launches_per_step,
+               write_ms=statistics.mean(write_ms), dec_ms=statistics.mean(dec_ms),
+               pre_ms=statistics.mean(pre_ms), step_ms_med=statistics.median(step_ms),
+               family=(op.kernel_family(0), op.kernel_family(1)))
+    return res
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="glm_decode")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--portable", action="store_true",
+                    help="force the portable CUDA-core attention kernels")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    args = ap.parse_args(argv)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    res = run_gpu_arm(args, rank, world, device)
+    if rank == 0:
+        w = res["w"]
+        hbm, bf16, peak_src = load_peaks()
+        dec_bytes = res["dec_work"]["bytes"] if w.num_decode_seqs else res["pre_work"]["bytes"]
+        dom_ms = res["dec_ms"] if w.num_decode_seqs else res["pre_ms"]
+        achieved = dec_bytes / (dom_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC,
+            "value": round(res["value"], 4),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": max(args.warmup, 3),
+            "ms_per_step": round(res["ms_per_step"], 5),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": {"torch.bfloat16": "bf16", "torch.float16": "f16"}[str(w.dtype)],
+            "data": "synthetic (seeded N(0,0.5^2) latent rows, shuffled block pool)",
+            "config": {"workload": w.name, "num_heads": w.num_heads,
+                       "head_size": w.head_size, "v_head_size": w.v_head_size,
+                       "rotary": [w.rotary_offset, w.rotary_dim], "block_size": w.block_size,
+                       "num_seqs": w.num_seqs, "num_tokens": w.num_tokens,
+                       "l2": "flushed before every step (write of 2x L2)",
+                       "parallelism": f"replicas x{world} (independent batches per rank)",
+                       "kernels": "portable" if args.portable else
+                       ("tcgen05" if res["family"][0] == 1 else "portable")},
+            "tflops": round(res["tflops"], 3),
+            "tokens_per_s": round(w.num_tokens * world / (res["ms_per_step"] * 1e-3), 1),
+            "phase_ms": {"write": round(res["write_ms"], 5), "decode": round(res["dec_ms"], 5),
+                         "prefill": round(res["pre_ms"], 5)},
+            "alg_bytes_per_step": res["work"]["bytes"],
+            "alg_flops_per_step": res["work"]["flops"],
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": None,
+                         "kernel": "decode call (split-KV attention + combine)"
+                         if w.num_decode_seqs else "prefill call",
+                         "peak_source": peak_src},
+            "e2e": {"value": round(res["work"]["bytes"] * world / (res["e2e_ms"] * 1e-3) / 1e12,
+                               4),
+                    "unit": UNIT, "ms_per_step": round(res["e2e_ms"], 5),
+                    "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": None if res["launches"] is None else res["launches"] * args.steps,
+            "clocks": res["clocks"],
+        }
+        if world == 1:
+            sec, work, n = time_oracle(w, args.cpu_budget)
+            line["cpu_baseline"] = {
+                "value": work["bytes"] / sec / 1e12, "unit": UNIT,
+                "cores": os.cpu_count(), "kind": "oracle",
+                "sample": f"oracle write phase over all {w.num_tokens} tokens + read phase of "
+                          f"the first {n} tokens ({sec:.1f} s, numpy float64, BLAS threads = "
+                          f"host cores)"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_reference(args, rank, world):
+    """The oracle arm: rank 0 times the CPU oracle on the same workload and
+    metric; each step is the oracle on one token's read phase (cycling
+    through the batch) after its write phase."""
+    if rank != 0:
+        return 0
+    import numpy as np
+    w = build_workload(args.workload, 0)
+    from oracle import pa_oracle as O
+    from paged_latent_attention_cache_gb300 import workloads as W
+    p = W.oracle_params(w)
+    dt, hs = p["dtype"], w.head_size
+    cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
+    cos_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt)
+    sin_t = O.bits_to_f64(W.to_bits(w.sin_cache), dt)
+    kb, qb = W.to_bits(w.key), W.to_bits(w.query)
+    cumseq, past, bt = w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy()
+    O.latent_write(lambda t: O.bits_to_f64(kb[t], dt), cos_t, sin_t, w.slot_mapping.numpy(),
+                   cumseq, past, cache, p)
+    T = w.num_tokens
+    # keep the whole run within a few minutes
+    per_step_budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+    def one(t):
+        out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
+                                    past, bt, p)
+        O.round_f64_to_bits(out, dt)
+    for i in range(max(args.warmup, 3)):
+        one(i % T)
+    total_s, total_bytes, done = 0.0, 0, 0
+    for i in range(args.steps):
+        t = i % T
+        t0 = time.perf_counter()
+        one(t)
+        dt_s = time.perf_counter() - t0
+        total_s += dt_s
+        total_bytes += algorithmic_work(w, tokens=[t], include_write=False)["bytes"]
+        done += 1
+        if total_s > per_step_budget * args.steps:
+            break
+    value = total_bytes / total_s / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": done, "warmup": max(args.warmup, 3),
+            "ms_per_step": 1e3 * total_s / done, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": W.dtype_tag(w.dtype), "data": "synthetic",
+            "config": {"workload": w.name},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": "one token's read phase per step, cycling through the "
+                                       "batch, after one write phase over all tokens"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

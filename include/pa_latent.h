@@ -1,0 +1,199 @@
+/*
+ * pa_latent.h — C ABI of the paged LATENT (absorbed multi-head latent)
+ * attention operator for NVIDIA GB300 (sm_103a).
+ *
+ * The operator is `com.microsoft::PagedAttention` v1 with
+ * kv_cache_layout="LATENT" as the onnx-runtime-ep-cuda page
+ * `src/kernels/paged_attention.rs` defines it (module doc, sections
+ * "LATENT semantics" and "Capture safety"; input order in the PR #1978
+ * review, "ORT v1.29 schema"). It has two phases, issued in this order on
+ * one stream:
+ *
+ *   1. pa_latent_write   — partial RoPE on each new latent key row, then a
+ *                          scatter into the paged cache at slot_mapping[t]
+ *                          (slot -1 skips the token).
+ *   2. pa_latent_decode  — causal attention of each query row (after
+ *      pa_latent_prefill   partial RoPE) over the sequence's cached prefix,
+ *                          read through block_table; one latent KV head of
+ *                          head_size channels; V is its leading
+ *                          v_head_size channels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every buffer pointer is a DEVICE pointer owned by the caller. The
+ *   library allocates nothing, never synchronises the host and never copies
+ *   between host and device; each call only enqueues kernels on `stream`
+ *   (a cudaStream_t passed as void*, NULL = the legacy default stream).
+ *   Calls are therefore safe to record into a CUDA graph, provided the
+ *   first call of each entry point on a device happened outside capture
+ *   (that call configures kernel attributes once per device).
+ * - Tensors are dense, row-major, with no padding between rows. Half
+ *   precision tensors (query, key, key_cache, cos/sin, out) must be
+ *   16-byte aligned; int32 tensors 4-byte aligned.
+ * - Symbols: T = num_tokens (new tokens in the batch, all sequences),
+ *   B = num_seqs, H = num_heads, hs = head_size, vhs = v_head_size,
+ *   bs = block_size, rd = rotary_dim.
+ * - Host-detectable errors return a status before anything is enqueued.
+ *   Conditions only the device can see (an index read from device memory
+ *   that is out of range) set a bit in the caller's int32 *err_flags
+ *   (atomic OR, never cleared by the library) and the offending access is
+ *   skipped: a cache row is not written, an output row is written as zeros.
+ *   No kernel traps, asserts or waits without bound.
+ */
+#ifndef PA_LATENT_H
+#define PA_LATENT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARGUMENT = 1, /* bad geometry, pointer, alignment or scale */
+  PA_ERR_NOT_IMPLEMENTED = 2,  /* a valid mode this library does not run   */
+  PA_ERR_CUDA = 3,             /* a CUDA runtime call failed               */
+  PA_ERR_WORKSPACE = 4         /* workspace missing or smaller than needed */
+} pa_status;
+
+typedef enum pa_dtype {
+  PA_DTYPE_F16 = 0,
+  PA_DTYPE_BF16 = 1
+} pa_dtype;
+
+/* Bits OR-ed into *err_flags by the device (see "Conventions"). */
+#define PA_DEVERR_SLOT        0x01 /* slot_mapping[t] >= num_blocks*bs or < -1     */
+#define PA_DEVERR_BLOCK       0x02 /* block_table entry read is not in [0, num_blocks) */
+#define PA_DEVERR_POSITION    0x04 /* absolute position >= cos_rows (rotary on)    */
+#define PA_DEVERR_CUMSEQ      0x08 /* cumseq not monotone, cumseq[0]!=0 or cumseq[B]!=T */
+#define PA_DEVERR_DECODE_QLEN 0x10 /* pa_latent_decode saw a sequence with q_len != 1 */
+#define PA_DEVERR_CONTEXT     0x20 /* past < 0 or context > max_blocks_per_seq*bs  */
+
+/* pa_latent_params.flags */
+#define PA_FLAG_PORTABLE 0x1 /* run the portable CUDA-core attention kernels even
+                                where a tensor-core kernel exists (verification aid) */
+
+/*
+ * Operator attributes and cache geometry (the PagedAttention node
+ * attributes num_heads, v_head_size, rotary_offset, do_rotary,
+ * rotary_interleaved, softcap, local_window_size and scale; paged_attention.rs
+ * PagedAttentionFactory::create and execute's geometry checks).
+ */
+typedef struct pa_latent_params {
+  int32_t dtype;              /* pa_dtype of query, key, key_cache, cos/sin, out     */
+  int32_t num_heads;          /* H >= 1 query heads (kv_num_heads is 1 in LATENT)    */
+  int32_t head_size;          /* hs: latent row width, multiple of 16, 16..1024      */
+  int32_t v_head_size;        /* vhs in 1..hs; 0 means hs                           */
+  int32_t rotary_offset;      /* first rotary channel, multiple of 8                 */
+  int32_t rotary_dim;         /* rd = 2 * cos_cache.dims[1]; 0 = no RoPE, else %16   */
+  int32_t rotary_interleaved; /* 0 = half-split pairs, 1 = adjacent pairs            */
+  int32_t cos_rows;           /* rows of cos/sin caches (largest position + 1)       */
+  int32_t block_size;         /* bs: power of two >= 16                              */
+  int32_t num_blocks;         /* physical blocks in key_cache                        */
+  int32_t max_blocks_per_seq; /* columns of block_table                              */
+  float scale;                /* > 0; 0 selects 1/sqrt(hs), allowed only if vhs==hs */
+  float softcap;              /* <= 0: off; else s = softcap*tanh(s/softcap)         */
+  int32_t local_window_size;  /* < 0: off; else keys with pos - j > window skipped   */
+  int32_t flags;              /* PA_FLAG_*                                           */
+} pa_latent_params;
+
+/* Checks the parameters alone (the first group of checks of every entry
+ * point). Returns PA_OK, PA_ERR_INVALID_ARGUMENT or PA_ERR_NOT_IMPLEMENTED. */
+pa_status pa_latent_validate(const pa_latent_params* p);
+
+/*
+ * Write phase — paged_attention.rs module doc "Write phase" and the device
+ * function write_impl: for every token t with slot_mapping[t] >= 0, the row
+ * key[t, :] gets partial RoPE on channels [rotary_offset, rotary_offset+rd)
+ * at the token's absolute position past[b] + (t - cumseq[b]) (b: the
+ * sequence with cumseq[b] <= t < cumseq[b+1]), is rounded to the dtype and
+ * stored at key_cache[slot_mapping[t], :]. Other channels are copied bit
+ * for bit; slot -1 skips the token.
+ *
+ *   key          [T, hs]                     input
+ *   cos_cache    [cos_rows, rd/2]            input (ignored when rd == 0)
+ *   sin_cache    [cos_rows, rd/2]            input (ignored when rd == 0)
+ *   slot_mapping int32 [T]                   input, block*bs + offset or -1
+ *   cumseq       int32 [B+1]                 input, cumseq[0]=0, cumseq[B]=T
+ *   past         int32 [B]                   input, context length minus q_len
+ *   key_cache    [num_blocks, bs, 1, hs]     updated in place
+ *   err_flags    int32 [1]                   device error bits (may be NULL)
+ * Two tokens naming the same slot race; the caller must not do that.
+ */
+pa_status pa_latent_write(const pa_latent_params* p, const void* key, int64_t num_tokens,
+                          const void* cos_cache, const void* sin_cache,
+                          const int32_t* slot_mapping, const int32_t* cumseq,
+                          const int32_t* past, int32_t num_seqs, void* key_cache,
+                          int32_t* err_flags, void* stream);
+
+/*
+ * Read phase for decode sequences — paged_attention.rs module doc "Read
+ * phase" and the device function attn_impl: for every token t of the
+ * sequences [seq_begin, seq_end) and every head h, q = RoPE(query[t,
+ * h*hs:(h+1)*hs]) at the token's position pos; keys j = 0..pos (minus
+ * those with pos - j > window when the window is on) are read from row
+ * block_table[b, j/bs]*bs + j%bs of key_cache; s_j = scale * q.K_j, then
+ * softcap*tanh(s_j/softcap) if softcap > 0; out[t, h*vhs:(h+1)*vhs] =
+ * sum_j softmax(s)_j K_j[:vhs], rounded to the dtype.
+ *
+ * Every sequence in [seq_begin, seq_end) must have exactly one new token
+ * (cumseq[b+1]-cumseq[b] == 1); a sequence that does not sets
+ * PA_DEVERR_DECODE_QLEN and its rows of `out` are left as they were.
+ * Keys are split across SMs and merged with a log-sum-exp combine, which
+ * uses the caller's workspace (pa_latent_workspace_size bytes, 256-byte
+ * aligned, contents need not be initialised, must not be shared with a
+ * concurrent call).
+ *
+ *   query        [T, H*hs]                   input
+ *   key_cache    [num_blocks, bs, 1, hs]     input (written by pa_latent_write)
+ *   block_table  int32 [B, max_blocks_per_seq] input, physical block ids
+ *   out          [T, H*vhs]                  output rows of the covered tokens
+ * Other arguments as for pa_latent_write.
+ */
+pa_status pa_latent_decode(const pa_latent_params* p, const void* query, int64_t num_tokens,
+                           const void* key_cache, const void* cos_cache,
+                           const void* sin_cache, const int32_t* cumseq,
+                           const int32_t* past, const int32_t* block_table,
+                           int32_t num_seqs, int32_t seq_begin, int32_t seq_end,
+                           void* workspace, size_t workspace_bytes, void* out,
+                           int32_t* err_flags, void* stream);
+
+/*
+ * Read phase for any sequences (same definition as pa_latent_decode, no
+ * restriction on q_len): the chunked-prefill form of attn_impl, where the
+ * new tokens of a sequence attend causally to each other through the cache
+ * rows pa_latent_write stored for them. Arguments as for pa_latent_decode.
+ */
+pa_status pa_latent_prefill(const pa_latent_params* p, const void* query, int64_t num_tokens,
+                            const void* key_cache, const void* cos_cache,
+                            const void* sin_cache, const int32_t* cumseq,
+                            const int32_t* past, const int32_t* block_table,
+                            int32_t num_seqs, int32_t seq_begin, int32_t seq_end,
+                            void* workspace, size_t workspace_bytes, void* out,
+                            int32_t* err_flags, void* stream);
+
+/* Bytes of workspace pa_latent_decode / pa_latent_prefill need for these
+ * parameters on the current device (0 if none). Host-only; returns 0 and
+ * records an error message for invalid parameters. */
+size_t pa_latent_workspace_size(const pa_latent_params* p, int32_t num_seqs,
+                                int64_t num_tokens);
+
+/* Which attention kernel family a decode (phase 0) or prefill (phase 1)
+ * call with these parameters runs: 0 = portable CUDA-core kernels,
+ * 1 = tcgen05/TMA tensor-core kernels, -1 = invalid parameters. */
+int32_t pa_latent_kernel_family(const pa_latent_params* p, int32_t phase);
+
+/* Static text for a status code. */
+const char* pa_latent_status_string(pa_status s);
+
+/* Message describing the last non-OK status returned on the calling thread
+ * (empty string if none). */
+const char* pa_latent_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_LATENT_H */

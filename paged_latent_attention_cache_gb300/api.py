@@ -1,0 +1,98 @@
+"""User-facing operator object over the C ABI.
+
+``PagedLatentAttention`` holds the operator parameters, the split-KV
+workspace and the device error word, all allocated once at construction;
+``forward`` then only enqueues the library's kernels (write phase, decode
+phase for the decode-first sequences, prefill phase for the rest) and is
+safe to record into a CUDA graph after one eager call.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class PagedLatentAttention:
+    def __init__(self, *, dtype: torch.dtype, num_heads: int, head_size: int,
+                 v_head_size: int = 0, rotary_offset: int = 0, rotary_dim: int = 0,
+                 rotary_interleaved: int = 0, cos_rows: int = 1, block_size: int,
+                 num_blocks: int, max_blocks_per_seq: int, scale: float = 0.0,
+                 softcap: float = 0.0, local_window_size: int = -1, max_seqs: int,
+                 max_tokens: int, device="cuda", portable: bool = False):
+        self.dtype = dtype
+        self.num_heads = num_heads
+        self.head_size = head_size
+        self.v_head_size = v_head_size or head_size
+        self.params = B.make_params(
+            dtype=dtype, num_heads=num_heads, head_size=head_size, v_head_size=v_head_size,
+            rotary_offset=rotary_offset, rotary_dim=rotary_dim,
+            rotary_interleaved=rotary_interleaved, cos_rows=cos_rows, block_size=block_size,
+            num_blocks=num_blocks, max_blocks_per_seq=max_blocks_per_seq, scale=scale,
+            softcap=softcap, local_window_size=local_window_size,
+            flags=B.PA_FLAG_PORTABLE if portable else 0)
+        s = B.pa_latent_validate(self.params)
+        if s != B.PA_OK:
+            raise B.PaError(s, B.last_error())
+        self.device = torch.device(device)
+        self.max_seqs, self.max_tokens = max_seqs, max_tokens
+        self.workspace = B.alloc_workspace(self.params, max_seqs, max_tokens, self.device)
+        self.err_flags = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    @classmethod
+    def from_workload(cls, w, device="cuda", portable=False) -> "PagedLatentAttention":
+        return cls(dtype=w.dtype, num_heads=w.num_heads, head_size=w.head_size,
+                   v_head_size=w.v_head_size, rotary_offset=w.rotary_offset,
+                   rotary_dim=w.rotary_dim, rotary_interleaved=w.rotary_interleaved,
+                   cos_rows=w.cos_rows, block_size=w.block_size, num_blocks=w.num_blocks,
+                   max_blocks_per_seq=w.max_blocks_per_seq, scale=w.scale, softcap=w.softcap,
+                   local_window_size=w.local_window_size, max_seqs=w.num_seqs,
+                   max_tokens=max(w.num_tokens, 1), device=device, portable=portable)
+
+    def kernel_family(self, phase: int) -> int:
+        return B.pa_latent_kernel_family(self.params, phase)
+
+    def write(self, key, cos_cache, sin_cache, slot_mapping, cumseq, past, key_cache,
+              stream=None):
+        B.pa_latent_write(self.params, key, cos_cache, sin_cache, slot_mapping, cumseq, past,
+                          key_cache, self.err_flags, stream)
+
+    def decode(self, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+               seq_begin=0, seq_end=None, stream=None):
+        B.pa_latent_decode(self.params, query, key_cache, cos_cache, sin_cache, cumseq, past,
+                           block_table, out, seq_begin, seq_end, self.workspace,
+                           self.err_flags, stream)
+
+    def prefill(self, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+                seq_begin=0, seq_end=None, stream=None):
+        B.pa_latent_prefill(self.params, query, key_cache, cos_cache, sin_cache, cumseq, past,
+                            block_table, out, seq_begin, seq_end, self.workspace,
+                            self.err_flags, stream)
+
+    def forward(self, query, key, key_cache, cos_cache, sin_cache, cumseq, past, block_table,
+                slot_mapping, num_decode_seqs: int, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        """Write phase over all tokens, then decode over sequences
+        [0, num_decode_seqs) and prefill over the rest; returns ``out``."""
+        T = query.shape[0]
+        nseq = past.shape[0]
+        if out is None:
+            out = torch.empty(T, self.num_heads * self.v_head_size, dtype=self.dtype,
+                              device=query.device)
+        self.write(key, cos_cache, sin_cache, slot_mapping, cumseq, past, key_cache, stream)
+        if num_decode_seqs > 0:
+            self.decode(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+                        0, num_decode_seqs, stream)
+        if num_decode_seqs < nseq:
+            self.prefill(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+                         num_decode_seqs, nseq, stream)
+        return out
+
+    def error_flags(self) -> int:
+        """Reads the device error word (synchronises with the device)."""
+        return int(self.err_flags.item())
+
+    def reset_error_flags(self):
+        self.err_flags.zero_()

@@ -1,0 +1,73 @@
+// Internal interface between the C-ABI entry points and the kernel
+// launchers. Not installed; the public interface is include/pa_latent.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "pa_latent.h"
+
+namespace pa {
+
+// Validated operator geometry with defaults resolved.
+struct Geometry {
+  int dtype;        // pa_dtype
+  int H;            // query heads
+  int hs;           // latent width
+  int vhs;          // value width (v_head_size, 0 resolved to hs)
+  int ro, rd;       // rotary offset / dim
+  int interleaved;  // 0 / 1
+  int cos_rows;
+  int bs;           // block size
+  int num_blocks;
+  int max_blocks;   // block_table columns
+  float scale;      // resolved (never 0)
+  float softcap;    // <= 0: off
+  int window;       // < 0: off
+  int flags;
+  int num_sms;      // SM count of the current device
+  int device;       // current device ordinal
+};
+
+enum class Phase { kDecode = 0, kPrefill = 1 };
+
+// ---- write phase (pa_write.cu)
+cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
+                         const void* cos_cache, const void* sin_cache,
+                         const int32_t* slot_mapping, const int32_t* cumseq, const int32_t* past,
+                         int32_t num_seqs, void* key_cache, int32_t* err_flags,
+                         cudaStream_t stream);
+
+// Arguments of one read-phase call.
+struct ReadArgs {
+  const void* query;
+  int64_t num_tokens;
+  const void* key_cache;
+  const void* cos_cache;
+  const void* sin_cache;
+  const int32_t* cumseq;
+  const int32_t* past;
+  const int32_t* block_table;
+  int32_t num_seqs, seq_begin, seq_end;
+  void* workspace;
+  size_t workspace_bytes;
+  void* out;
+  int32_t* err_flags;
+  cudaStream_t stream;
+};
+
+// ---- portable CUDA-core attention (pa_portable.cu)
+size_t portable_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs,
+                                int64_t num_tokens);
+// Workspace a call over nq queries (decode: sequences, prefill: tokens) needs.
+size_t portable_call_workspace(const Geometry& g, Phase ph, int64_t nq);
+cudaError_t launch_portable(const Geometry& g, Phase ph, const ReadArgs& a);
+
+// ---- tcgen05 / TMA attention (pa_tc.cu)
+bool tc_supported(const Geometry& g, Phase ph);
+size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t num_tokens);
+size_t tc_call_workspace(const Geometry& g, Phase ph, const ReadArgs& a);
+cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a);
+
+}  // namespace pa

@@ -1,0 +1,94 @@
+// Write phase: partial RoPE on each new latent key row, scattered into the
+// paged cache (paged_attention.rs, module doc "Write phase" / write_impl).
+//
+// One thread per (token, 8-channel group): a 16-byte load of the group, a
+// 16-byte load of its rotary partner group when the group is rotary, and a
+// 16-byte store into the cache row. Rows are 16-byte aligned (hs % 16 == 0)
+// so every access is a full vector; a warp covers 32 consecutive groups,
+// i.e. whole rows, so loads and stores are coalesced. HBM traffic is the
+// algorithmic minimum: each key row read once (plus its 128-byte rotary
+// partner slice, which hits L1), each written row stored once.
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+template <typename T>
+__global__ void __launch_bounds__(256)
+latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
+                    const T* __restrict__ sin_cache, const int32_t* __restrict__ slot_mapping,
+                    const int32_t* __restrict__ cumseq, const int32_t* __restrict__ past,
+                    int32_t num_seqs, T* __restrict__ key_cache, int64_t num_tokens, int hs,
+                    int ro, int rd, int interleaved, int cos_rows, int64_t num_slots,
+                    int32_t* err_flags) {
+  const int groups = hs >> 3;
+  const int64_t total = num_tokens * groups;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / groups;
+    const int g = (int)(i - t * groups);
+    const int32_t slot = slot_mapping[t];
+    if (slot < 0) {
+      if (slot < -1 && g == 0) raise_flag(err_flags, PA_DEVERR_SLOT);
+      continue;
+    }
+    if ((int64_t)slot >= num_slots) {
+      if (g == 0) raise_flag(err_flags, PA_DEVERR_SLOT);
+      continue;
+    }
+    int32_t b;
+    int64_t pos;
+    if (!locate_token(t, cumseq, past, num_seqs, g == 0 ? err_flags : nullptr, &b, &pos))
+      continue;
+    if (rd > 0 && (pos < 0 || pos >= cos_rows)) {  // whole row skipped
+      if (g == 0) raise_flag(err_flags, pos < 0 ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
+      continue;
+    }
+    const T* row = key + t * hs;
+    const int d0 = g << 3;
+    uint4 v = *reinterpret_cast<const uint4*>(row + d0);
+    if (rd > 0 && d0 >= ro && d0 < ro + rd) {
+      float x[8], xp[8];
+      unpack8<T>(v, x);
+      if (!interleaved) {
+        const int half = rd >> 1;
+        const int dp = (d0 - ro < half) ? d0 + half : d0 - half;
+        unpack8<T>(*reinterpret_cast<const uint4*>(row + dp), xp);
+      }
+      const T* crow = cos_cache + pos * (rd >> 1);
+      const T* srow = sin_cache + pos * (rd >> 1);
+      rope8<T>(x, xp, d0, ro, rd, interleaved, crow, srow);
+      v = pack8<T>(x);
+    }
+    *reinterpret_cast<uint4*>(key_cache + (int64_t)slot * hs + d0) = v;
+  }
+}
+
+cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
+                         const void* cos_cache, const void* sin_cache,
+                         const int32_t* slot_mapping, const int32_t* cumseq, const int32_t* past,
+                         int32_t num_seqs, void* key_cache, int32_t* err_flags,
+                         cudaStream_t stream) {
+  const int64_t total = num_tokens * (g.hs >> 3);
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  const int64_t cap = (int64_t)g.num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  const int64_t num_slots = (int64_t)g.num_blocks * g.bs;
+  if (g.dtype == PA_DTYPE_BF16) {
+    latent_write_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
+        (const __nv_bfloat16*)key, (const __nv_bfloat16*)cos_cache,
+        (const __nv_bfloat16*)sin_cache, slot_mapping, cumseq, past, num_seqs,
+        (__nv_bfloat16*)key_cache, num_tokens, g.hs, g.ro, g.rd, g.interleaved, g.cos_rows,
+        num_slots, err_flags);
+  } else {
+    latent_write_kernel<__half><<<(unsigned)blocks, threads, 0, stream>>>(
+        (const __half*)key, (const __half*)cos_cache, (const __half*)sin_cache, slot_mapping,
+        cumseq, past, num_seqs, (__half*)key_cache, num_tokens, g.hs, g.ro, g.rd,
+        g.interleaved, g.cos_rows, num_slots, err_flags);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace pa

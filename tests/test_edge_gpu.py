@@ -1,0 +1,165 @@
+"""GPU edge cases: option variants, odd geometries, empty and ragged
+batches, device error flags, determinism and CUDA-graph capture/replay."""
+import numpy as np
+import pytest
+import torch
+
+from paged_latent_attention_cache_gb300 import binding as B
+from paged_latent_attention_cache_gb300 import workloads as W
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, portable=False, tokens=None, default_scale=False):
+    got = Hn.run_gpu(w, portable=portable, scale=0.0 if default_scale else None)
+    ref = Hn.run_oracle(w, tokens)
+    assert got["flags"] == 0, hex(got["flags"])
+    Hn.check_cache(w, got["cache"], ref["cache"])
+    Hn.check_out(w, got["out"], ref["out"], tokens)
+    return got
+
+
+VARIANTS = {
+    "interleaved": dict(rotary_interleaved=1),
+    "no_rotary": dict(rotary_dim=0, rotary_offset=0),
+    "vhs_eq_hs_default_scale": dict(v_head_size=192, scale=0.0),
+    "odd_vhs": dict(v_head_size=40),
+    "heads_6": dict(num_heads=6),
+    "bs_32": dict(block_size=32),
+    "bs_256": dict(block_size=256),
+    "window_0": dict(local_window_size=0),
+    "window_5": dict(local_window_size=5),
+    "window_huge": dict(local_window_size=1 << 20),
+    "softcap_3": dict(softcap=3.0),
+    "fp16": dict(dtype=torch.float16),
+    "rotary_at_0": dict(rotary_offset=0, rotary_dim=32),
+}
+
+
+@pytest.mark.parametrize("portable", [False, True], ids=["default", "portable"])
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+def test_variant(name, portable):
+    kw = dict(num_heads=4, **W.GLM, block_size=16, seed=21, drop_slots=2)
+    kw.update(VARIANTS[name])
+    default_scale = kw.pop("scale", None) == 0.0
+    w = W.make_workload(name, q_lens=[1, 1, 9, 0, 33], past_lens=[70, 0, 40, 5, 3], **kw)
+    _check(w, portable, default_scale=default_scale)
+
+
+@pytest.mark.parametrize("hs,vhs,ro,rd,H", [(64, 64, 0, 0, 2), (576, 512, 512, 64, 16),
+                                            (256, 200, 128, 128, 3), (1024, 512, 960, 64, 2)])
+def test_geometries(hs, vhs, ro, rd, H):
+    w = W.make_workload("geo", q_lens=[1, 17], past_lens=[100, 30], num_heads=H, head_size=hs,
+                        v_head_size=vhs, rotary_offset=ro, rotary_dim=rd, block_size=16,
+                        seed=22, scale=0.08)
+    _check(w)
+
+
+def test_long_decode_splits():
+    """Long contexts (many key splits merged by the combine step)."""
+    w = W.make_workload("long", q_lens=[1, 1, 1], past_lens=[20000, 3, 777], num_heads=16,
+                        **W.GLM, block_size=64, seed=23)
+    _check(w)
+    _check(w, portable=True)
+
+
+def test_empty_batch_is_a_no_op():
+    w = W.make_workload("empty", q_lens=[0, 0], past_lens=[3, 4], num_heads=2, **W.GLM,
+                        block_size=16, seed=24)
+    d = w.to("cuda")
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    op = PagedLatentAttention.from_workload(w)
+    cache = d.key_cache.clone()
+    out = torch.empty(0, 2 * 128, dtype=w.dtype, device="cuda")
+    op.forward(d.query, d.key, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+               d.block_table, d.slot_mapping, 0, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(cache, d.key_cache) and op.error_flags() == 0
+
+
+def test_deterministic_and_graph_replay_bit_equal():
+    """Capture write + decode + prefill in one CUDA graph; 3 replays are bit
+    equal to the eager result (the pages' capture + 3 replays gate)."""
+    w = W.tiny()
+    d = w.to("cuda")
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    op = PagedLatentAttention.from_workload(w)
+    base = d.key_cache.clone()
+    cache = base.clone()
+    out = torch.empty(w.num_tokens, w.num_heads * w.v_head_size, dtype=w.dtype, device="cuda")
+    args = (d.query, d.key, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past, d.block_table,
+            d.slot_mapping, w.num_decode_seqs)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        op.forward(*args, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    eager_out, eager_cache = out.clone(), cache.clone()
+    cache.copy_(base)
+    op.forward(*args, out=out)
+    assert torch.equal(out, eager_out) and torch.equal(cache, eager_cache)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        op.forward(*args, out=out)
+    for _ in range(3):
+        cache.copy_(base)
+        out.fill_(0)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager_out) and torch.equal(cache, eager_cache)
+    assert op.error_flags() == 0
+
+
+def _flag_case(mutate, expect_bit, phase="both"):
+    w = W.make_workload("flags", q_lens=[1, 4], past_lens=[30, 10], num_heads=4, **W.GLM,
+                        block_size=16, seed=25, cos_rows=64)
+    mutate(w)
+    got = Hn.run_gpu(w)
+    assert got["flags"] & expect_bit, hex(got["flags"])
+    return w, got
+
+
+def test_flag_slot_out_of_range():
+    def m(w):
+        w.slot_mapping[2] = w.num_blocks * w.block_size + 5
+    w, got = _flag_case(m, B.PA_DEVERR_SLOT)
+
+
+def test_flag_bad_block_zeroes_rows():
+    def m(w):
+        w.block_table[1, 0] = -1           # a block the prefill sequence reads
+    w, got = _flag_case(m, B.PA_DEVERR_BLOCK)
+    vals = got["out"][1:5]
+    assert np.all(vals == 0)               # rows of the affected sequence are zero
+
+
+def test_flag_position_beyond_cos_cache():
+    def m(w):
+        w.past[0] = 100                    # cos_rows is 64
+    _flag_case(m, B.PA_DEVERR_POSITION)
+
+
+def test_flag_decode_qlen():
+    w = W.make_workload("flags", q_lens=[2, 4], past_lens=[30, 10], num_heads=4, **W.GLM,
+                        block_size=16, seed=26)
+    w.num_decode_seqs = 1                  # sequence 0 has 2 tokens: not a decode
+    got = Hn.run_gpu(w)
+    assert got["flags"] & B.PA_DEVERR_DECODE_QLEN
+    rows = got["out"]
+    from oracle import pa_oracle as O
+    f = O.bits_to_f64(rows, "bf16")
+    assert np.isnan(f[0:2]).all()          # rows of the rejected sequence untouched
+    assert np.isfinite(f[2:]).all()        # the prefill sequence still ran
+
+
+def test_flag_cumseq_short():
+    def m(w):
+        w.cumseq[-1] = w.cumseq[-1] - 1    # last token lies beyond cumseq[B]
+    _flag_case(m, B.PA_DEVERR_CUMSEQ)
+
+
+def test_flag_context_beyond_block_table():
+    def m(w):
+        w.past[1] = w.max_blocks_per_seq * w.block_size   # cos_rows too small as well
+    w, got = _flag_case(m, B.PA_DEVERR_CONTEXT | B.PA_DEVERR_POSITION)
