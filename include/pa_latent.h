@@ -70,6 +70,8 @@ typedef enum pa_dtype {
 #define PA_DEVERR_CUMSEQ      0x08 /* cumseq not monotone, cumseq[0]!=0 or cumseq[B]!=T */
 #define PA_DEVERR_DECODE_QLEN 0x10 /* pa_latent_decode saw a sequence with q_len != 1 */
 #define PA_DEVERR_CONTEXT     0x20 /* past < 0 or context > max_blocks_per_seq*bs  */
+#define PA_DEVERR_TIMEOUT     0x40 /* an internal pipeline wait exceeded its bound;
+                                      the affected rows were not written          */
 
 /* pa_latent_params.flags */
 #define PA_FLAG_PORTABLE 0x1 /* run the portable CUDA-core attention kernels even

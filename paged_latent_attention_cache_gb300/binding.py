@@ -34,6 +34,7 @@ PA_DEVERR_POSITION = 0x04
 PA_DEVERR_CUMSEQ = 0x08
 PA_DEVERR_DECODE_QLEN = 0x10
 PA_DEVERR_CONTEXT = 0x20
+PA_DEVERR_TIMEOUT = 0x40
 
 PA_FLAG_PORTABLE = 0x1
 

@@ -39,6 +39,9 @@ def test_workload_parity(name, portable, oracle_results):
     got = Hn.run_gpu(w, portable=portable)
     ref = _oracle(oracle_results, name)
     assert got["flags"] == 0
+    # the default path of every named workload is the tensor-core kernel
+    expect = 0 if portable else 1
+    assert got["op"].kernel_family(0) == expect and got["op"].kernel_family(1) == expect
     Hn.check_cache(w, got["cache"], ref["cache"])
     Hn.check_out(w, got["out"], ref["out"])
 
