@@ -10,10 +10,11 @@ token per sequence, contexts uniform in [1024, 8192], bs=64).
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl reference] [--portable]
 
-Timing: W untimed steps, then K timed steps bracketed by a barrier and a
-device synchronise; each step is timed with CUDA events on the launching
-stream and L2 is flushed (a write of 2x the L2 size) before every step,
-outside the events. Under torchrun each rank runs its own seeded batch
+Timing: W untimed eager steps, then the step is captured in a CUDA graph
+and K graph replays are timed, bracketed by a barrier and a device
+synchronise; each replay is timed with CUDA events on the launching stream
+and L2 is flushed (a write of 2x the L2 size) before every replay, outside
+the events. A second loop replays one graph per phase for the breakdown. Under torchrun each rank runs its own seeded batch
 (weak scaling, no collective on the data path) and the max over ranks is
 reported. `value` is algorithmic latent-cache bytes per second (TB/s);
 `e2e` is the same metric through the operator object with the step's inputs
@@ -220,21 +221,45 @@ def build_workload(name: str, seed_offset: int):
     return fn(seed=default_seed + seed_offset)
 
 
-def count_launches(step_fn):
-    """Kernels of this library launched by one step, counted by the torch
-    profiler (CUPTI); None if the profiler is unavailable."""
+def make_graph(fn, keep=False):
+    """Captures fn() into a CUDA graph; with keep=True the cudaGraph_t is kept
+    so its nodes can be inspected (falls back to a plain graph)."""
     import torch
+    g = None
+    if keep:
+        try:
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+        except TypeError:
+            g = None
+    if g is None:
+        g = torch.cuda.CUDAGraph()
+        keep = False
+    with torch.cuda.graph(g):
+        fn()
+    if keep:
+        g.instantiate()
+    return g, keep
+
+
+def graph_kernel_nodes(g):
+    """Kernel nodes in a captured graph (the launches of one replay), read
+    through the driver API; None if unavailable."""
+    import ctypes
     try:
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            step_fn()
-            torch.cuda.synchronize()
-        n = 0
-        for e in prof.events():
-            name = e.name or ""
-            if ("pa::" in name or "_ZN2pa" in name) and "kernel" in name:
-                n += 1
-        return n
+        cu = ctypes.CDLL("libcuda.so.1")
+        h = ctypes.c_void_p(g.raw_cuda_graph())
+        n = ctypes.c_size_t(0)
+        if cu.cuGraphGetNodes(h, None, ctypes.byref(n)) != 0:
+            return None
+        nodes = (ctypes.c_void_p * n.value)()
+        if cu.cuGraphGetNodes(h, nodes, ctypes.byref(n)) != 0:
+            return None
+        cnt = 0
+        for nd in nodes:
+            t = ctypes.c_int(-1)
+            cu.cuGraphNodeGetType(ctypes.c_void_p(nd), ctypes.byref(t))
+            cnt += 1 if t.value == 0 else 0   # CU_GRAPH_NODE_TYPE_KERNEL
+        return cnt
     except Exception:
         return None
 
@@ -255,33 +280,44 @@ def run_gpu_arm(args, rank, world, device):
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def write():
         op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
-        if ev is not None:
-            ev[1].record(stream)
+
+    def decode():
         if nd > 0:
             op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
                       d.block_table, out, 0, nd)
-        if ev is not None:
-            ev[2].record(stream)
+
+    def prefill():
         if nd < w.num_seqs:
             op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
                        d.block_table, out, nd, w.num_seqs)
-        if ev is not None:
-            ev[3].record(stream)
 
-    for _ in range(max(args.warmup, 3)):
+    def step():
+        write()
+        decode()
+        prefill()
+
+    for _ in range(max(args.warmup, 3)):   # eager warm-up (also configures kernels)
         flush.zero_()
         step()
     torch.cuda.synchronize(device)
-    launches_per_step = count_launches(step)
     if op.error_flags() != 0:
         raise RuntimeError(f"device error flags {op.error_flags():#x}")
+    # One graph for the whole step (the timed unit) and one per phase (the
+    # breakdown and the dominant call's duration).
+    g_step, kept = make_graph(step, keep=True)
+    launches_per_step = graph_kernel_nodes(g_step) if kept else None
+    g_phase = [make_graph(f)[0] for f in (write, decode, prefill)]
+    for _ in range(3):
+        flush.zero_()
+        g_step.replay()
+        for gp in g_phase:
+            gp.replay()
+    torch.cuda.synchronize(device)
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     gpu_index = device.index
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
     if vis:
@@ -297,16 +333,27 @@ def run_gpu_arm(args, rank, world, device):
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
-        step(evs[i])
+        evs[i][0].record(stream)
+        g_step.replay()
+        evs[i][1].record(stream)
     torch.cuda.synchronize(device)
     barrier(device)
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
+    # per-phase breakdown (separate loop, same flushing)
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        pev[i][0].record(stream)
+        for j, gp in enumerate(g_phase):
+            gp.replay()
+            pev[i][j + 1].record(stream)
+    torch.cuda.synchronize(device)
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
-    write_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    pre_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    write_ms = [e[0].elapsed_time(e[1]) for e in pev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in pev]
+    pre_ms = [e[2].elapsed_time(e[3]) for e in pev]
     ms_per_step = reduce_max(sum(step_ms) / K, device)
 
     # End to end through the operator object: H2D of the step's inputs from
@@ -417,6 +464,7 @@ def main(argv=None):
                        "rotary": [w.rotary_offset, w.rotary_dim], "block_size": w.block_size,
                        "num_seqs": w.num_seqs, "num_tokens": w.num_tokens,
                        "l2": "flushed before every step (write of 2x L2)",
+                       "timing": "CUDA graph of the step, CUDA events per replay",
                        "parallelism": f"replicas x{world} (independent batches per rank)",
                        "kernels": "portable" if args.portable else
                        ("tcgen05" if res["family"][0] == 1 else "portable")},

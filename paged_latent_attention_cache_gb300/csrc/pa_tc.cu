@@ -40,7 +40,6 @@ namespace tc {
 
 constexpr int kThreads = 192;
 constexpr int kRows = 128;               // MMA M: TMEM lanes
-constexpr uint32_t kSpinLimit = 1u << 24;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (factor 256)
 
@@ -59,16 +58,6 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
 }
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -157,6 +146,37 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// 32 consecutive columns without waiting; pair with tmem_wait_ld() and
+// reg_fence() before the registers are read.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// Orders later uses of r after the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
+                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+// Programmatic dependent launch controls (no-ops for an ordinary launch).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -176,6 +196,28 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Optional timeline trace (compiled only with -DPA_TC_TRACE): %globaltimer
+// stamps at phase boundaries per CTA, read back by a debug entry point.
+#ifdef PA_TC_TRACE
+__device__ unsigned long long g_trace[8192][16];
+__device__ __forceinline__ void trace(int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (blockIdx.x < 8192) g_trace[blockIdx.x][slot] = t;
+}
+__device__ unsigned long long g_trace_tile[256][8];
+__device__ __forceinline__ void trace_tile(int k, int slot) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (blockIdx.x == 0 && k < 256) g_trace_tile[k][slot] = t;
+}
+#define PA_TRACE(slot) trace(slot)
+#define PA_TRACE_TILE(k, slot) trace_tile(k, slot)
+#else
+#define PA_TRACE(slot) ((void)0)
+#define PA_TRACE_TILE(k, slot) ((void)0)
+#endif
+
 // ---------------------------------------------------------------------------
 // Parameters
 // ---------------------------------------------------------------------------
@@ -184,6 +226,7 @@ struct Params {
   void* out;
   float* ws_o;      // [units][G][128][VG]   (key-split partials, decode)
   float* ws_ml;     // [units][G][128][2]    (log2-domain max, denominator)
+  int2* ws_plan;    // [nseq] (first unit, number of key splits) per decode sequence
   const void* cos_cache;
   const void* sin_cache;
   const int32_t* cumseq;
@@ -199,49 +242,93 @@ struct Params {
   float cap_out;     // softcap * log2(e)
   int softcap_on;
   int window;
-  int splits;        // key splits per decode token (1: write the output directly)
+  int units;         // decode: CTA units (per value group) the grid provides
   int decode;
   int box_rows;      // rows per TMA box: min(N, bs)
 };
 
-template <int HS, int VG, int G, int N, int STAGES>
+// QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
+// MMA then reads rows 64-127 from the next slab, rows that are never stored).
+template <int HS, int VG, int G, int N, int STAGES, int QR>
 struct Cfg {
   static constexpr int kBoxes = HS / 64;                  // 64-channel slabs
-  static constexpr int kQBytes = kRows * HS * 2;
-  static constexpr int kQBox = kRows * 128;                // bytes per Q slab
+  static constexpr int kQBytes = QR * HS * 2;
+  static constexpr int kQBox = QR * 128;                   // bytes per Q slab
   static constexpr int kKBox = N * 128;                    // bytes per K slab
   static constexpr int kStageBytes = N * HS * 2;
   static constexpr int kSmemData = kQBytes + STAGES * kStageBytes;
-  // TMEM columns: O | S0 | S1 | P0 | P1
+  // TMEM columns: O | S0 | S1 | P0 | P1   (P is 16-bit: N/2 columns each)
   static constexpr int kColO = 0;
   static constexpr int kColS = VG;
   static constexpr int kColP = VG + 2 * N;
-  static constexpr int kCols = VG + 2 * N + N;  // P is 16-bit: N/2 columns x 2 buffers
+  static constexpr int kCols = VG + 2 * N + N;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
                                    : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM budget");
-  static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 256, "shape");
+  static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 128, "shape");
+  static_assert(STAGES <= 8, "stages");
+  static_assert(QR == 64 || QR == 128, "query rows");
 };
 
 struct Barriers {
   uint64_t full[8], empty[8];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t q_full;
+  uint64_t q_tma, q_full;
   uint64_t drain;
   uint32_t tmem_base;
   int bad;
   int abort;
 };
 
-// Bounded wait on an mbarrier phase: non-blocking polls, then polls with a
-// short sleep; about a second in total before giving up. Returns false (and
-// marks the CTA aborted) on expiry or when another role already aborted.
+// Resolved work of one CTA (written by warp 0 during the prologue).
+struct Work {
+  int64_t t, pos, t_begin, t_end;
+  int b, splits, first, split;
+  int status;  // 0 = run, 1 = idle, 2 = error already reported (write nothing more)
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// Non-blocking probe (used where one thread polls several barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase. try_wait lets the hardware suspend the
+// thread while the phase is pending (no issue slots burnt); the wait gives
+// up after about a second of %globaltimer time, or as soon as another role
+// of the CTA has aborted, and then returns false.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
                                          int32_t* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort) return false;
-    if (i >= 4096u) __nanosleep(32);
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) break;
+    }
   }
   *abort = 1;
   raise_flag(err, PA_DEVERR_TIMEOUT);
@@ -250,9 +337,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // Bounded wait used while tearing down: ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* err) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (mbar_test_wait(bar, parity)) return;
-    if (i >= 4096u) __nanosleep(32);
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) break;
   }
   raise_flag(err, PA_DEVERR_TIMEOUT);
 }
@@ -271,13 +359,123 @@ __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
 }
 
 // ---------------------------------------------------------------------------
+// Decode work plan. Each valid decode sequence has n_b key tiles; it is cut
+// into c_b(T) = ceil(n_b / T) splits of at most T tiles, T being the smallest
+// split length for which all splits fit in the grid's units. Invalid
+// sequences (q_len != 1, out-of-range position) get one unit, which only
+// reports the error. Every CTA derives the same plan from past_seqlens with
+// one warp (lane-strided sequences, shuffle reductions), so no host round
+// trip or separate planning launch is needed.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int64_t decode_tiles(const Params& P, int b, int n_tile) {
+  const int32_t q0 = P.cumseq[b], q1 = P.cumseq[b + 1];
+  if (q1 - q0 != 1 || q0 < 0 || q0 >= P.num_tokens) return 0;
+  const int64_t pos = P.past[b];
+  if (pos < 0 || pos >= (int64_t)P.max_blocks * P.bs || (P.rd > 0 && pos >= P.cos_rows)) return 0;
+  const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+  return pos / n_tile - lo / n_tile + 1;
+}
+
+__device__ __forceinline__ int64_t splits_of(int64_t tiles, int64_t T) {
+  // 32-bit division: tile counts and split lengths stay far below 2^31
+  return tiles <= 0 ? 1 : (int64_t)(((uint32_t)tiles + (uint32_t)T - 1u) / (uint32_t)T);
+}
+
+__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Run by one full warp; returns the unit's plan in every lane.
+template <int N>
+__device__ Work decode_plan_warp(const Params& P, int unit) {
+  constexpr int kCache = 8;  // sequences per lane kept in registers
+  const int lane = threadIdx.x & 31;
+  const int nseq = P.seq_end - P.seq_begin;
+  const int chunk = (nseq + 31) / 32;
+  const int c0 = min(nseq, lane * chunk), c1 = min(nseq, c0 + chunk);
+  int64_t tl[kCache];
+#pragma unroll
+  for (int i = 0; i < kCache; ++i)
+    tl[i] = (c0 + i < c1) ? decode_tiles(P, P.seq_begin + c0 + i, N) : 0;
+  auto tiles_at = [&](int i) -> int64_t {
+    const int k = i - c0;
+    if (k < kCache) {
+      int64_t v = 0;
+#pragma unroll
+      for (int q = 0; q < kCache; ++q) v = (q == k) ? tl[q] : v;
+      return v;
+    }
+    return decode_tiles(P, P.seq_begin + i, N);
+  };
+  int64_t mx = 1;
+  for (int i = c0; i < c1; ++i) mx = max(mx, tiles_at(i));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int64_t lo = 1, hi = mx;
+  while (lo < hi) {  // smallest T with sum_b splits_of(n_b, T) <= units
+    const int64_t mid = (lo + hi) >> 1;
+    int64_t cnt = 0;
+    for (int i = c0; i < c1; ++i) cnt += splits_of(tiles_at(i), mid);
+    if (warp_sum64(cnt) <= P.units) hi = mid; else lo = mid + 1;
+  }
+  const int64_t T = lo;
+  int64_t mine = 0;
+  for (int i = c0; i < c1; ++i) mine += splits_of(tiles_at(i), T);
+  int64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int64_t run = incl - mine;
+  Work w;
+  w.status = 1;
+  w.b = -1;
+  int hit = 0;
+  for (int i = c0; i < c1; ++i) {
+    const int64_t tiles = tiles_at(i);
+    const int64_t c = splits_of(tiles, T);
+    if (unit >= run && unit < run + c) {
+      hit = 1;
+      w.b = P.seq_begin + i;
+      w.split = (int)(unit - run);
+      w.splits = (int)c;
+      w.first = (int)run;
+      w.t_begin = w.t_end = 0;
+      if (tiles > 0) {
+        const int64_t pos = P.past[w.b];
+        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        w.t_begin = lo_key / N + (int64_t)w.split * T;
+        w.t_end = min(pos / N + 1, w.t_begin + T);
+      }
+    }
+    run += c;
+  }
+  const unsigned who = __ballot_sync(0xffffffffu, hit);
+  if (who == 0) return w;  // idle unit
+  const int src = __ffs(who) - 1;
+  w.b = __shfl_sync(0xffffffffu, w.b, src);
+  w.split = __shfl_sync(0xffffffffu, w.split, src);
+  w.splits = __shfl_sync(0xffffffffu, w.splits, src);
+  w.first = __shfl_sync(0xffffffffu, w.first, src);
+  w.t_begin = __shfl_sync(0xffffffffu, w.t_begin, src);
+  w.t_end = __shfl_sync(0xffffffffu, w.t_end, src);
+  w.status = 0;
+  return w;
+}
+
+// ---------------------------------------------------------------------------
 // The attention kernel
 // ---------------------------------------------------------------------------
-template <typename T, int HS, int VG, int G, int N, int STAGES>
+template <typename T, int HS, int VG, int G, int N, int STAGES, int QR>
 __global__ void __launch_bounds__(kThreads, 1)
-tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ Params P) {
-  using C = Cfg<HS, VG, G, N, STAGES>;
+tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+               const __grid_constant__ Params P) {
+  using C = Cfg<HS, VG, G, N, STAGES, QR>;
   extern __shared__ uint8_t smem_raw[];
+  __shared__ Work work;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   uint8_t* q_s = smem;
@@ -286,69 +484,68 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x % G;            // value-channel group
-  const int64_t unit = blockIdx.x / G;
-
-  // ---- resolve the query token, its sequence and key range (uniform) ----
-  int64_t t, pos;
-  int32_t b;
-  int split = 0;
-  int64_t x = unit;
-  if (P.decode) {
-    x = unit / P.splits;
-    split = (int)(unit % P.splits);
-    b = P.seq_begin + (int32_t)x;
-    const int32_t q0 = P.cumseq[b], q1 = P.cumseq[b + 1];
-    if (q1 - q0 != 1) {
-      if (tid == 0 && g == 0 && split == 0) raise_flag(P.err_flags, PA_DEVERR_DECODE_QLEN);
-      return;
-    }
-    if (q0 < 0 || q0 >= P.num_tokens) {
-      if (tid == 0 && g == 0 && split == 0) raise_flag(P.err_flags, PA_DEVERR_CUMSEQ);
-      return;
-    }
-    t = q0;
-    pos = P.past[b];
-  } else {
-    if (!locate_token(unit, P.cumseq, P.past, P.num_seqs,
-                      (tid == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos))
-      return;
-    if (b < P.seq_begin || b >= P.seq_end) return;
-    t = unit;
-  }
+  const int unit = blockIdx.x / G;
   const int vhs = P.vhs;
-  T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
-  const bool bad_ctx = P.past[b] < 0 || pos >= (int64_t)P.max_blocks * P.bs;
-  const bool bad_pos = P.rd > 0 && pos >= P.cos_rows;
-  if (bad_ctx || bad_pos) {
-    if (tid == 0 && g == 0 && split == 0)
-      raise_flag(P.err_flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
-    if (split == 0)
-      for (int i = tid; i < P.H * VG; i += kThreads) {
-        const int h = i / VG, c = i % VG;
-        out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
-      }
-    return;
-  }
-  const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-  const int64_t tile_first = lo / N, tile_last = pos / N;
-  const int64_t ntiles_all = tile_last - tile_first + 1;
-  const int64_t per = (ntiles_all + P.splits - 1) / P.splits;
-  const int64_t t_begin = tile_first + (int64_t)split * per;
-  const int64_t t_end = min(tile_last + 1, t_begin + per);
-  const int n = (int)max((int64_t)0, t_end - t_begin);
-  const int64_t part = (x * P.splits + split) * G + g;  // partial slot (decode splits)
+  if (tid == 0) PA_TRACE(0);
 
-  if (n == 0) {  // an empty key split contributes nothing
-    if (P.splits > 1)
-      for (int r = tid; r < kRows; r += kThreads) {
-        P.ws_ml[(part * kRows + r) * 2 + 0] = -INFINITY;
-        P.ws_ml[(part * kRows + r) * 2 + 1] = 0.f;
+  // ---- prologue: warp 0 resolves the work while warps 1/5 set up ----
+  // With programmatic dependent launch this CTA may start while the previous
+  // kernel on the stream is still running: nothing reads inputs or writes
+  // outputs before griddepcontrol.wait returns. Dependents (the split
+  // combine) are released only when this CTA reaches its epilogue, so their
+  // waiting CTAs do not share the SM with the main loop.
+  if (warp == 0) {
+    grid_dep_wait();
+    Work w;
+    if (P.decode) {
+      w = decode_plan_warp<N>(P, unit);
+      if (w.status == 0) {
+        const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
+        if (lane == 0 && w.split == 0 && g == 0) P.ws_plan[w.b - P.seq_begin] = make_int2(w.first, w.splits);
+        if (q1 - q0 != 1) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_DECODE_QLEN);
+          w.status = 2;
+        } else if (q0 < 0 || q0 >= P.num_tokens) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_CUMSEQ);
+          w.status = 2;
+        } else {
+          w.t = q0;
+          w.pos = P.past[w.b];
+        }
       }
-    return;
-  }
-
-  // ---- setup: barriers, TMEM ----
-  if (tid == 0) {
+    } else {
+      int32_t b;
+      int64_t pos;
+      w.status = 1;
+      w.splits = 1;
+      if (locate_token(unit, P.cumseq, P.past, P.num_seqs,
+                       (lane == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos) &&
+          b >= P.seq_begin && b < P.seq_end) {
+        w.status = 0;
+        w.b = b;
+        w.t = unit;
+        w.pos = pos;
+        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        w.t_begin = lo_key / N;
+        w.t_end = pos / N + 1;
+      }
+    }
+    if (w.status == 0) {
+      const bool bad_ctx = P.past[w.b] < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
+      const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
+      if (bad_ctx || bad_pos) {
+        if (lane == 0 && g == 0)
+          raise_flag(P.err_flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
+        T* out_row = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs;
+        for (int i = lane; i < P.H * VG; i += 32) {
+          const int h = i / VG, c = i % VG;
+          out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
+        }
+        w.status = 2;
+      }
+    }
+    if (lane == 0) work = w;
+  } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
@@ -359,356 +556,436 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       mbar_init(smem_u32(&bars->p_full[i]), kRows);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
+    mbar_init(smem_u32(&bars->q_tma), 1);
     mbar_init(smem_u32(&bars->q_full), kRows);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->bad = 0;
     bars->abort = 0;
     fence_barrier_init();
-  }
-  if (warp == 5) {
+  } else if (warp == 4 && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&qmap);
+  } else if (warp == 5) {
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) prefetch_tmap(&kmap);
+  if (warp != 0) grid_dep_wait();  // every thread is ordered after the previous grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
+  const Work W = work;
+  if (tid == 0) PA_TRACE(1);
 
-  if (warp < 4) {
-    // =================== softmax / epilogue warps ===================
-    const int row = tid;  // TMEM lane == head
-    // Q with RoPE into the 128B-swizzled K-major layout: slab s holds
-    // channels [64s, 64s+64); row r's 16-byte chunk c sits at chunk c ^ (r&7).
-    {
-      const T* q = reinterpret_cast<const T*>(P.query) + t * (int64_t)P.H * HS;
-      const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
-      const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
-      constexpr int kChunks = HS / 8;
-      for (int i = tid; i < kRows * kChunks; i += 128) {
-        const int r = i / kChunks, c = i - r * kChunks;
-        const int d0 = c * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < P.H) {
-          const T* qr = q + (int64_t)r * HS;
-          v = *reinterpret_cast<const uint4*>(qr + d0);
-          if (P.rd > 0 && d0 >= P.ro && d0 < P.ro + P.rd) {
-            float xv[8], xp[8];
-            unpack8<T>(v, xv);
-            if (!P.interleaved) {
-              const int half = P.rd >> 1;
-              const int dp = (d0 - P.ro < half) ? d0 + half : d0 - half;
-              unpack8<T>(*reinterpret_cast<const uint4*>(qr + dp), xp);
-            }
-            rope8<T>(xv, xp, d0, P.ro, P.rd, P.interleaved, crow, srow);
-            v = pack8<T>(xv);
+  if (W.status == 0) {
+    const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
+    const int32_t b = W.b;
+    const int splits = W.splits;
+    const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    const int n = (int)max((int64_t)0, W.t_end - t_begin);
+    const int64_t part = (int64_t)unit * G + g;  // partial slot (decode splits)
+    T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
+
+    if (warp < 4) {
+      // =================== softmax / epilogue warps ===================
+      const int row = tid;                 // TMEM lane == head
+      const bool live = warp * 32 < P.H;   // warp holds at least one real head
+      // Q arrives by TMA in the 128B-swizzled K-major layout (slab s holds
+      // channels [64s, 64s+64); row r's 16-byte chunk c sits at c ^ (r&7));
+      // each thread then rotates its own row's rotary channels in place.
+      bool ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+      if (ok && P.rd > 0 && row < P.H) {
+        const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
+        const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+        auto at = [&](int d0) -> uint4* {
+          const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
+          return reinterpret_cast<uint4*>(q_s + slab * C::kQBox + row * 128 +
+                                          ((ch ^ (row & 7)) << 4));
+        };
+        if (!P.interleaved) {
+          const int half = P.rd >> 1;
+          for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
+            float a[8], bb[8], na[8], nb[8];
+            unpack8<T>(*at(d0), a);
+            unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+            rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
+            rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
+            *at(d0) = pack8<T>(na);
+            *at(d0 + half) = pack8<T>(nb);
+          }
+        } else {
+          for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
+            float a[8], dummy[8];
+            unpack8<T>(*at(d0), a);
+            rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
+            *at(d0) = pack8<T>(a);
           }
         }
-        const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
-        *reinterpret_cast<uint4*>(q_s + slab * C::kQBox + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
       }
       fence_proxy_async();
       mbar_arrive(smem_u32(&bars->q_full));
-    }
+      if (tid == 0) PA_TRACE(3);
 
-    const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int k = 0; k < n && ok; ++k) {
-      const int sb = k & 1;
-      const int64_t j0 = (t_begin + k) * N;
-      ok = __all_sync(0xffffffffu,
-                      wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
-      if (!ok) break;
-      tc_fence_after();
-      float s[N];
+      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+      float m_used = -INFINITY, l = 0.f;
+      for (int k = 0; k < n && ok; ++k) {
+        const int sb = k & 1;
+        const int64_t j0 = (t_begin + k) * N;
+        const bool edge = j0 < lo || j0 + N - 1 > pos;   // uniform across the CTA
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
+        if (!ok) break;
+        if (tid == 0 && k == 0) PA_TRACE(4);
+        if (tid == 0) PA_TRACE_TILE(k, 0);
+        float s[N];
+        if (live) {
+          tc_fence_after();
+          uint32_t r[N / 32][32];
 #pragma unroll
-      for (int c = 0; c < N; c += 16) {
-        uint32_t r[16];
-        tmem_ld16(lane_addr + C::kColS + sb * N + c, r);
+          for (int c = 0; c < N / 32; ++c)
+            tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 16; ++e) s[c + e] = __uint_as_float(r[e]);
-      }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->s_free[sb]));
-
-      float mt = -INFINITY;
+          for (int c = 0; c < N / 32; ++c) {
+            reg_fence(r[c]);
 #pragma unroll
-      for (int c = 0; c < N; ++c) {
-        const int64_t j = j0 + c;
-        float v = P.softcap_on ? P.cap_out * tanhf(s[c] * P.cap_in) : s[c] * P.scale_log2;
-        v = (j >= lo && j <= pos) ? v : -INFINITY;
-        s[c] = v;
-        mt = fmaxf(mt, v);
-      }
-      float factor = 1.f;
-      bool rescale = false;
-      if (k == 0) {
-        m_used = mt;
-      } else if (mt > m_used + kRescaleLog2) {
-        factor = ex2(m_used - mt);
-        m_used = mt;
-        l *= factor;
-        rescale = true;
-      }
-      uint32_t pk[N / 2];
-      float lsum = 0.f;
-#pragma unroll
-      for (int c = 0; c < N; c += 2) {
-        const float p0 = ex2(s[c] - m_used), p1 = ex2(s[c + 1] - m_used);
-        lsum += p0 + p1;
-        pk[c / 2] = pack2<T>(p0, p1);
-      }
-      l += lsum;
-
-      // Keys outside [lo, pos] in a boundary tile: zero their value rows so
-      // stale or unwritten cache slots cannot reach the PV product.
-      if (j0 < lo || j0 + N - 1 > pos) {
-        uint8_t* kst = k_s + (k % STAGES) * C::kStageBytes;
-        constexpr int kVSlabs = VG / 64;
-        for (int i = tid; i < N * kVSlabs * 8; i += 128) {
-          const int rr = i / (kVSlabs * 8);
-          const int rem = i - rr * (kVSlabs * 8);
-          const int slab = g * kVSlabs + rem / 8, ch = rem & 7;
-          const int64_t j = j0 + rr;
-          if (j < lo || j > pos)
-            *reinterpret_cast<uint4*>(kst + slab * C::kKBox + rr * 128 + ch * 16) =
-                make_uint4(0, 0, 0, 0);
+            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
+          }
+          tc_fence_before();
         }
-        fence_proxy_async();
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+
+        float factor = 1.f;
+        bool rescale = false;
+        // Scores in the log2 domain are x * sl (sl = scale*log2e) without
+        // softcap; with softcap they are rewritten in place and sl = 1.
+        const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        if (live) {
+          float mt = -INFINITY;
+          if (P.softcap_on) {
+#pragma unroll
+            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanhf(s[c] * P.cap_in);
+          }
+          if (edge) {
+#pragma unroll
+            for (int c = 0; c < N; ++c) {
+              const int64_t j = j0 + c;
+              if (j < lo || j > pos) s[c] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < N; ++c) mt = fmaxf(mt, s[c]);
+          mt *= sl;  // order-preserving (sl > 0)
+          if (k == 0) {
+            m_used = mt;
+          } else if (mt > m_used + kRescaleLog2) {
+            factor = ex2(m_used - mt);
+            m_used = mt;
+            l *= factor;
+            rescale = true;
+          }
+        }
+
+        // Keys outside [lo, pos] in a boundary tile: zero their value rows so
+        // stale or unwritten cache slots cannot reach the PV product.
+        if (edge) {
+          uint8_t* kst = k_s + (k % STAGES) * C::kStageBytes;
+          constexpr int kVSlabs = VG / 64;
+          for (int i = tid; i < N * kVSlabs * 8; i += 128) {
+            const int rr = i / (kVSlabs * 8);
+            const int rem = i - rr * (kVSlabs * 8);
+            const int slab = g * kVSlabs + rem / 8, ch = rem & 7;
+            const int64_t j = j0 + rr;
+            if (j < lo || j > pos)
+              *reinterpret_cast<uint4*>(kst + slab * C::kKBox + rr * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+
+        // P buffer sb is free once PV(k-2) has completed.
+        if (k >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]),
+                                                ((k - 2) >> 1) & 1, abort, P.err_flags));
+          if (!ok) break;
+        }
+        if (live) {
+          tc_fence_after();
+          float lsum = 0.f;
+#pragma unroll
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2(fmaf(s[c + 2 * e], sl, -m_used));
+              const float p1 = ex2(fmaf(s[c + 2 * e + 1], sl, -m_used));
+              lsum += p0 + p1;
+              r[e] = pack2<T>(p0, p1);
+            }
+            tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, r);
+          }
+          l += lsum;
+          if (__any_sync(0xffffffffu, rescale)) {
+            // O may only be touched once PV(k-1) has completed.
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
+                                                  ((k - 1) >> 1) & 1, abort, P.err_flags));
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < VG; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + C::kColO + c, r);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+                tmem_st16(lane_addr + C::kColO + c, r);
+              }
+            }
+          }
+          tmem_wait_st();
+        }
+        if (!ok) break;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[sb]));
+        if (tid == 0) PA_TRACE_TILE(k, 1);
       }
 
-      // P buffer sb is free once PV(k-2) has completed.
-      if (k >= 2) {
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]), ((k - 2) >> 1) & 1,
-                                              abort, P.err_flags));
-        if (!ok) break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < N / 2; c += 16) {
-        uint32_t r[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) r[e] = pk[c + e];
-        tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c, r);
-      }
-      if (__any_sync(0xffffffffu, rescale)) {
-        // O may only be touched once PV(k-1) has completed.
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
-                                              ((k - 1) >> 1) & 1, abort, P.err_flags));
-        if (!ok) break;
+      // ---- epilogue ----
+      if (tid == 0) PA_TRACE(5);
+      grid_dep_launch();
+      named_sync(2, 160);  // the producer has finished issuing (bad-block flag final)
+      ok = __all_sync(0xffffffffu, ok && !*abort);
+      if (ok)
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
+                                              ((n - 1) >> 1) & 1, abort, P.err_flags));
+      if (ok && live) {
         tc_fence_after();
+        const bool bad = bars->bad != 0;
+        if (splits == 1) {
+          const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
 #pragma unroll 1
-        for (int c = 0; c < VG; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(lane_addr + C::kColO + c, r);
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              uint4 o[2];
+              uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
-          tmem_st16(lane_addr + C::kColO + c, r);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(smem_u32(&bars->p_full[sb]));
-    }
-
-    // ---- epilogue ----
-    named_sync(2, 160);  // the producer has finished issuing (bad-block flag final)
-    ok = __all_sync(0xffffffffu, ok && !*abort);
-    if (ok)
-      ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
-                                            ((n - 1) >> 1) & 1, abort, P.err_flags));
-    if (ok) {
-      tc_fence_after();
-      const bool bad = bars->bad != 0;
-      if (P.splits == 1) {
-        const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
+              for (int e = 0; e < 8; ++e)
+                ow[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv,
+                                 __uint_as_float(r[2 * e + 1]) * inv);
+              uint4* dst = reinterpret_cast<uint4*>(out_row + (int64_t)row * vhs + g * VG + c);
+              dst[0] = o[0];
+              dst[1] = o[1];
+            }
+          }
+        } else {
+          float* wo = P.ws_o + (part * kRows + row) * VG;
 #pragma unroll 1
-        for (int c = 0; c < VG; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(lane_addr + C::kColO + c, r);
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              float4* dst = reinterpret_cast<float4*>(wo + c);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                     __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+          }
           if (row < P.H) {
-            uint4 o[2];
-            uint32_t* ow = reinterpret_cast<uint32_t*>(o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              ow[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
-            uint4* dst = reinterpret_cast<uint4*>(out_row + (int64_t)row * vhs + g * VG + c);
-            dst[0] = o[0];
-            dst[1] = o[1];
-          }
-        }
-      } else {
-        float* wo = P.ws_o + (part * kRows + row) * VG;
-#pragma unroll 1
-        for (int c = 0; c < VG; c += 16) {
-          uint32_t r[16];
-          tmem_ld16(lane_addr + C::kColO + c, r);
-          float4* dst = reinterpret_cast<float4*>(wo + c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                 __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
-        }
-        // a NaN max marks a split that read an invalid block
-        P.ws_ml[(part * kRows + row) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : m_used;
-        P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
-      }
-    }
-  } else if (warp == 4) {
-    // =================== TMA producer ===================
-    const int nsub = N / P.box_rows;
-    const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
-    int issued = 0;
-    for (int k = 0; k < n; ++k) {
-      const int stage = k % STAGES;
-      if (k >= STAGES) {
-        bool okw = true;
-        if (lane == 0)
-          okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
-                         P.err_flags);
-        if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
-      }
-      const int64_t j0 = (t_begin + k) * N;
-      // coordinates of the nsub boxes of rows (one cache block each)
-      int y = (int)P.num_slots;  // out of range: TMA fills zeros
-      if (lane < nsub) {
-        const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
-        if (key0 <= pos && key0 + P.box_rows - 1 >= lo) {
-          const int32_t phys = bt[key0 / P.bs];
-          if (phys >= 0 && phys < P.num_blocks) {
-            y = (int)((int64_t)phys * P.bs + key0 % P.bs);
-          } else {
-            bars->bad = 1;
-            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+            // a NaN max marks a split that read an invalid block
+            P.ws_ml[(part * kRows + row) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : m_used;
+            P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
           }
         }
       }
-      // broadcast the coordinates, then lane 0 issues every box
-      int ysub[8];
-#pragma unroll
-      for (int sb = 0; sb < 8; ++sb) ysub[sb] = __shfl_sync(0xffffffffu, y, sb < nsub ? sb : 0);
-      if (lane == 0) {
-        const uint32_t full = smem_u32(&bars->full[stage]);
-        mbar_expect_tx(full, C::kStageBytes);
-        const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes);
-#pragma unroll 1
+    } else if (warp == 4) {
+      // =================== TMA producer ===================
+      if (lane == 0) {  // Q: one box of QR rows (this token's heads) per 64-channel slab
+        const uint32_t qb = smem_u32(&bars->q_tma);
+        mbar_expect_tx(qb, C::kQBytes);
         for (int slab = 0; slab < C::kBoxes; ++slab)
-#pragma unroll 1
-          for (int sb = 0; sb < nsub; ++sb)
-            tma_load_2d(dst0 + slab * C::kKBox + sb * P.box_rows * 128, &kmap, slab * 64,
-                        ysub[sb], full);
+          tma_load_2d(smem_u32(q_s) + slab * C::kQBox, &qmap, slab * 64, (int)(t * P.H), qb);
       }
-      issued = k + 1;
+      const int nsub = N / P.box_rows;
+      const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int stage = k % STAGES;
+        if (k >= STAGES) {
+          bool okw = true;
+          if (lane == 0)
+            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
+                           P.err_flags);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
+        }
+        const int64_t j0 = (t_begin + k) * N;
+        if (lane == 0 && k == 0) PA_TRACE(8);
+        if (lane == 0 && k == n - 1) PA_TRACE(9);
+        // coordinates of the nsub boxes of rows (one cache block each)
+        int y = (int)P.num_slots;  // out of range: TMA fills zeros
+        if (lane < nsub) {
+          const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
+          if (key0 <= pos && key0 + P.box_rows - 1 >= lo) {
+            const int32_t phys = bt[key0 / P.bs];
+            if (phys >= 0 && phys < P.num_blocks) {
+              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
+            } else {
+              bars->bad = 1;
+              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+            }
+          }
+        }
+        if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
+        if (lane == 0) PA_TRACE_TILE(k, 5);
+        __syncwarp();
+        if (lane < nsub) {  // lane sb issues the boxes of rows sb (every slab)
+          const uint32_t full = smem_u32(&bars->full[stage]);
+          const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
+#pragma unroll 1
+          for (int slab = 0; slab < C::kBoxes; ++slab)
+            tma_load_2d(dst0 + slab * C::kKBox, &kmap, slab * 64, y, full);
+        }
+        issued = k + 1;
+        __syncwarp();
+      }
+      if (*abort && lane == 0) {
+        // copies still in flight must land before the CTA exits
+        drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+          const int kl = issued - 1 - ((issued - 1 - st) % STAGES);
+          drain_wait(smem_u32(&bars->full[st]), (kl / STAGES) & 1, P.err_flags);
+        }
+      }
+      __syncwarp();
+      named_arrive(2, 160);
+    } else if (warp == 5) {
+      // =================== MMA issuer ===================
+      if (lane == 0) {
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
+        constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
+        const uint32_t q_base = smem_u32(q_s);
+        const uint32_t k_base = smem_u32(k_s);
+        bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
+        if (ok) {
+          tc_fence_after();
+          PA_TRACE(10);
+          // Event loop: QK^T(k) needs its key tile (full) and a free S buffer
+          // (s_free of k-2); PV(k) needs P(k) (p_full). Issue whichever is
+          // ready, QK^T first, so neither waits behind the other's inputs.
+          int kq = 0, kp = 0;
+          const uint64_t t0 = globaltimer();
+          uint32_t spins = 0;
+          while (kp < n) {
+            bool progressed = false;
+            // PV first: it is short and releases the key stage to the producer.
+            if (kp < kq) {
+              const int stage = kp % STAGES, sb = kp & 1;
+              if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
+                tc_fence_after();
+                const uint32_t vb = k_base + stage * C::kStageBytes + (g * (VG / 64)) * C::kKBox;
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                  // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox
+                  // apart (leading offset), 8-key groups 1024 bytes apart (stride).
+                  const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8, bdesc, kIdPV,
+                         (kp > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->pv_done[sb]));
+                tc_commit(smem_u32(&bars->empty[stage]));
+                PA_TRACE_TILE(kp, 3);
+                ++kp;
+                progressed = true;
+              }
+            }
+            // QK^T(kq): needs its key tile and a free S buffer.
+            if (kq < n && kq < kp + 2) {
+              const int stage = kq % STAGES, sb = kq & 1;
+              if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
+                  (kq < 2 || mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - 2) >> 1) & 1))) {
+                PA_TRACE_TILE(kq, 4);
+                tc_fence_after();
+                const uint32_t kb = k_base + stage * C::kStageBytes;
+#pragma unroll
+                for (int kk = 0; kk < HS / 16; ++kk) {
+                  const int slab = kk >> 2, w = (kk & 3) * 32;
+                  const uint64_t a = sdesc(q_base + slab * C::kQBox + w, 16, 1024);
+                  const uint64_t bdesc = sdesc(kb + slab * C::kKBox + w, 16, 1024);
+                  mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, kk > 0 ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->s_full[sb]));
+                PA_TRACE_TILE(kq, 2);
+                ++kq;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              spins = 0;
+              continue;
+            }
+            if ((++spins & 15u) == 0) {
+              if (*abort) { ok = false; break; }
+              if (globaltimer() - t0 > kWaitLimitNs * 4) {
+                *abort = 1;
+                raise_flag(P.err_flags, PA_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        PA_TRACE(11);
+        // every MMA issued above completes before TMEM is released
+        tc_commit(smem_u32(&bars->drain));
+        drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
+      }
       __syncwarp();
     }
-    if (*abort && lane == 0) {
-      // copies still in flight must land before the CTA exits
-      for (int st = 0; st < STAGES && st < issued; ++st) {
-        const int kl = issued - 1 - ((issued - 1 - st) % STAGES);
-        drain_wait(smem_u32(&bars->full[st]), (kl / STAGES) & 1, P.err_flags);
-      }
-    }
-    __syncwarp();
-    named_arrive(2, 160);
-  } else {
-    // =================== MMA issuer (warp 5) ===================
-    if (lane == 0) {
-      constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
-      constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
-      constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
-      const uint32_t q_base = smem_u32(q_s);
-      const uint32_t k_base = smem_u32(k_s);
-      bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
-      int issued_pv = -1;
-      auto issue_qk = [&](int k) -> bool {
-        const int stage = k % STAGES, sb = k & 1;
-        if (!wait_bar(smem_u32(&bars->full[stage]), (k / STAGES) & 1, abort, P.err_flags))
-          return false;
-        if (k >= 2 &&
-            !wait_bar(smem_u32(&bars->s_free[sb]), ((k - 2) >> 1) & 1, abort, P.err_flags))
-          return false;
-        tc_fence_after();
-        const uint32_t kb = k_base + stage * C::kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < HS / 16; ++kk) {
-          const int slab = kk >> 2, w = (kk & 3) * 32;
-          const uint64_t a = sdesc(q_base + slab * C::kQBox + w, 16, 1024);
-          const uint64_t bdesc = sdesc(kb + slab * C::kKBox + w, 16, 1024);
-          mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&bars->s_full[sb]));
-        return true;
-      };
-      auto issue_pv = [&](int k) -> bool {
-        const int stage = k % STAGES, sb = k & 1;
-        if (!wait_bar(smem_u32(&bars->p_full[sb]), (k >> 1) & 1, abort, P.err_flags))
-          return false;
-        tc_fence_after();
-        const uint32_t vb = k_base + stage * C::kStageBytes + (g * (VG / 64)) * C::kKBox;
-#pragma unroll
-        for (int kk = 0; kk < N / 16; ++kk) {
-          // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox apart
-          // (leading offset), 8-key groups 1024 bytes apart (stride offset).
-          const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
-          mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8, bdesc, kIdPV,
-                 (k > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(smem_u32(&bars->pv_done[sb]));
-        tc_commit(smem_u32(&bars->empty[stage]));
-        issued_pv = k;
-        return true;
-      };
-      if (ok) {
-        tc_fence_after();
-        ok = issue_qk(0);
-        for (int k = 0; k < n && ok; ++k) {
-          if (k + 1 < n) ok = issue_qk(k + 1);
-          if (ok) ok = issue_pv(k);
-        }
-      }
-      (void)issued_pv;
-      // every MMA issued above completes before TMEM is released
-      tc_commit(smem_u32(&bars->drain));
-      drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
-    }
-    __syncwarp();
   }
 
+  if (W.status != 0) grid_dep_launch();
+  if (tid == 0) PA_TRACE(6);
   tc_fence_before();
   __syncthreads();
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (tid == 0) PA_TRACE(7);
 }
 
-// Merges key splits: M = max_s m_s, out = sum_s 2^(m_s-M) O_s / sum_s 2^(m_s-M) l_s.
+// Merges the key splits of each decode sequence (plan written by the
+// attention kernel): M = max_s m_s, out = sum_s 2^(m_s-M) O_s / sum_s
+// 2^(m_s-M) l_s; zero when a split read an invalid block.
 template <typename T, int VG, int G>
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ Params P) {
-  const int64_t x = blockIdx.x;
+  grid_dep_wait();  // the attention kernel's partials are complete and visible
+  const int x = blockIdx.x;
   const int h = blockIdx.y;
-  const int32_t b = P.seq_begin + (int32_t)x;
-  const int32_t q0 = P.cumseq[b], q1 = P.cumseq[b + 1];
-  if (q1 - q0 != 1 || q0 < 0 || q0 >= P.num_tokens) return;
-  const int64_t pos = P.past[b];
-  if (P.past[b] < 0 || pos >= (int64_t)P.max_blocks * P.bs || (P.rd > 0 && pos >= P.cos_rows))
-    return;
-  const int S = P.splits;
+  const int2 plan = P.ws_plan[x];
+  const int S = plan.y;
+  if (S <= 1) return;  // single split: the attention kernel wrote the output
+  const int32_t b = P.seq_begin + x;
+  const int32_t q0 = P.cumseq[b];
   T* dst = reinterpret_cast<T*>(P.out) + (int64_t)q0 * P.H * P.vhs + (int64_t)h * P.vhs;
   for (int c = threadIdx.x; c < G * VG; c += blockDim.x) {
     const int g = c / VG, cc = c - g * VG;
     float M = -INFINITY;
     bool bad = false;
     for (int s = 0; s < S; ++s) {
-      const float m = P.ws_ml[((((x * S + s) * G + g) * kRows) + h) * 2];
+      const float m = P.ws_ml[(((int64_t)(plan.x + s) * G + g) * kRows + h) * 2];
       bad |= isnan(m);
       M = fmaxf(M, m);
     }
     float L = 0.f, o = 0.f;
     for (int s = 0; s < S && !bad; ++s) {
-      const int64_t slot = ((x * S + s) * G + g) * kRows + h;
+      const int64_t slot = ((int64_t)(plan.x + s) * G + g) * kRows + h;
       const float l = P.ws_ml[slot * 2 + 1];
       if (l > 0.f) {
         const float w = ex2(P.ws_ml[slot * 2] - M);
@@ -742,71 +1019,92 @@ EncodeTiledFn encode_fn() {
 }
 
 struct Shape {
-  int hs, vg, groups, n, stages;
+  int hs, vg, groups, n, stages, qr;
 };
 
 bool pick(const Geometry& g, Shape* s) {
   if (g.H > kRows) return false;
   if (g.hs == 192 && g.vhs == 128) {
-    *s = {192, 128, 1, 64, 4};
+    *s = g.H <= 64 ? Shape{192, 128, 1, 128, 4, 64} : Shape{192, 128, 1, 128, 3, 128};
     return true;
   }
   if (g.hs == 576 && g.vhs == 512) {
-    *s = {576, 256, 2, 32, 2};
+    *s = {576, 256, 2, 32, 2, 128};
     return true;
   }
   return false;
 }
 
-int splits_for(const Geometry& g, const Shape& s, Phase ph, int64_t nq) {
-  if (ph == Phase::kPrefill || nq <= 0) return 1;
-  int64_t sp = g.num_sms / (nq * s.groups);
-  const int64_t max_tiles = ((int64_t)g.max_blocks * g.bs + s.n - 1) / s.n;
-  const int64_t cap = max_tiles / 4 > 1 ? max_tiles / 4 : 1;
-  if (sp > cap) sp = cap;
-  if (sp > 32) sp = 32;
-  if (sp < 1) sp = 1;
-  return (int)sp;
+// Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
+int64_t decode_units(const Geometry& g, const Shape& s, int64_t nseq) {
+  const int64_t wave = g.num_sms / s.groups;
+  return nseq > wave ? nseq : wave;
 }
 
-size_t partial_bytes(const Shape& s, int64_t units) {
+size_t decode_ws_bytes(const Shape& s, int64_t units, int64_t nseq) {
   const size_t per = (size_t)units * s.groups * kRows;
   const size_t o = ((per * s.vg * sizeof(float)) + 255) & ~(size_t)255;
-  return o + per * 2 * sizeof(float);
+  const size_t ml = ((per * 2 * sizeof(float)) + 255) & ~(size_t)255;
+  return o + ml + (size_t)nseq * sizeof(int2);
 }
 
-template <typename T, int HS, int VG, int G, int N, int STAGES>
+template <typename K, typename... Args>
+cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <typename T, int HS, int VG, int G, int N, int STAGES, int QR>
 cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
-  using C = Cfg<HS, VG, G, N, STAGES>;
+  using C = Cfg<HS, VG, G, N, STAGES, QR>;
   const size_t smem = C::kSmemData + sizeof(Barriers) + 1024;
   static bool configured[64] = {false};
+  auto kern = tc_attn_kernel<T, HS, VG, G, N, STAGES, QR>;
   if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_attn_kernel<T, HS, VG, G, N, STAGES>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     configured[g.device] = true;
   }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
+                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // Cache rows [num_blocks*bs, hs]: boxes of 64 channels x box_rows rows.
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)HS, (cuuint64_t)g.num_blocks * g.bs};
   const cuuint64_t strides[1] = {(cuuint64_t)HS * 2};
   const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map,
-                   std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                         : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                   2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const int64_t units = ph == Phase::kDecode ? nq * P.splits : nq;
-  tc_attn_kernel<T, HS, VG, G, N, STAGES>
-      <<<(unsigned)(units * G), kThreads, smem, a.stream>>>(map, P);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || P.splits == 1) return e;
-  tc_combine_kernel<T, VG, G><<<dim3((unsigned)nq, (unsigned)g.H), 128, 0, a.stream>>>(P);
-  return cudaGetLastError();
+  // Query rows [T*H, hs]: one QR-row box per 64-channel slab loads a token's heads.
+  CUtensorMap qmap;
+  const cuuint64_t qdims[2] = {(cuuint64_t)HS, (cuuint64_t)a.num_tokens * g.H};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)QR};
+  r = enc(&qmap, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(kThreads), smem, a.stream,
+                             map, qmap, P);
+  if (e != cudaSuccess || ph != Phase::kDecode) return e;
+  return launch_pdl(tc_combine_kernel<T, VG, G>, dim3((unsigned)nq, (unsigned)g.H), dim3(128), 0,
+                    a.stream, P);
 }
 
 }  // namespace tc
@@ -821,18 +1119,14 @@ size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t
   (void)num_tokens;
   tc::Shape s;
   if (ph == Phase::kPrefill || num_seqs <= 0 || !tc::pick(g, &s)) return 0;
-  // nq * S(nq) <= max(nq, num_sms / groups) for S(nq) = max(1, num_sms/(nq*groups)).
-  int64_t units = num_seqs > g.num_sms ? num_seqs : g.num_sms;
-  if (tc::splits_for(g, s, ph, 1) <= 1) return 0;
-  return tc::partial_bytes(s, units);
+  return tc::decode_ws_bytes(s, tc::decode_units(g, s, num_seqs), num_seqs);
 }
 
 size_t tc_call_workspace(const Geometry& g, Phase ph, const ReadArgs& a) {
   tc::Shape s;
-  if (!tc::pick(g, &s)) return 0;
-  const int64_t nq = ph == Phase::kDecode ? (int64_t)(a.seq_end - a.seq_begin) : a.num_tokens;
-  const int sp = tc::splits_for(g, s, ph, nq);
-  return sp > 1 ? tc::partial_bytes(s, nq * sp) : 0;
+  if (ph == Phase::kPrefill || !tc::pick(g, &s)) return 0;
+  const int64_t nq = (int64_t)(a.seq_end - a.seq_begin);
+  return tc::decode_ws_bytes(s, tc::decode_units(g, s, nq), nq);
 }
 
 cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
@@ -869,25 +1163,50 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.cap_out = g.softcap * tc::kLog2e;
   P.window = g.window;
   P.decode = ph == Phase::kDecode ? 1 : 0;
-  P.splits = tc::splits_for(g, s, ph, nq);
   P.box_rows = s.n < g.bs ? s.n : g.bs;
   P.ws_o = nullptr;
   P.ws_ml = nullptr;
-  if (P.splits > 1) {
-    const size_t per = (size_t)nq * P.splits * s.groups * tc::kRows;
+  P.ws_plan = nullptr;
+  P.units = 0;
+  if (ph == Phase::kDecode) {
+    const int64_t units = tc::decode_units(g, s, nq);
+    P.units = (int)units;
+    const size_t per = (size_t)units * s.groups * tc::kRows;
     const size_t o = ((per * s.vg * sizeof(float)) + 255) & ~(size_t)255;
-    if (a.workspace == nullptr || a.workspace_bytes < o + per * 2 * sizeof(float))
+    const size_t ml = ((per * 2 * sizeof(float)) + 255) & ~(size_t)255;
+    if (a.workspace == nullptr || a.workspace_bytes < tc::decode_ws_bytes(s, units, nq))
       return cudaErrorInvalidValue;
-    P.ws_o = reinterpret_cast<float*>(a.workspace);
-    P.ws_ml = reinterpret_cast<float*>(reinterpret_cast<char*>(a.workspace) + o);
+    char* w = reinterpret_cast<char*>(a.workspace);
+    P.ws_o = reinterpret_cast<float*>(w);
+    P.ws_ml = reinterpret_cast<float*>(w + o);
+    P.ws_plan = reinterpret_cast<int2*>(w + o + ml);
   }
   const bool bf16 = g.dtype == PA_DTYPE_BF16;
-  if (s.hs == 192) {
-    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 64, 4>(g, ph, a, P, nq)
-                : tc::launch_shape<__half, 192, 128, 1, 64, 4>(g, ph, a, P, nq);
+  if (s.hs == 192 && s.qr == 64) {
+    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 4, 64>(g, ph, a, P, nq)
+                : tc::launch_shape<__half, 192, 128, 1, 128, 4, 64>(g, ph, a, P, nq);
   }
-  return bf16 ? tc::launch_shape<__nv_bfloat16, 576, 256, 2, 32, 2>(g, ph, a, P, nq)
-              : tc::launch_shape<__half, 576, 256, 2, 32, 2>(g, ph, a, P, nq);
+  if (s.hs == 192) {
+    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq)
+                : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq);
+  }
+  return bf16 ? tc::launch_shape<__nv_bfloat16, 576, 256, 2, 32, 2, 128>(g, ph, a, P, nq)
+              : tc::launch_shape<__half, 576, 256, 2, 32, 2, 128>(g, ph, a, P, nq);
 }
 
 }  // namespace pa
+
+#ifdef PA_TC_TRACE
+extern "C" int pa_trace_dump(void* host, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, bytes < sizeof(pa::tc::g_trace)
+                                                              ? bytes : sizeof(pa::tc::g_trace));
+}
+extern "C" int pa_trace_clear(void) {
+  static unsigned long long zero[8192][16];
+  cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
+  return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
+}
+extern "C" int pa_trace_tile_dump(void* host) {
+  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
+}
+#endif

@@ -21,6 +21,10 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
                     int32_t num_seqs, T* __restrict__ key_cache, int64_t num_tokens, int hs,
                     int ro, int rd, int interleaved, int cos_rows, int64_t num_slots,
                     int32_t* err_flags) {
+  // A kernel launched after this one with programmatic dependent launch may
+  // start its prologue now; it waits (griddepcontrol.wait) for this grid to
+  // complete before it reads the cache.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int groups = hs >> 3;
   const int64_t total = num_tokens * groups;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
