@@ -176,6 +176,34 @@ pa_status pa_latent_prefill(const pa_latent_params* p, const void* query, int64_
                             void* workspace, size_t workspace_bytes, void* out,
                             int32_t* err_flags, void* stream);
 
+/*
+ * Allocation-free decode. The operator definition has no counterpart for
+ * this call; it exists for callers that cannot allocate device memory and so
+ * cannot hand pa_latent_decode a workspace: an execution provider whose host
+ * framework owns every device allocation, a serving loop that must not touch
+ * the allocator once running, or plain C code without a device allocator.
+ *
+ * Same arguments and results as pa_latent_decode, minus the workspace: the
+ * split-KV partials go to a scratch array of 32 MiB in device global memory
+ * that the library creates when it is loaded on a GPU and holds until the
+ * process exits (on every GPU that loads it). A call whose
+ * pa_latent_workspace_size exceeds 32 MiB returns PA_ERR_WORKSPACE. The call
+ * allocates nothing.
+ *
+ * The first call on each device looks up the scratch address on that device
+ * (with the device current); make that first call before any stream capture.
+ * Every call shares the one scratch array and leaves its contents behind:
+ * calls that overlap on the GPU (other streams, other threads) race on it,
+ * so serialize them.
+ */
+pa_status pa_latent_decode_noalloc(const pa_latent_params* p, const void* query,
+                                   int64_t num_tokens, const void* key_cache,
+                                   const void* cos_cache, const void* sin_cache,
+                                   const int32_t* cumseq, const int32_t* past,
+                                   const int32_t* block_table, int32_t num_seqs,
+                                   int32_t seq_begin, int32_t seq_end, void* out,
+                                   int32_t* err_flags, void* stream);
+
 /* Bytes of workspace pa_latent_decode / pa_latent_prefill need for these
  * parameters on the current device (0 if none). Host-only; returns 0 and
  * records an error message for invalid parameters. */

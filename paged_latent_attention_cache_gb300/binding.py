@@ -39,8 +39,8 @@ PA_DEVERR_TIMEOUT = 0x40
 PA_FLAG_PORTABLE = 0x1
 
 EXPORTED = ("pa_latent_validate", "pa_latent_write", "pa_latent_decode", "pa_latent_prefill",
-            "pa_latent_workspace_size", "pa_latent_kernel_family", "pa_latent_status_string",
-            "pa_latent_last_error")
+            "pa_latent_decode_noalloc", "pa_latent_workspace_size", "pa_latent_kernel_family",
+            "pa_latent_status_string", "pa_latent_last_error")
 
 
 class PaError(RuntimeError):
@@ -85,6 +85,9 @@ def _load() -> ctypes.CDLL:
     lib.pa_latent_decode.restype = ctypes.c_int
     lib.pa_latent_prefill.argtypes = read
     lib.pa_latent_prefill.restype = ctypes.c_int
+    lib.pa_latent_decode_noalloc.argtypes = [P, vp, i64, vp, vp, vp, vp, vp, vp, i32, i32, i32,
+                                             vp, vp, vp]
+    lib.pa_latent_decode_noalloc.restype = ctypes.c_int
     lib.pa_latent_workspace_size.argtypes = [P, i32, i64]
     lib.pa_latent_workspace_size.restype = sz
     lib.pa_latent_kernel_family.argtypes = [P, i32]
@@ -181,6 +184,20 @@ def pa_latent_prefill(p, query, key_cache, cos_cache, sin_cache, cumseq, past, b
                       num_tokens=None, num_seqs=None):
     _read(lib.pa_latent_prefill, p, query, key_cache, cos_cache, sin_cache, cumseq, past,
           block_table, out, seq_begin, seq_end, workspace, err_flags, stream, num_tokens, num_seqs)
+
+
+def pa_latent_decode_noalloc(p, query, key_cache, cos_cache, sin_cache, cumseq, past,
+                             block_table, out, seq_begin=0, seq_end=None, err_flags=None,
+                             stream=None, num_tokens=None, num_seqs=None):
+    """Decode using the library's static scratch instead of a workspace (for
+    callers that cannot allocate device memory)."""
+    T = query.shape[0] if num_tokens is None else num_tokens
+    B = past.shape[0] if num_seqs is None else num_seqs
+    se = B if seq_end is None else seq_end
+    _check(lib.pa_latent_decode_noalloc(
+        ctypes.byref(p), _ptr(query), int(T), _ptr(key_cache), _ptr(cos_cache), _ptr(sin_cache),
+        _ptr(cumseq), _ptr(past), _ptr(block_table), int(B), int(seq_begin), int(se), _ptr(out),
+        _ptr(err_flags), _stream(stream)))
 
 
 def alloc_workspace(p: pa_latent_params, num_seqs: int, num_tokens: int,

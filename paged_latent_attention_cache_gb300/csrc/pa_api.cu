@@ -190,6 +190,9 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
 }
 
 }  // namespace
+
+pa_status record_error(pa_status s, const char* msg) { return fail(s, "%s", msg); }
+
 }  // namespace pa
 
 using namespace pa;

@@ -32,6 +32,10 @@ struct Geometry {
 
 enum class Phase { kDecode = 0, kPrefill = 1 };
 
+// Records msg as the calling thread's pa_latent_last_error() text and
+// returns s.
+pa_status record_error(pa_status s, const char* msg);
+
 // ---- write phase (pa_write.cu)
 cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
                          const void* cos_cache, const void* sin_cache,
