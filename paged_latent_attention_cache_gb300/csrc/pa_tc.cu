@@ -30,441 +30,10 @@
 // double-buffered in TMEM. Every mbarrier wait is bounded: on expiry the
 // CTA sets PA_DEVERR_TIMEOUT in the error word, drains what it issued and
 // exits without trapping.
-#include <cuda.h>
-
-#include "pa_common.cuh"
-#include "pa_internal.h"
+#include "pa_tc_common.cuh"
 
 namespace pa {
 namespace tc {
-
-constexpr int kThreads = 192;
-constexpr int kRows = 128;               // MMA M: TMEM lanes
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleLog2 = 8.0f;     // lazy-rescale threshold (factor 256)
-
-// ---------------------------------------------------------------------------
-// PTX wrappers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void named_sync(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void named_arrive(uint32_t id, uint32_t n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// D(tmem) (+)= A(smem) * B(smem)
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// D(tmem) (+)= A(tmem) * B(smem)
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-      "r"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-// 16 consecutive 32-bit TMEM columns of this thread's lane; the wait is in
-// the same statement so the registers are valid when it returns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-// 32 consecutive columns without waiting; pair with tmem_wait_ld() and
-// reg_fence() before the registers are read.
-__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-// Orders later uses of r after the preceding tcgen05.wait::ld.
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
-#pragma unroll
-  for (int i = 0; i < 32; i += 8)
-    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]),
-                 "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
-}
-// Programmatic dependent launch controls (no-ops for an ordinary launch).
-__device__ __forceinline__ void grid_dep_wait() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-}
-__device__ __forceinline__ void grid_dep_launch() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
-// start address, leading / stride byte offsets (>> 4), version 1, layout 2.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// Instruction descriptor, kind::f16: f32 accumulator, A/B both bf16 or
-// both f16, A K-major, B K-major or MN-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b_mn) {
-  return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
-         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// Optional timeline trace (compiled only with -DPA_TC_TRACE): %globaltimer
-// stamps at phase boundaries per CTA, read back by a debug entry point.
-#ifdef PA_TC_TRACE
-__device__ unsigned long long g_trace[8192][16];
-__device__ __forceinline__ void trace(int slot) {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  if (blockIdx.x < 8192) g_trace[blockIdx.x][slot] = t;
-}
-__device__ unsigned long long g_trace_tile[256][8];
-__device__ __forceinline__ void trace_tile(int k, int slot) {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  if (blockIdx.x == 0 && k < 256) g_trace_tile[k][slot] = t;
-}
-#define PA_TRACE(slot) trace(slot)
-#define PA_TRACE_TILE(k, slot) trace_tile(k, slot)
-#else
-#define PA_TRACE(slot) ((void)0)
-#define PA_TRACE_TILE(k, slot) ((void)0)
-#endif
-
-// ---------------------------------------------------------------------------
-// Parameters
-// ---------------------------------------------------------------------------
-struct Params {
-  const void* query;
-  void* out;
-  float* ws_o;      // [units][G][128][VG]   (key-split partials, decode)
-  float* ws_ml;     // [units][G][128][2]    (log2-domain max, denominator)
-  int2* ws_plan;    // [nseq] (first unit, number of key splits) per decode sequence
-  const void* cos_cache;
-  const void* sin_cache;
-  const int32_t* cumseq;
-  const int32_t* past;
-  const int32_t* block_table;
-  int32_t* err_flags;
-  int64_t num_tokens;
-  int64_t num_slots;
-  int num_seqs, seq_begin, seq_end;
-  int H, vhs, ro, rd, interleaved, cos_rows, bs, num_blocks, max_blocks;
-  float scale_log2;  // scale * log2(e)
-  float cap_in;      // scale / softcap   (softcap > 0)
-  float cap_out;     // softcap * log2(e)
-  int softcap_on;
-  int window;
-  int units;         // decode: CTA units (per value group) the grid provides
-  int decode;
-  int box_rows;      // rows per TMA box: min(N, bs)
-};
-
-// QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
-// MMA then reads rows 64-127 from the next slab, rows that are never stored).
-template <int HS, int VG, int G, int N, int STAGES, int QR>
-struct Cfg {
-  static constexpr int kBoxes = HS / 64;                  // 64-channel slabs
-  static constexpr int kQBytes = QR * HS * 2;
-  static constexpr int kQBox = QR * 128;                   // bytes per Q slab
-  static constexpr int kKBox = N * 128;                    // bytes per K slab
-  static constexpr int kStageBytes = N * HS * 2;
-  static constexpr int kSmemData = kQBytes + STAGES * kStageBytes;
-  // TMEM columns: O | S0 | S1 | P0 | P1   (P is 16-bit: N/2 columns each)
-  static constexpr int kColO = 0;
-  static constexpr int kColS = VG;
-  static constexpr int kColP = VG + 2 * N;
-  static constexpr int kCols = VG + 2 * N + N;
-  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
-                                   : kCols <= 256 ? 256 : 512;
-  static_assert(kCols <= 512, "TMEM budget");
-  static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 128, "shape");
-  static_assert(STAGES <= 8, "stages");
-  static_assert(QR == 64 || QR == 128, "query rows");
-};
-
-struct Barriers {
-  uint64_t full[8], empty[8];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
-  uint64_t q_tma, q_full;
-  uint64_t drain;
-  uint32_t tmem_base;
-  int bad;
-  int abort;
-};
-
-// Resolved work of one CTA (written by warp 0 during the prologue).
-struct Work {
-  int64_t t, pos, t_begin, t_end;
-  int b, splits, first, split;
-  int status;  // 0 = run, 1 = idle, 2 = error already reported (write nothing more)
-};
-
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
-// Non-blocking probe (used where one thread polls several barriers).
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait on an mbarrier phase. try_wait lets the hardware suspend the
-// thread while the phase is pending (no issue slots burnt); the wait gives
-// up after about a second of %globaltimer time, or as soon as another role
-// of the CTA has aborted, and then returns false.
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort,
-                                         int32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0) {
-      if (*abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) break;
-    }
-  }
-  *abort = 1;
-  raise_flag(err, PA_DEVERR_TIMEOUT);
-  return false;
-}
-
-// Bounded wait used while tearing down: ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int32_t* err) {
-  const uint64_t t0 = globaltimer();
-  for (uint32_t i = 0;; ++i) {
-    if (mbar_try_wait(bar, parity)) return;
-    if ((i & 15u) == 15u && globaltimer() - t0 > kWaitLimitNs) break;
-  }
-  raise_flag(err, PA_DEVERR_TIMEOUT);
-}
-
-template <typename T>
-__device__ __forceinline__ uint32_t pack2(float a, float b);
-template <>
-__device__ __forceinline__ uint32_t pack2<__nv_bfloat16>(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-template <>
-__device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
-  __half2 v = __floats2half2_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// ---------------------------------------------------------------------------
-// Decode work plan. Each valid decode sequence has n_b key tiles; it is cut
-// into c_b(T) = ceil(n_b / T) splits of at most T tiles, T being the smallest
-// split length for which all splits fit in the grid's units. Invalid
-// sequences (q_len != 1, out-of-range position) get one unit, which only
-// reports the error. Every CTA derives the same plan from past_seqlens with
-// one warp (lane-strided sequences, shuffle reductions), so no host round
-// trip or separate planning launch is needed.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int64_t decode_tiles(const Params& P, int b, int n_tile) {
-  const int32_t q0 = P.cumseq[b], q1 = P.cumseq[b + 1];
-  if (q1 - q0 != 1 || q0 < 0 || q0 >= P.num_tokens) return 0;
-  const int64_t pos = P.past[b];
-  if (pos < 0 || pos >= (int64_t)P.max_blocks * P.bs || (P.rd > 0 && pos >= P.cos_rows)) return 0;
-  const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-  return pos / n_tile - lo / n_tile + 1;
-}
-
-__device__ __forceinline__ int64_t splits_of(int64_t tiles, int64_t T) {
-  // 32-bit division: tile counts and split lengths stay far below 2^31
-  return tiles <= 0 ? 1 : (int64_t)(((uint32_t)tiles + (uint32_t)T - 1u) / (uint32_t)T);
-}
-
-__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
-// Run by one full warp; returns the unit's plan in every lane.
-template <int N>
-__device__ Work decode_plan_warp(const Params& P, int unit) {
-  constexpr int kCache = 8;  // sequences per lane kept in registers
-  const int lane = threadIdx.x & 31;
-  const int nseq = P.seq_end - P.seq_begin;
-  const int chunk = (nseq + 31) / 32;
-  const int c0 = min(nseq, lane * chunk), c1 = min(nseq, c0 + chunk);
-  int64_t tl[kCache];
-#pragma unroll
-  for (int i = 0; i < kCache; ++i)
-    tl[i] = (c0 + i < c1) ? decode_tiles(P, P.seq_begin + c0 + i, N) : 0;
-  auto tiles_at = [&](int i) -> int64_t {
-    const int k = i - c0;
-    if (k < kCache) {
-      int64_t v = 0;
-#pragma unroll
-      for (int q = 0; q < kCache; ++q) v = (q == k) ? tl[q] : v;
-      return v;
-    }
-    return decode_tiles(P, P.seq_begin + i, N);
-  };
-  int64_t mx = 1;
-  for (int i = c0; i < c1; ++i) mx = max(mx, tiles_at(i));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  int64_t lo = 1, hi = mx;
-  while (lo < hi) {  // smallest T with sum_b splits_of(n_b, T) <= units
-    const int64_t mid = (lo + hi) >> 1;
-    int64_t cnt = 0;
-    for (int i = c0; i < c1; ++i) cnt += splits_of(tiles_at(i), mid);
-    if (warp_sum64(cnt) <= P.units) hi = mid; else lo = mid + 1;
-  }
-  const int64_t T = lo;
-  int64_t mine = 0;
-  for (int i = c0; i < c1; ++i) mine += splits_of(tiles_at(i), T);
-  int64_t incl = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  int64_t run = incl - mine;
-  Work w;
-  w.status = 1;
-  w.b = -1;
-  int hit = 0;
-  for (int i = c0; i < c1; ++i) {
-    const int64_t tiles = tiles_at(i);
-    const int64_t c = splits_of(tiles, T);
-    if (unit >= run && unit < run + c) {
-      hit = 1;
-      w.b = P.seq_begin + i;
-      w.split = (int)(unit - run);
-      w.splits = (int)c;
-      w.first = (int)run;
-      w.t_begin = w.t_end = 0;
-      if (tiles > 0) {
-        const int64_t pos = P.past[w.b];
-        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-        w.t_begin = lo_key / N + (int64_t)w.split * T;
-        w.t_end = min(pos / N + 1, w.t_begin + T);
-      }
-    }
-    run += c;
-  }
-  const unsigned who = __ballot_sync(0xffffffffu, hit);
-  if (who == 0) return w;  // idle unit
-  const int src = __ffs(who) - 1;
-  w.b = __shfl_sync(0xffffffffu, w.b, src);
-  w.split = __shfl_sync(0xffffffffu, w.split, src);
-  w.splits = __shfl_sync(0xffffffffu, w.splits, src);
-  w.first = __shfl_sync(0xffffffffu, w.first, src);
-  w.t_begin = __shfl_sync(0xffffffffu, w.t_begin, src);
-  w.t_end = __shfl_sync(0xffffffffu, w.t_end, src);
-  w.status = 0;
-  return w;
-}
 
 // ---------------------------------------------------------------------------
 // The attention kernel
@@ -960,68 +529,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) PA_TRACE(7);
 }
 
-// Merges the key splits of each decode sequence (plan written by the
-// attention kernel): M = max_s m_s, out = sum_s 2^(m_s-M) O_s / sum_s
-// 2^(m_s-M) l_s; zero when a split read an invalid block.
-template <typename T, int VG, int G>
-__global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ Params P) {
-  grid_dep_wait();  // the attention kernel's partials are complete and visible
-  const int x = blockIdx.x;
-  const int h = blockIdx.y;
-  const int2 plan = P.ws_plan[x];
-  const int S = plan.y;
-  if (S <= 1) return;  // single split: the attention kernel wrote the output
-  const int32_t b = P.seq_begin + x;
-  const int32_t q0 = P.cumseq[b];
-  T* dst = reinterpret_cast<T*>(P.out) + (int64_t)q0 * P.H * P.vhs + (int64_t)h * P.vhs;
-  for (int c = threadIdx.x; c < G * VG; c += blockDim.x) {
-    const int g = c / VG, cc = c - g * VG;
-    float M = -INFINITY;
-    bool bad = false;
-    for (int s = 0; s < S; ++s) {
-      const float m = P.ws_ml[(((int64_t)(plan.x + s) * G + g) * kRows + h) * 2];
-      bad |= isnan(m);
-      M = fmaxf(M, m);
-    }
-    float L = 0.f, o = 0.f;
-    for (int s = 0; s < S && !bad; ++s) {
-      const int64_t slot = ((int64_t)(plan.x + s) * G + g) * kRows + h;
-      const float l = P.ws_ml[slot * 2 + 1];
-      if (l > 0.f) {
-        const float w = ex2(P.ws_ml[slot * 2] - M);
-        L += w * l;
-        o += w * P.ws_o[slot * VG + cc];
-      }
-    }
-    dst[c] = Half<T>::from_f32(L > 0.f && !bad ? o / L : 0.f);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-struct Shape {
-  int hs, vg, groups, n, stages, qr;
-};
-
 bool pick(const Geometry& g, Shape* s) {
   if (g.H > kRows) return false;
   if (g.hs == 192 && g.vhs == 128) {
@@ -1029,39 +539,13 @@ bool pick(const Geometry& g, Shape* s) {
     return true;
   }
   if (g.hs == 576 && g.vhs == 512) {
-    *s = {576, 256, 2, 32, 2, 128};
+    // CTA-pair kernel (pa_tc_pair.cu): each CTA rotates the query channels it
+    // holds, so the rotary channels must lie in one CTA's range.
+    if (!(g.rd == 0 || g.ro >= 320 || g.ro + g.rd <= 256)) return false;
+    *s = {576, 256, 2, 64, 2, 128};
     return true;
   }
   return false;
-}
-
-// Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
-int64_t decode_units(const Geometry& g, const Shape& s, int64_t nseq) {
-  const int64_t wave = g.num_sms / s.groups;
-  return nseq > wave ? nseq : wave;
-}
-
-size_t decode_ws_bytes(const Shape& s, int64_t units, int64_t nseq) {
-  const size_t per = (size_t)units * s.groups * kRows;
-  const size_t o = ((per * s.vg * sizeof(float)) + 255) & ~(size_t)255;
-  const size_t ml = ((per * 2 * sizeof(float)) + 255) & ~(size_t)255;
-  return o + ml + (size_t)nseq * sizeof(int2);
-}
-
-template <typename K, typename... Args>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                       Args... args) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 template <typename T, int HS, int VG, int G, int N, int STAGES, int QR>
@@ -1190,8 +674,8 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
     return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq)
                 : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq);
   }
-  return bf16 ? tc::launch_shape<__nv_bfloat16, 576, 256, 2, 32, 2, 128>(g, ph, a, P, nq)
-              : tc::launch_shape<__half, 576, 256, 2, 32, 2, 128>(g, ph, a, P, nq);
+  return bf16 ? tc::launch_pair<__nv_bfloat16>(g, ph, a, P, nq)
+              : tc::launch_pair<__half>(g, ph, a, P, nq);
 }
 
 }  // namespace pa
@@ -1202,7 +686,7 @@ extern "C" int pa_trace_dump(void* host, size_t bytes) {
                                                               ? bytes : sizeof(pa::tc::g_trace));
 }
 extern "C" int pa_trace_clear(void) {
-  static unsigned long long zero[8192][16];
+  static unsigned long long zero[8192][16];  // >= sizeof either trace array
   cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
   return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
 }

@@ -1,0 +1,728 @@
+// Tensor-core read phase for the 576/512 latent geometry on a CTA pair.
+//
+// Operator (paged_attention.rs, module doc "Read phase" / attn_impl):
+//   out[h] = softmax_j(scale * RoPE(q_h) . K_j) @ K_j[:512],  j in [lo, pos].
+// A 128-head output accumulator of 512 f32 columns fills a whole SM's TMEM
+// and a 128 x 576 query tile most of its shared memory, so one token is
+// handled by a cluster of two CTAs on two SMs that split the latent channels:
+//
+//   CTA c in {0,1} holds query slabs (64 channels each) 4c..4c+4 and loads
+//   the same five slabs of every key tile. Its QK^T covers 18 of the 36
+//   16-channel K steps (channels [288c, 288c+288)), so S = S_0 + S_1 with
+//   S_c its partial; each softmax thread sends its row of S_c to the peer
+//   through distributed shared memory and adds the peer's row (both CTAs
+//   form S_0 + S_1 in the same order, so they hold bit-identical S, P, m, l).
+//   CTA c then accumulates O[:, 256c : 256c+256] = P @ V with V = its slabs
+//   0-3 (global slabs 4c..4c+3), i.e. each output half on one SM and no
+//   product computed twice.
+//
+// Roles per CTA as in pa_tc.cu: warps 0-3 softmax/epilogue (thread = head
+// row = TMEM lane), warp 4 TMA producer, warp 5 TMEM allocation + the
+// MMA-issuing thread. Key tiles of 64 keys, 2 stages; S and P
+// double-buffered in TMEM; every wait is bounded.
+#include "pa_tc_common.cuh"
+
+namespace pa {
+namespace tc {
+
+template <int N, int STAGES>
+struct PairCfg {
+  static constexpr int kSlabs = 5;                  // 64-channel slabs per CTA (of 9)
+  static constexpr int kSteps = 18;                 // 16-channel QK^T K-steps per CTA
+  static constexpr int kQBox = kRows * 128;         // bytes per full query slab (SW128)
+  static constexpr int kQHalf = kRows * 64;         // the 32 channels of slab 4 (SW64)
+  static constexpr int kQBytes = 4 * kQBox + kQHalf;
+  static constexpr int kKBox = N * 128;             // bytes per key slab of a stage
+  static constexpr int kStageBytes = kSlabs * kKBox;
+  static constexpr int kXBytes = kRows * N * 4;     // incoming partial-S rows
+  static constexpr int kSmemData = kQBytes + STAGES * kStageBytes + kXBytes;
+  static constexpr int kVG = 256;                   // output channels per CTA
+  static constexpr int kColO = 0;
+  static constexpr int kColS = kVG;
+  static constexpr int kColP = kVG + 2 * N;
+  static constexpr int kTmemCols = 512;
+  static_assert(kVG + 3 * N <= 512, "TMEM budget");
+  static_assert(N % 32 == 0 && N <= 128, "key tile");
+};
+
+struct PairBarriers {
+  uint64_t full[4], empty[4];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t q_tma, q_full;
+  uint64_t x_in;    // x_s holds the peer's partial rows (local expect_tx + the
+                    // peer's st.async complete_tx bytes)
+  uint64_t x_out;   // the peer has read the rows this CTA sent into its x_s
+  uint64_t drain;
+  uint32_t tmem_base;
+  int bad;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n barrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ uint32_t map_peer(uint32_t saddr, uint32_t peer) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(peer));
+  return r;
+}
+__device__ __forceinline__ void st_peer_v4(uint32_t raddr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+// Relaxed remote arrive: used where the ordering it announces (loads that
+// have already returned their values) needs no release fence, so the thread
+// does not wait for its own in-flight remote stores.
+__device__ __forceinline__ void arrive_peer_relaxed(uint32_t raddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr)
+               : "memory");
+}
+// Shared-memory descriptor for a K-major operand with 64-byte rows in the
+// 64-byte swizzle layout (8-row atoms of 512 bytes): layout type 4.
+__device__ __forceinline__ uint64_t sdesc64(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+// Remote 16-byte store whose arrival completes tx bytes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
+                                            uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(raddr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (for arrivals made by the peer).
+__device__ __forceinline__ bool wait_bar_cluster(uint32_t bar, uint32_t parity,
+                                                 volatile int* abort, int32_t* err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 15u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) break;
+    }
+  }
+  *abort = 1;
+  raise_flag(err, PA_DEVERR_TIMEOUT);
+  return false;
+}
+
+template <typename T, int N, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+               const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
+  using C = PairCfg<N, STAGES>;
+  constexpr int G = 2, VG = C::kVG;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Work work;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* q_s = smem;
+  uint8_t* k_s = smem + C::kQBytes;
+  float* x_s = reinterpret_cast<float*>(smem + C::kQBytes + STAGES * C::kStageBytes);
+  PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + C::kSmemData);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t g = cluster_rank();         // channel half == value group
+  const uint32_t peer = g ^ 1u;
+  const int unit = blockIdx.x / G;
+  const int vhs = P.vhs;
+  if (tid == 0) PA_TRACE(0);
+
+  // ---- prologue (same plan in both CTAs of the pair) ----
+  if (warp == 0) {
+    grid_dep_wait();
+    Work w;
+    if (P.decode) {
+      w = decode_plan_warp<N>(P, unit);
+      if (w.status == 0) {
+        const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
+        if (lane == 0 && w.split == 0 && g == 0)
+          P.ws_plan[w.b - P.seq_begin] = make_int2(w.first, w.splits);
+        if (q1 - q0 != 1) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_DECODE_QLEN);
+          w.status = 2;
+        } else if (q0 < 0 || q0 >= P.num_tokens) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_CUMSEQ);
+          w.status = 2;
+        } else {
+          w.t = q0;
+          w.pos = P.past[w.b];
+        }
+      }
+    } else {
+      int32_t b;
+      int64_t pos;
+      w.status = 1;
+      w.splits = 1;
+      if (locate_token(unit, P.cumseq, P.past, P.num_seqs,
+                       (lane == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos) &&
+          b >= P.seq_begin && b < P.seq_end) {
+        w.status = 0;
+        w.b = b;
+        w.t = unit;
+        w.pos = pos;
+        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        w.t_begin = lo_key / N;
+        w.t_end = pos / N + 1;
+      }
+    }
+    if (w.status == 0) {
+      const bool bad_ctx = P.past[w.b] < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
+      const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
+      if (bad_ctx || bad_pos) {
+        if (lane == 0 && g == 0)
+          raise_flag(P.err_flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
+        T* out_row = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs;
+        for (int i = lane; i < P.H * VG; i += 32) {
+          const int h = i / VG, c = i % VG;
+          out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
+        }
+        w.status = 2;
+      }
+    }
+    if (lane == 0) work = w;
+  } else if (warp == 1 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->s_full[i]), 1);
+      mbar_init(smem_u32(&bars->s_free[i]), kRows);
+      mbar_init(smem_u32(&bars->p_full[i]), kRows);
+      mbar_init(smem_u32(&bars->pv_done[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_tma), 1);
+    mbar_init(smem_u32(&bars->q_full), kRows);
+    mbar_init(smem_u32(&bars->x_in), 1);
+    mbar_init(smem_u32(&bars->x_out), 1);
+    mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);  // armed for tile 0
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->bad = 0;
+    bars->abort = 0;
+    fence_barrier_init();
+  } else if (warp == 4 && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&qmap64);
+  } else if (warp == 5) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp != 0) grid_dep_wait();
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+  const Work W = work;
+  if (tid == 0) PA_TRACE(1);
+
+  if (W.status == 0) {
+    const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
+    const int32_t b = W.b;
+    const int splits = W.splits;
+    const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    const int n = (int)max((int64_t)0, W.t_end - t_begin);
+    const int64_t part = (int64_t)unit * G + g;
+    T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
+    const int slab0 = 4 * (int)g;  // global slab of local key slab 0
+    // Query layout in shared memory: CTA 0 holds full slabs 0-3 (SW128) then
+    // channels 256-287 as a 64-byte-swizzled half slab; CTA 1 holds channels
+    // 288-319 as the half slab, then full slabs 5-8.
+    const int q_full0 = g ? 5 : 0;                         // global slab of full slab 0
+    const int q_full_off = g ? C::kQHalf : 0;              // byte offset of full slab 0
+    const int q_half_off = g ? 0 : 4 * C::kQBox;           // byte offset of the half slab
+
+    if (warp < 4) {
+      // =================== softmax / exchange / epilogue ===================
+      const int row = tid;
+      const bool live = warp * 32 < P.H;
+      bool ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+      // RoPE in place on this CTA's slabs (the pair kernel only runs when the
+      // rotary channels and their partners lie inside one CTA's slabs).
+      if (ok && P.rd > 0 && row < P.H) {
+        const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;  // full query slabs only
+        if (P.ro >= c_lo && P.ro + P.rd <= c_hi) {
+          const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
+          const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+          auto at = [&](int d0) -> uint4* {
+            const int slab = (d0 >> 6) - q_full0, ch = (d0 >> 3) & 7;
+            return reinterpret_cast<uint4*>(q_s + q_full_off + slab * C::kQBox + row * 128 +
+                                            ((ch ^ (row & 7)) << 4));
+          };
+          if (!P.interleaved) {
+            const int half = P.rd >> 1;
+            for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
+              float a[8], bb[8], na[8], nb[8];
+              unpack8<T>(*at(d0), a);
+              unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+              rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
+              rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
+              *at(d0) = pack8<T>(na);
+              *at(d0 + half) = pack8<T>(nb);
+            }
+          } else {
+            for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
+              float a[8], dummy[8];
+              unpack8<T>(*at(d0), a);
+              rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
+              *at(d0) = pack8<T>(a);
+            }
+          }
+        }
+      }
+      fence_proxy_async();
+      mbar_arrive(smem_u32(&bars->q_full));
+      if (tid == 0) PA_TRACE(3);
+
+      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+      // incoming partial rows (two buffers), chunk-major: 16-byte chunk q of
+      // row r at [q][r], so a warp's store or load of one chunk for its 32
+      // rows is 512 contiguous bytes (one coalesced transfer to the peer)
+      constexpr int kChunks = N / 4;
+      float m_used = -INFINITY, l = 0.f;
+      for (int k = 0; k < n && ok; ++k) {
+        const int sb = k & 1;
+        const int64_t j0 = (t_begin + k) * N;
+        const bool edge = j0 < lo || j0 + N - 1 > pos;
+        ok = __all_sync(0xffffffffu,
+                        wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
+        if (!ok) break;
+        if (tid == 0) PA_TRACE_TILE(k, 0);
+        if (tid == 0 && k == 0) PA_TRACE(4);
+        float s[N];
+        {
+          tc_fence_after();
+          uint32_t r[N / 32][32];
+#pragma unroll
+          for (int c = 0; c < N / 32; ++c)
+            tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < N / 32; ++c) {
+            reg_fence(r[c]);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
+          }
+          tc_fence_before();
+        }
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+        // Send this row's partial into the peer's buffer b = k%2 with st.async
+        // (each store completes its bytes on the peer's x_in[b]); buffer b is
+        // free once the peer has read tile k-2 from it.
+        float* x_buf = x_s + row * 4;
+        const uint32_t x_peer = map_peer(smem_u32(x_buf), peer);
+        const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in), peer);
+        if (k >= 1) {  // the peer has read tile k-1 from its x_s
+          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out), (k - 1) & 1,
+                                                        abort, P.err_flags));
+          if (!ok) break;
+        }
+        if (tid == 0) PA_TRACE_TILE(k, 8);
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q)
+          st_async_v4(x_peer + q * kRows * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3],
+                      x_in_peer);
+        if (tid == 0) PA_TRACE_TILE(k, 9);
+        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in), k & 1, abort,
+                                                      P.err_flags));
+        if (!ok) break;
+        if (tid == 0) PA_TRACE_TILE(k, 12);
+        // S = S_0 + S_1 in that order in both CTAs
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(x_buf + q * kRows * 4);
+          if (g == 0) {
+            s[4 * q] += v.x; s[4 * q + 1] += v.y; s[4 * q + 2] += v.z; s[4 * q + 3] += v.w;
+          } else {
+            s[4 * q] = v.x + s[4 * q]; s[4 * q + 1] = v.y + s[4 * q + 1];
+            s[4 * q + 2] = v.z + s[4 * q + 2]; s[4 * q + 3] = v.w + s[4 * q + 3];
+          }
+        }
+        named_sync(3, 128);  // every row of x_s has been read
+        if (tid == 0) {
+          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);
+          arrive_peer_relaxed(map_peer(smem_u32(&bars->x_out), peer));
+        }
+        if (tid == 0) PA_TRACE_TILE(k, 6);
+
+        float factor = 1.f;
+        bool rescale = false;
+        const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        if (live) {
+          float mt = -INFINITY;
+          if (P.softcap_on) {
+#pragma unroll
+            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanhf(s[c] * P.cap_in);
+          }
+          if (edge) {
+#pragma unroll
+            for (int c = 0; c < N; ++c) {
+              const int64_t j = j0 + c;
+              if (j < lo || j > pos) s[c] = -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < N; ++c) mt = fmaxf(mt, s[c]);
+          mt *= sl;
+          if (k == 0) {
+            m_used = mt;
+          } else if (mt > m_used + kRescaleLog2) {
+            factor = ex2(m_used - mt);
+            m_used = mt;
+            l *= factor;
+            rescale = true;
+          }
+        }
+        if (edge) {  // zero value rows of masked keys (stale cache slots)
+          uint8_t* kst = k_s + (k % STAGES) * C::kStageBytes;
+          for (int i = tid; i < N * 4 * 8; i += 128) {
+            const int rr = i / 32, rem = i - rr * 32;
+            const int slab = rem / 8, ch = rem & 7;
+            const int64_t j = j0 + rr;
+            if (j < lo || j > pos)
+              *reinterpret_cast<uint4*>(kst + slab * C::kKBox + rr * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        if (k >= 2) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]),
+                                                ((k - 2) >> 1) & 1, abort, P.err_flags));
+          if (!ok) break;
+        }
+        if (live) {
+          tc_fence_after();
+          float lsum = 0.f;
+#pragma unroll
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2(fmaf(s[c + 2 * e], sl, -m_used));
+              const float p1 = ex2(fmaf(s[c + 2 * e + 1], sl, -m_used));
+              lsum += p0 + p1;
+              r[e] = pack2<T>(p0, p1);
+            }
+            tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, r);
+          }
+          l += lsum;
+          if (__any_sync(0xffffffffu, rescale)) {
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
+                                                  ((k - 1) >> 1) & 1, abort, P.err_flags));
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < VG; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + C::kColO + c, r);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+                tmem_st16(lane_addr + C::kColO + c, r);
+              }
+            }
+          }
+          tmem_wait_st();
+        }
+        if (!ok) break;
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->p_full[sb]));
+        if (tid == 0) PA_TRACE_TILE(k, 1);
+      }
+
+      // ---- epilogue ----
+      if (tid == 0) PA_TRACE(5);
+      grid_dep_launch();
+      named_sync(2, 160);
+      ok = __all_sync(0xffffffffu, ok && !*abort);
+      if (ok)
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
+                                              ((n - 1) >> 1) & 1, abort, P.err_flags));
+      if (ok && live) {
+        tc_fence_after();
+        const bool bad = bars->bad != 0;
+        if (splits == 1) {
+          const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
+#pragma unroll 1
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              uint4 o[2];
+              uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                ow[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv,
+                                 __uint_as_float(r[2 * e + 1]) * inv);
+              uint4* dst = reinterpret_cast<uint4*>(out_row + (int64_t)row * vhs + g * VG + c);
+              dst[0] = o[0];
+              dst[1] = o[1];
+            }
+          }
+        } else {
+          float* wo = P.ws_o + (part * kRows + row) * VG;
+#pragma unroll 1
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              float4* dst = reinterpret_cast<float4*>(wo + c);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                     __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+          }
+          if (row < P.H) {
+            P.ws_ml[(part * kRows + row) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : m_used;
+            P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
+          }
+        }
+      }
+    } else if (warp == 4) {
+      // =================== TMA producer ===================
+      if (lane == 0) {  // this CTA's five query slabs (QR = 128 rows: the token's heads)
+        const uint32_t qb = smem_u32(&bars->q_tma);
+        mbar_expect_tx(qb, C::kQBytes);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(smem_u32(q_s) + q_full_off + j * C::kQBox, &qmap, (q_full0 + j) * 64,
+                      (int)(t * P.H), qb);
+        tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
+      }
+      const int nsub = N / P.box_rows;
+      const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int stage = k % STAGES;
+        if (k >= STAGES) {
+          bool okw = true;
+          if (lane == 0)
+            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
+                           P.err_flags);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
+        }
+        const int64_t j0 = (t_begin + k) * N;
+        int y = (int)P.num_slots;  // out of range: TMA fills zeros
+        if (lane < nsub) {
+          const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
+          if (key0 <= pos && key0 + P.box_rows - 1 >= lo) {
+            const int32_t phys = bt[key0 / P.bs];
+            if (phys >= 0 && phys < P.num_blocks) {
+              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
+            } else {
+              bars->bad = 1;
+              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+            }
+          }
+        }
+        if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
+        if (lane == 0) PA_TRACE_TILE(k, 5);
+        __syncwarp();
+        if (lane < nsub) {
+          const uint32_t full = smem_u32(&bars->full[stage]);
+          const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
+#pragma unroll 1
+          for (int j = 0; j < C::kSlabs; ++j)
+            tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+        }
+        issued = k + 1;
+        __syncwarp();
+      }
+      if (*abort && lane == 0) {
+        drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+          const int kl = issued - 1 - ((issued - 1 - st) % STAGES);
+          drain_wait(smem_u32(&bars->full[st]), (kl / STAGES) & 1, P.err_flags);
+        }
+      }
+      __syncwarp();
+      named_arrive(2, 160);
+    } else if (warp == 5) {
+      // =================== MMA issuer ===================
+      if (lane == 0) {
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
+        constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
+        const uint32_t q_base = smem_u32(q_s);
+        const uint32_t k_base = smem_u32(k_s);
+        bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
+        if (ok) {
+          tc_fence_after();
+          int kq = 0, kp = 0;
+          const uint64_t t0 = globaltimer();
+          uint32_t spins = 0;
+          while (kp < n) {
+            bool progressed = false;
+            if (kp < kq) {
+              const int stage = kp % STAGES, sb = kp & 1;
+              if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
+                tc_fence_after();
+                const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                  const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8, bdesc, kIdPV,
+                         (kp > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->pv_done[sb]));
+                tc_commit(smem_u32(&bars->empty[stage]));
+                PA_TRACE_TILE(kp, 3);
+                ++kp;
+                progressed = true;
+              }
+            }
+            if (kq < n && kq < kp + 2) {
+              const int stage = kq % STAGES, sb = kq & 1;
+              if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
+                  (kq < 2 || mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - 2) >> 1) & 1))) {
+                PA_TRACE_TILE(kq, 4);
+                tc_fence_after();
+                const uint32_t kb = k_base + stage * C::kStageBytes;
+#pragma unroll
+                for (int i = 0; i < C::kSteps; ++i) {
+                  // CTA g covers K steps [18g, 18g+18) = channels [288g, 288g+288):
+                  // the key operand is local slab e>>2, step e&3 (e = i + 2g); the
+                  // query operand is a full slab, or the 32-channel half slab.
+                  const int e = i + 2 * (int)g;
+                  const int kslab = e >> 2, w = (e & 3) * 32;
+                  const bool half = g ? (i < 2) : (i >= 16);
+                  uint64_t a;
+                  if (half) {
+                    a = sdesc64(q_base + q_half_off + (g ? i : i - 16) * 32);
+                  } else {
+                    const int j = g ? (i - 2) >> 2 : i >> 2;
+                    const int wq = (g ? (i - 2) & 3 : i & 3) * 32;
+                    a = sdesc(q_base + q_full_off + j * C::kQBox + wq, 16, 1024);
+                  }
+                  const uint64_t bdesc = sdesc(kb + kslab * C::kKBox + w, 16, 1024);
+                  mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, i > 0 ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->s_full[sb]));
+                PA_TRACE_TILE(kq, 2);
+                ++kq;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              spins = 0;
+              continue;
+            }
+            if ((++spins & 15u) == 0) {
+              if (*abort) { ok = false; break; }
+              if (globaltimer() - t0 > kWaitLimitNs * 4) {
+                *abort = 1;
+                raise_flag(P.err_flags, PA_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        tc_commit(smem_u32(&bars->drain));
+        drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
+      }
+      __syncwarp();
+    }
+  }
+
+  if (W.status != 0) grid_dep_launch();
+  if (tid == 0) PA_TRACE(6);
+  tc_fence_before();
+  cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (tid == 0) PA_TRACE(7);
+}
+
+template <typename T>
+cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
+  constexpr int N = 64, STAGES = 3;
+  using C = PairCfg<N, STAGES>;
+  const size_t smem = C::kSmemData + sizeof(PairBarriers) + 1024;
+  static bool configured[64] = {false};
+  auto kern = tc_pair_kernel<T, N, STAGES>;
+  if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[g.device] = true;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
+                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap map, qmap;
+  const cuuint64_t dims[2] = {576, (cuuint64_t)g.num_blocks * g.bs};
+  const cuuint64_t strides[1] = {576 * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cuuint64_t qdims[2] = {576, (cuuint64_t)a.num_tokens * g.H};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)kRows};
+  r = enc(&qmap, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // 32-channel boxes (64-byte rows, 64-byte swizzle) for the half query slab
+  CUtensorMap qmap64;
+  const cuuint32_t qbox64[2] = {32, (cuuint32_t)kRows};
+  r = enc(&qmap64, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox64, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(kThreads), smem, a.stream,
+                             map, qmap, qmap64, P);
+  if (e != cudaSuccess || ph != Phase::kDecode) return e;
+  return launch_pdl(tc_combine_kernel<T, 256, 2>, dim3((unsigned)nq, (unsigned)g.H), dim3(128), 0,
+                    a.stream, P);
+}
+
+template cudaError_t launch_pair<__nv_bfloat16>(const Geometry&, Phase, const ReadArgs&, Params&,
+                                                int64_t);
+template cudaError_t launch_pair<__half>(const Geometry&, Phase, const ReadArgs&, Params&,
+                                         int64_t);
+
+}  // namespace tc
+}  // namespace pa
+
+#ifdef PA_TC_TRACE
+extern "C" int pa_trace_pair_dump(void* host, void* tile_host) {
+  cudaMemcpyFromSymbol(tile_host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
+  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, sizeof(pa::tc::g_trace));
+}
+extern "C" int pa_trace_pair_clear(void) {
+  static unsigned long long zero[8192][16];  // >= sizeof either trace array
+  cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
+  return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
+}
+#endif
