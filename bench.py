@@ -319,12 +319,12 @@ def run_gpu_arm(args, rank, world, device):
     def decode():
         if nd > 0:
             op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                      d.block_table, out, 0, nd)
+                      d.block_table, out, 0, nd, after_write=True)
 
     def prefill():
         if nd < w.num_seqs:
             op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                       d.block_table, out, nd, w.num_seqs)
+                       d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
 
     def step():
         write()

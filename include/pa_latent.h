@@ -76,6 +76,16 @@ typedef enum pa_dtype {
 /* pa_latent_params.flags */
 #define PA_FLAG_PORTABLE 0x1 /* run the portable CUDA-core attention kernels even
                                 where a tensor-core kernel exists (verification aid) */
+/* PA_FLAG_AFTER_WRITE (read calls only; the write phase ignores it): the
+ * caller promises that this call is enqueued on the same stream directly
+ * after pa_latent_write of the same batch, with no other work in between.
+ * The read kernel may then start while the write kernel runs: it loads the
+ * query rows, sequence tables and rotary rows at once and waits for the
+ * write only before its first cache read. Without the flag the read kernel
+ * waits for all earlier work on the stream before touching any input. Set
+ * it on the first read call after the write only (a second read call
+ * follows a read, not the write). */
+#define PA_FLAG_AFTER_WRITE 0x2
 
 /*
  * Operator attributes and cache geometry (the PagedAttention node

@@ -36,6 +36,9 @@ class PagedLatentAttention:
         s = B.pa_latent_validate(self.params)
         if s != B.PA_OK:
             raise B.PaError(s, B.last_error())
+        # the same parameters for the first read call after the write phase
+        self.params_after_write = B.pa_latent_params.from_buffer_copy(self.params)
+        self.params_after_write.flags |= B.PA_FLAG_AFTER_WRITE
         self.device = torch.device(device)
         self.max_seqs, self.max_tokens = max_seqs, max_tokens
         self.workspace = B.alloc_workspace(self.params, max_seqs, max_tokens, self.device)
@@ -59,15 +62,21 @@ class PagedLatentAttention:
         B.pa_latent_write(self.params, key, cos_cache, sin_cache, slot_mapping, cumseq, past,
                           key_cache, self.err_flags, stream)
 
+    def _read_params(self, after_write: bool):
+        return self.params_after_write if after_write else self.params
+
     def decode(self, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
-               seq_begin=0, seq_end=None, stream=None):
-        B.pa_latent_decode(self.params, query, key_cache, cos_cache, sin_cache, cumseq, past,
+               seq_begin=0, seq_end=None, stream=None, after_write: bool = False):
+        """Decode phase over sequences [seq_begin, seq_end). ``after_write``:
+        this call directly follows ``write`` on the same stream (see
+        PA_FLAG_AFTER_WRITE)."""
+        B.pa_latent_decode(self._read_params(after_write), query, key_cache, cos_cache, sin_cache, cumseq, past,
                            block_table, out, seq_begin, seq_end, self.workspace,
                            self.err_flags, stream)
 
     def prefill(self, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
-                seq_begin=0, seq_end=None, stream=None):
-        B.pa_latent_prefill(self.params, query, key_cache, cos_cache, sin_cache, cumseq, past,
+                seq_begin=0, seq_end=None, stream=None, after_write: bool = False):
+        B.pa_latent_prefill(self._read_params(after_write), query, key_cache, cos_cache, sin_cache, cumseq, past,
                             block_table, out, seq_begin, seq_end, self.workspace,
                             self.err_flags, stream)
 
@@ -84,10 +93,10 @@ class PagedLatentAttention:
         self.write(key, cos_cache, sin_cache, slot_mapping, cumseq, past, key_cache, stream)
         if num_decode_seqs > 0:
             self.decode(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
-                        0, num_decode_seqs, stream)
+                        0, num_decode_seqs, stream, after_write=True)
         if num_decode_seqs < nseq:
             self.prefill(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
-                         num_decode_seqs, nseq, stream)
+                         num_decode_seqs, nseq, stream, after_write=num_decode_seqs == 0)
         return out
 
     def error_flags(self) -> int:

@@ -60,11 +60,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   // ---- prologue: warp 0 resolves the work while warps 1/5 set up ----
   // With programmatic dependent launch this CTA may start while the previous
   // kernel on the stream is still running: nothing reads inputs or writes
-  // outputs before griddepcontrol.wait returns. Dependents (the split
-  // combine) are released only when this CTA reaches its epilogue, so their
-  // waiting CTAs do not share the SM with the main loop.
+  // outputs before griddepcontrol.wait returns, except when P.early says that
+  // the previous kernel is this library's write phase; then only the cache
+  // rows it writes are off limits, and the producer waits before its first
+  // cache load. Dependents (the split combine) are released only when this
+  // CTA reaches its epilogue, so their waiting CTAs do not share the SM with
+  // the main loop.
   if (warp == 0) {
-    grid_dep_wait();
+    if (!P.early) grid_dep_wait();
     Work w;
     if (P.decode) {
       w = decode_plan_warp<N>(P, unit);
@@ -114,6 +117,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
     }
     if (lane == 0) work = w;
+    if (lane == 0) PA_TRACE(12);
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
@@ -138,7 +142,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp != 0) grid_dep_wait();  // every thread is ordered after the previous grid
+  if (warp != 0 && !P.early) grid_dep_wait();  // every thread is ordered after the previous grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -160,95 +164,106 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // =================== softmax / epilogue warps ===================
       const int row = tid;                 // TMEM lane == head
       const bool live = warp * 32 < P.H;   // warp holds at least one real head
-      // Q arrives by TMA in the 128B-swizzled K-major layout (slab s holds
-      // channels [64s, 64s+64); row r's 16-byte chunk c sits at c ^ (r&7));
-      // each thread then rotates its own row's rotary channels in place.
-      bool ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
-      if (ok && P.rd > 0 && row < P.H) {
-        const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
-        const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
-        auto at = [&](int d0) -> uint4* {
-          const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
-          return reinterpret_cast<uint4*>(q_s + slab * C::kQBox + row * 128 +
-                                          ((ch ^ (row & 7)) << 4));
-        };
-        if (!P.interleaved) {
-          const int half = P.rd >> 1;
-          for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
-            float a[8], bb[8], na[8], nb[8];
-            unpack8<T>(*at(d0), a);
-            unpack8<T>(*at(d0 + half), bb);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
-            rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
-            rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
-            *at(d0) = pack8<T>(na);
-            *at(d0 + half) = pack8<T>(nb);
-          }
-        } else {
-          for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
-            float a[8], dummy[8];
-            unpack8<T>(*at(d0), a);
-            rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
-            *at(d0) = pack8<T>(a);
-          }
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(smem_u32(&bars->q_full));
-      if (tid == 0) PA_TRACE(3);
-
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
       float m_used = -INFINITY, l = 0.f;
-      for (int k = 0; k < n && ok; ++k) {
+      bool ok = true;
+      // Pass k = -1 runs the tile code once with every wait, arrive, shared
+      // memory write and state update switched off, on whatever TMEM holds:
+      // it brings the loop's instructions into the instruction cache while
+      // the query and the first key tile are still in flight, instead of on
+      // the first tile's critical path. (The opaque start keeps the compiler
+      // from peeling it into a copy of its own.)
+      int k_first = -1;
+      asm volatile("" : "+r"(k_first));
+      for (int k = k_first; k < n && ok; ++k) {
+        const bool dry = k < 0;
+        if (k == 0) {  // every work item has n >= 1 tiles
+          // Q arrives by TMA in the 128B-swizzled K-major layout (slab s holds
+          // channels [64s, 64s+64); row r's 16-byte chunk c sits at c ^ (r&7));
+          // each thread then rotates its own row's rotary channels in place.
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+          if (ok && P.rd > 0 && row < P.H) {
+            const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
+            const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+            auto at = [&](int d0) -> uint4* {
+              const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
+              return reinterpret_cast<uint4*>(q_s + slab * C::kQBox + row * 128 +
+                                              ((ch ^ (row & 7)) << 4));
+            };
+            if (!P.interleaved) {
+              const int half = P.rd >> 1;
+              for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
+                float a[8], bb[8], na[8], nb[8];
+                unpack8<T>(*at(d0), a);
+                unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+                rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
+                rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
+                *at(d0) = pack8<T>(na);
+                *at(d0 + half) = pack8<T>(nb);
+              }
+            } else {
+              for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
+                float a[8], dummy[8];
+                unpack8<T>(*at(d0), a);
+                rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
+                *at(d0) = pack8<T>(a);
+              }
+            }
+          }
+          fence_proxy_async();
+          mbar_arrive(smem_u32(&bars->q_full));
+          if (tid == 0) PA_TRACE(3);
+          if (!ok) break;
+        }
         const int sb = k & 1;
         const int64_t j0 = (t_begin + k) * N;
-        const bool edge = j0 < lo || j0 + N - 1 > pos;   // uniform across the CTA
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
-        if (!ok) break;
-        if (tid == 0 && k == 0) PA_TRACE(4);
-        if (tid == 0) PA_TRACE_TILE(k, 0);
-        float s[N];
-        if (live) {
-          tc_fence_after();
-          uint32_t r[N / 32][32];
-#pragma unroll
-          for (int c = 0; c < N / 32; ++c)
-            tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < N / 32; ++c) {
-            reg_fence(r[c]);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
-          }
-          tc_fence_before();
+        const bool edge = !dry && (j0 < lo || j0 + N - 1 > pos);   // uniform across the CTA
+        if (!dry) {
+          ok = __all_sync(0xffffffffu,
+                          wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
+          if (!ok) break;
+          if (tid == 0 && k == 0) PA_TRACE(4);
+          if (tid == 0) PA_TRACE_TILE(k, 0);
         }
-        mbar_arrive(smem_u32(&bars->s_free[sb]));
-
+        // The tile is handled in 32-column chunks read from TMEM twice (row
+        // maximum, then exponentials), which keeps the loop body short:
+        // the first tile then does not wait long for its instructions.
         float factor = 1.f;
         bool rescale = false;
         // Scores in the log2 domain are x * sl (sl = scale*log2e) without
         // softcap; with softcap they are rewritten in place and sl = 1.
         const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        const uint32_t s_addr = lane_addr + C::kColS + sb * N;
         if (live) {
+          tc_fence_after();
           float mt = -INFINITY;
-          if (P.softcap_on) {
+          const bool rewrite = P.softcap_on || edge;
+#pragma unroll 1
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[32];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            if (rewrite) {
 #pragma unroll
-            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanhf(s[c] * P.cap_in);
-          }
-          if (edge) {
-#pragma unroll
-            for (int c = 0; c < N; ++c) {
-              const int64_t j = j0 + c;
-              if (j < lo || j > pos) s[c] = -INFINITY;
+              for (int e = 0; e < 32; ++e) {
+                float v = __uint_as_float(r[e]);
+                if (P.softcap_on) v = P.cap_out * tanhf(v * P.cap_in);
+                const int64_t j = j0 + c + e;
+                if (edge && (j < lo || j > pos)) v = -INFINITY;
+                r[e] = __float_as_uint(v);
+              }
+              tmem_st32(s_addr + c, r);
             }
-          }
 #pragma unroll
-          for (int c = 0; c < N; ++c) mt = fmaxf(mt, s[c]);
+            for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
+          }
+          if (rewrite) tmem_wait_st();
           mt *= sl;  // order-preserving (sl > 0)
-          if (k == 0) {
+          if (dry) {
+          } else if (k == 0) {
             m_used = mt;
           } else if (mt > m_used + kRescaleLog2) {
             factor = ex2(m_used - mt);
@@ -284,19 +299,22 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (live) {
           tc_fence_after();
           float lsum = 0.f;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < N; c += 32) {
-            uint32_t r[16];
+            uint32_t r[32], pk[16];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(s[c + 2 * e], sl, -m_used));
-              const float p1 = ex2(fmaf(s[c + 2 * e + 1], sl, -m_used));
+              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -m_used));
+              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -m_used));
               lsum += p0 + p1;
-              r[e] = pack2<T>(p0, p1);
+              pk[e] = pack2<T>(p0, p1);
             }
-            tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, r);
+            tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, pk);
           }
-          l += lsum;
+          if (!dry) l += lsum;
           if (__any_sync(0xffffffffu, rescale)) {
             // O may only be touched once PV(k-1) has completed.
             ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
@@ -318,6 +336,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         if (!ok) break;
         tc_fence_before();
+        if (dry) continue;
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
         mbar_arrive(smem_u32(&bars->p_full[sb]));
         if (tid == 0) PA_TRACE_TILE(k, 1);
       }
@@ -380,6 +400,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         for (int slab = 0; slab < C::kBoxes; ++slab)
           tma_load_2d(smem_u32(q_s) + slab * C::kQBox, &qmap, slab * 64, (int)(t * P.H), qb);
       }
+      if (P.early) grid_dep_wait();  // the write phase's cache rows are complete and visible
       const int nsub = N / P.box_rows;
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
       int issued = 0;
@@ -648,6 +669,7 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.window = g.window;
   P.decode = ph == Phase::kDecode ? 1 : 0;
   P.box_rows = s.n < g.bs ? s.n : g.bs;
+  P.early = (g.flags & PA_FLAG_AFTER_WRITE) ? 1 : 0;
   P.ws_o = nullptr;
   P.ws_ml = nullptr;
   P.ws_plan = nullptr;

@@ -119,6 +119,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+      "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+      "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+      "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -221,6 +232,8 @@ struct Params {
   int units;         // decode: CTA units (per value group) the grid provides
   int decode;
   int box_rows;      // rows per TMA box: min(N, bs)
+  int early;         // the previous kernel is the write phase: inputs other than
+                     // the cache may be read before griddepcontrol.wait
 };
 
 // QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
@@ -352,83 +365,96 @@ __device__ __forceinline__ int64_t decode_tiles(const Params& P, int b, int n_ti
   return pos / n_tile - lo / n_tile + 1;
 }
 
-__device__ __forceinline__ int64_t splits_of(int64_t tiles, int64_t T) {
-  // 32-bit division: tile counts and split lengths stay far below 2^31
-  return tiles <= 0 ? 1 : (int64_t)(((uint32_t)tiles + (uint32_t)T - 1u) / (uint32_t)T);
+// Splits of a sequence with `tiles` key tiles at split length T (a
+// sequence without tiles still takes one unit, which reports its error).
+__device__ __forceinline__ int ceil_div32(int a, int b) {
+  return (int)(((uint32_t)a + (uint32_t)b - 1u) / (uint32_t)b);
+}
+__device__ __forceinline__ int splits32(int tiles, int T) {
+  return tiles <= 0 ? 1 : ceil_div32(tiles, T);
 }
 
-__device__ __forceinline__ int64_t warp_sum64(int64_t v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
+// Sum over the warp of the splits of every sequence at split length T.
+// Lane l holds sequences l, l+32, ...; `own` is the tile count of sequence
+// l. Batches of up to 32 sequences are summed from registers alone.
+template <int N>
+__device__ __forceinline__ int warp_splits(const Params& P, int own, int T, int nseq,
+                                           int seq_begin) {
+  const int lane = threadIdx.x & 31;
+  int cnt = lane < nseq ? splits32(own, T) : 0;
+  if (nseq > 32) {
+    for (int i = lane + 32; i < nseq; i += 32)
+      cnt += splits32((int)decode_tiles(P, seq_begin + i, N), T);
+  }
+#pragma unroll 1
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  return cnt;
 }
 
-// Run by one full warp; returns the unit's plan in every lane.
+// Run by one full warp; returns the unit's plan in every lane. Units are
+// numbered lane by lane (lane 0's sequences first, each sequence's splits
+// consecutive), the same in every CTA. The code runs once per CTA, so it is
+// kept short: its instructions are fetched cold on every launch.
 template <int N>
 __device__ Work decode_plan_warp(const Params& P, int unit) {
-  constexpr int kCache = 8;  // sequences per lane kept in registers
   const int lane = threadIdx.x & 31;
-  const int nseq = P.seq_end - P.seq_begin;
-  const int chunk = (nseq + 31) / 32;
-  const int c0 = min(nseq, lane * chunk), c1 = min(nseq, c0 + chunk);
-  int64_t tl[kCache];
-#pragma unroll
-  for (int i = 0; i < kCache; ++i)
-    tl[i] = (c0 + i < c1) ? decode_tiles(P, P.seq_begin + c0 + i, N) : 0;
-  auto tiles_at = [&](int i) -> int64_t {
-    const int k = i - c0;
-    if (k < kCache) {
-      int64_t v = 0;
-#pragma unroll
-      for (int q = 0; q < kCache; ++q) v = (q == k) ? tl[q] : v;
-      return v;
-    }
-    return decode_tiles(P, P.seq_begin + i, N);
-  };
-  int64_t mx = 1;
-  for (int i = c0; i < c1; ++i) mx = max(mx, tiles_at(i));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  int64_t lo = 1, hi = mx;
-  while (lo < hi) {  // smallest T with sum_b splits_of(n_b, T) <= units
-    const int64_t mid = (lo + hi) >> 1;
-    int64_t cnt = 0;
-    for (int i = c0; i < c1; ++i) cnt += splits_of(tiles_at(i), mid);
-    if (warp_sum64(cnt) <= P.units) hi = mid; else lo = mid + 1;
+  const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin, units = P.units;
+  const int own = lane < nseq ? (int)decode_tiles(P, seq_begin + lane, N) : 0;
+  if (lane == 0) PA_TRACE(13);
+  // Smallest T with sum_b ceil(n_b / T) <= units. Since n_b / T <=
+  // ceil(n_b / T) <= n_b / T + 1, it lies in [ceil(total / units),
+  // ceil(total / (units - nseq))] (total = sum_b n_b; units >= nseq, and
+  // units == nseq forces T = the longest sequence), so a bisection over
+  // that bracket takes a step or two.
+  int total = lane < nseq ? max(own, 0) : 0, longest = total;
+  for (int i = lane + 32; i < nseq; i += 32) {
+    const int t = max((int)decode_tiles(P, seq_begin + i, N), 0);
+    total += t;
+    longest = max(longest, t);
   }
-  const int64_t T = lo;
-  int64_t mine = 0;
-  for (int i = c0; i < c1; ++i) mine += splits_of(tiles_at(i), T);
-  int64_t incl = mine;
-#pragma unroll
+#pragma unroll 1
+  for (int o = 16; o > 0; o >>= 1) {
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+  }
+  int lo = max(1, ceil_div32(total, units));
+  int hi = units > nseq ? max(lo, ceil_div32(total, units - nseq)) : max(lo, longest);
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (warp_splits<N>(P, own, mid, nseq, seq_begin) <= units) hi = mid; else lo = mid + 1;
+  }
+  const int T = lo;
+  if (lane == 0) PA_TRACE(14);
+  // this lane's units, then an exclusive scan over the lanes
+  int mine = 0;
+  for (int i = lane; i < nseq; i += 32)
+    mine += splits32(i == lane ? own : (int)decode_tiles(P, seq_begin + i, N), T);
+  int incl = mine;
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
-    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  int64_t run = incl - mine;
+  int run = incl - mine;
   Work w;
   w.status = 1;
   w.b = -1;
-  int hit = 0;
-  for (int i = c0; i < c1; ++i) {
-    const int64_t tiles = tiles_at(i);
-    const int64_t c = splits_of(tiles, T);
+  w.t_begin = w.t_end = 0;
+  int hit = 0, tiles_hit = 0;
+  for (int i = lane; i < nseq; i += 32) {
+    const int tiles = i == lane ? own : (int)decode_tiles(P, seq_begin + i, N);
+    const int c = splits32(tiles, T);
     if (unit >= run && unit < run + c) {
       hit = 1;
-      w.b = P.seq_begin + i;
-      w.split = (int)(unit - run);
-      w.splits = (int)c;
-      w.first = (int)run;
-      w.t_begin = w.t_end = 0;
-      if (tiles > 0) {
-        const int64_t pos = P.past[w.b];
-        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-        w.t_begin = lo_key / N + (int64_t)w.split * T;
-        w.t_end = min(pos / N + 1, w.t_begin + T);
-      }
+      tiles_hit = tiles;
+      w.b = seq_begin + i;
+      w.split = unit - run;
+      w.splits = c;
+      w.first = run;
     }
     run += c;
   }
+  if (lane == 0) PA_TRACE(15);
   const unsigned who = __ballot_sync(0xffffffffu, hit);
   if (who == 0) return w;  // idle unit
   const int src = __ffs(who) - 1;
@@ -436,8 +462,13 @@ __device__ Work decode_plan_warp(const Params& P, int unit) {
   w.split = __shfl_sync(0xffffffffu, w.split, src);
   w.splits = __shfl_sync(0xffffffffu, w.splits, src);
   w.first = __shfl_sync(0xffffffffu, w.first, src);
-  w.t_begin = __shfl_sync(0xffffffffu, w.t_begin, src);
-  w.t_end = __shfl_sync(0xffffffffu, w.t_end, src);
+  tiles_hit = __shfl_sync(0xffffffffu, tiles_hit, src);
+  if (tiles_hit > 0) {
+    const int64_t pos = P.past[w.b];
+    const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    w.t_begin = lo_key / N + (int64_t)w.split * T;
+    w.t_end = min(pos / N + 1, w.t_begin + T);
+  }
   w.status = 0;
   return w;
 }

@@ -111,6 +111,55 @@ def test_deterministic_and_graph_replay_bit_equal():
     assert op.error_flags() == 0
 
 
+@pytest.mark.parametrize("name", ["glm_decode", "mixed_serving", "dsv3_decode"])
+def test_after_write_flag_bit_equal(name):
+    """The first read call after the write phase may start early
+    (PA_FLAG_AFTER_WRITE); its output is bit-equal to the same calls made
+    without the flag, eagerly and inside a CUDA graph."""
+    w = Hn.workload(name)
+    d = w.to("cuda")
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    op = PagedLatentAttention.from_workload(w)
+    base = d.key_cache.clone()
+    shape = (w.num_tokens, w.num_heads * w.v_head_size)
+    nd = w.num_decode_seqs
+
+    def step(cache, out, flag):
+        op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
+        if nd > 0:
+            op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past, d.block_table,
+                      out, 0, nd, after_write=flag)
+        if nd < w.num_seqs:
+            op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                       d.block_table, out, nd, w.num_seqs, after_write=flag and nd == 0)
+
+    res = {}
+    for flag in (False, True):
+        cache = base.clone()
+        out = torch.full(shape, float("nan"), dtype=w.dtype, device="cuda")
+        step(cache, out, flag)
+        torch.cuda.synchronize()
+        res[flag] = (out.clone(), cache.clone())
+    assert torch.equal(res[False][0], res[True][0]) and torch.equal(res[False][1], res[True][1])
+    cache = base.clone()
+    out = torch.full(shape, float("nan"), dtype=w.dtype, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step(cache, out, True)   # eager warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(g):
+        step(cache, out, True)
+    for _ in range(2):
+        cache.copy_(base)
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, res[False][0]) and torch.equal(cache, res[False][1])
+    assert op.error_flags() == 0
+
+
 def _flag_case(mutate, expect_bit, phase="both"):
     w = W.make_workload("flags", q_lens=[1, 4], past_lens=[30, 10], num_heads=4, **W.GLM,
                         block_size=16, seed=25, cos_rows=64)
