@@ -70,7 +70,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if (!P.early) grid_dep_wait();
     Work w;
     if (P.decode) {
-      w = decode_plan_warp<N>(P, unit);
+      // the query region is free until the query load that follows the plan
+      w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), C::kQBytes / 4);
       if (w.status == 0) {
         const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
         if (lane == 0 && w.split == 0 && g == 0) P.ws_plan[w.b - P.seq_begin] = make_int2(w.first, w.splits);
@@ -117,6 +118,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
     }
     if (lane == 0) work = w;
+    fence_proxy_async();  // scratch stores before the query load reuses the region
     if (lane == 0) PA_TRACE(12);
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -479,14 +481,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
                 tc_fence_after();
                 const uint32_t vb = k_base + stage * C::kStageBytes + (g * (VG / 64)) * C::kKBox;
+                // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox
+                // apart (leading offset), 8-key groups 1024 bytes apart (stride).
+                // The descriptor's address field (bytes / 16) advances by 2048 / 16
+                // per 16 keys.
+                const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                  // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox
-                  // apart (leading offset), 8-key groups 1024 bytes apart (stride).
-                  const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
-                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8, bdesc, kIdPV,
-                         (kp > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < N / 16; ++kk)
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8,
+                         b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(smem_u32(&bars->pv_done[sb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
                 PA_TRACE_TILE(kp, 3);
@@ -502,12 +505,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 const uint32_t kb = k_base + stage * C::kStageBytes;
+                const uint64_t a0 = sdesc(q_base, 16, 1024), b0 = sdesc(kb, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < HS / 16; ++kk) {
-                  const int slab = kk >> 2, w = (kk & 3) * 32;
-                  const uint64_t a = sdesc(q_base + slab * C::kQBox + w, 16, 1024);
-                  const uint64_t bdesc = sdesc(kb + slab * C::kKBox + w, 16, 1024);
-                  mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, kk > 0 ? 1u : 0u);
+                  // step kk: slab kk/4, 32-byte column (kk%4) of the 128-byte rows
+                  const uint32_t col = (uint32_t)(kk & 3) * 2;  // 32 bytes / 16
+                  const uint32_t slab = (uint32_t)(kk >> 2);
+                  mma_ss(tmem + C::kColS + sb * N, a0 + (slab * (C::kQBox >> 4) + col),
+                         b0 + (slab * (C::kKBox >> 4) + col), kIdQK, kk > 0 ? 1u : 0u);
                 }
                 tc_commit(smem_u32(&bars->s_full[sb]));
                 PA_TRACE_TILE(kq, 2);

@@ -374,17 +374,25 @@ __device__ __forceinline__ int splits32(int tiles, int T) {
   return tiles <= 0 ? 1 : ceil_div32(tiles, T);
 }
 
+// Tile count of sequence i >= 32 (lane-strided beyond the first 32): from
+// the shared-memory scratch the plan filled, or reloaded past its capacity.
+template <int N>
+__device__ __forceinline__ int far_tiles(const Params& P, int i, int seq_begin, const int* more,
+                                         int cap) {
+  return i - 32 < cap ? more[i - 32] : (int)decode_tiles(P, seq_begin + i, N);
+}
+
 // Sum over the warp of the splits of every sequence at split length T.
 // Lane l holds sequences l, l+32, ...; `own` is the tile count of sequence
 // l. Batches of up to 32 sequences are summed from registers alone.
 template <int N>
 __device__ __forceinline__ int warp_splits(const Params& P, int own, int T, int nseq,
-                                           int seq_begin) {
+                                           int seq_begin, const int* more, int cap) {
   const int lane = threadIdx.x & 31;
   int cnt = lane < nseq ? splits32(own, T) : 0;
   if (nseq > 32) {
     for (int i = lane + 32; i < nseq; i += 32)
-      cnt += splits32((int)decode_tiles(P, seq_begin + i, N), T);
+      cnt += splits32(far_tiles<N>(P, i, seq_begin, more, cap), T);
   }
 #pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
@@ -394,9 +402,11 @@ __device__ __forceinline__ int warp_splits(const Params& P, int own, int T, int 
 // Run by one full warp; returns the unit's plan in every lane. Units are
 // numbered lane by lane (lane 0's sequences first, each sequence's splits
 // consecutive), the same in every CTA. The code runs once per CTA, so it is
-// kept short: its instructions are fetched cold on every launch.
+// kept short: its instructions are fetched cold on every launch. `more` is
+// shared-memory scratch for the tile counts of sequences 32.. (up to `cap`
+// of them), which later passes read instead of reloading them.
 template <int N>
-__device__ Work decode_plan_warp(const Params& P, int unit) {
+__device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) {
   const int lane = threadIdx.x & 31;
   const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin, units = P.units;
   const int own = lane < nseq ? (int)decode_tiles(P, seq_begin + lane, N) : 0;
@@ -408,10 +418,12 @@ __device__ Work decode_plan_warp(const Params& P, int unit) {
   // that bracket takes a step or two.
   int total = lane < nseq ? max(own, 0) : 0, longest = total;
   for (int i = lane + 32; i < nseq; i += 32) {
-    const int t = max((int)decode_tiles(P, seq_begin + i, N), 0);
-    total += t;
+    const int t = (int)decode_tiles(P, seq_begin + i, N);
+    if (i - 32 < cap) more[i - 32] = t;
+    total += max(t, 0);
     longest = max(longest, t);
   }
+  __syncwarp();
 #pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) {
     total += __shfl_xor_sync(0xffffffffu, total, o);
@@ -421,14 +433,14 @@ __device__ Work decode_plan_warp(const Params& P, int unit) {
   int hi = units > nseq ? max(lo, ceil_div32(total, units - nseq)) : max(lo, longest);
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    if (warp_splits<N>(P, own, mid, nseq, seq_begin) <= units) hi = mid; else lo = mid + 1;
+    if (warp_splits<N>(P, own, mid, nseq, seq_begin, more, cap) <= units) hi = mid; else lo = mid + 1;
   }
   const int T = lo;
   if (lane == 0) PA_TRACE(14);
   // this lane's units, then an exclusive scan over the lanes
   int mine = 0;
   for (int i = lane; i < nseq; i += 32)
-    mine += splits32(i == lane ? own : (int)decode_tiles(P, seq_begin + i, N), T);
+    mine += splits32(i == lane ? own : far_tiles<N>(P, i, seq_begin, more, cap), T);
   int incl = mine;
 #pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
@@ -442,7 +454,7 @@ __device__ Work decode_plan_warp(const Params& P, int unit) {
   w.t_begin = w.t_end = 0;
   int hit = 0, tiles_hit = 0;
   for (int i = lane; i < nseq; i += 32) {
-    const int tiles = i == lane ? own : (int)decode_tiles(P, seq_begin + i, N);
+    const int tiles = i == lane ? own : far_tiles<N>(P, i, seq_begin, more, cap);
     const int c = splits32(tiles, T);
     if (unit >= run && unit < run + c) {
       hit = 1;

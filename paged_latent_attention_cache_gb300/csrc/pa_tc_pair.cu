@@ -152,7 +152,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     grid_dep_wait();
     Work w;
     if (P.decode) {
-      w = decode_plan_warp<N>(P, unit);
+      // the query region is free until the query load that follows the plan
+      w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), C::kQBytes / 4);
       if (w.status == 0) {
         const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
         if (lane == 0 && w.split == 0 && g == 0)
@@ -200,6 +201,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
     }
     if (lane == 0) work = w;
+    fence_proxy_async();  // scratch stores before the query load reuses the region
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
@@ -581,12 +583,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
                 tc_fence_after();
                 const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
+                // descriptor address field (bytes / 16) advances 2048 / 16 per 16
+                // keys
+                const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk) {
-                  const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
-                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8, bdesc, kIdPV,
-                         (kp > 0 || kk > 0) ? 1u : 0u);
-                }
+                for (int kk = 0; kk < N / 16; ++kk)
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8,
+                         b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(smem_u32(&bars->pv_done[sb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
                 PA_TRACE_TILE(kp, 3);
@@ -601,24 +604,29 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 const uint32_t kb = k_base + stage * C::kStageBytes;
+                // Descriptors built once; per step only the address field
+                // (bytes / 16) moves.
+                const uint64_t b0 = sdesc(kb, 16, 1024);
+                const uint64_t af0 = sdesc(q_base + q_full_off, 16, 1024);
+                const uint64_t ah0 = sdesc64(q_base + q_half_off);
 #pragma unroll
                 for (int i = 0; i < C::kSteps; ++i) {
                   // CTA g covers K steps [18g, 18g+18) = channels [288g, 288g+288):
                   // the key operand is local slab e>>2, step e&3 (e = i + 2g); the
                   // query operand is a full slab, or the 32-channel half slab.
                   const int e = i + 2 * (int)g;
-                  const int kslab = e >> 2, w = (e & 3) * 32;
+                  const uint32_t kslab = (uint32_t)(e >> 2), w = (uint32_t)(e & 3) * 2;
                   const bool half = g ? (i < 2) : (i >= 16);
                   uint64_t a;
                   if (half) {
-                    a = sdesc64(q_base + q_half_off + (g ? i : i - 16) * 32);
+                    a = ah0 + (uint64_t)((g ? i : i - 16) * 2);
                   } else {
-                    const int j = g ? (i - 2) >> 2 : i >> 2;
-                    const int wq = (g ? (i - 2) & 3 : i & 3) * 32;
-                    a = sdesc(q_base + q_full_off + j * C::kQBox + wq, 16, 1024);
+                    const uint32_t j = (uint32_t)(g ? (i - 2) >> 2 : i >> 2);
+                    const uint32_t wq = (uint32_t)(g ? (i - 2) & 3 : i & 3) * 2;
+                    a = af0 + (j * (C::kQBox >> 4) + wq);
                   }
-                  const uint64_t bdesc = sdesc(kb + kslab * C::kKBox + w, 16, 1024);
-                  mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, i > 0 ? 1u : 0u);
+                  mma_ss(tmem + C::kColS + sb * N, a, b0 + (kslab * (C::kKBox >> 4) + w), kIdQK,
+                         i > 0 ? 1u : 0u);
                 }
                 tc_commit(smem_u32(&bars->s_full[sb]));
                 PA_TRACE_TILE(kq, 2);

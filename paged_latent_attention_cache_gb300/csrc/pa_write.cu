@@ -13,6 +13,11 @@
 
 namespace pa {
 
+// Largest batch whose cumulative offsets are staged in shared memory (the
+// token -> sequence search then runs on chip instead of as a chain of
+// dependent global loads).
+constexpr int kStagedSeqs = 8191;
+
 template <typename T>
 __global__ void __launch_bounds__(256)
 latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
@@ -25,13 +30,31 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
   // start its prologue now; it waits (griddepcontrol.wait) for this grid to
   // complete before it reads the cache.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ int32_t s_cum[];  // cumseq[0..num_seqs] when staged
+  const bool staged = num_seqs <= kStagedSeqs;
+  if (staged) {
+    for (int i = threadIdx.x; i <= num_seqs; i += blockDim.x) s_cum[i] = cumseq[i];
+    __syncthreads();
+  }
+  const int32_t* cum = staged ? s_cum : cumseq;
   const int groups = hs >> 3;
   const int64_t total = num_tokens * groups;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / groups;
     const int g = (int)(i - t * groups);
+    const int d0 = g << 3;
+    const T* row = key + t * hs;
+    // loads that depend on nothing else go out first
     const int32_t slot = slot_mapping[t];
+    uint4 v = *reinterpret_cast<const uint4*>(row + d0);
+    const bool rot = rd > 0 && d0 >= ro && d0 < ro + rd;
+    uint4 vp = v;
+    if (rot && !interleaved) {
+      const int half = rd >> 1;
+      const int dp = (d0 - ro < half) ? d0 + half : d0 - half;
+      vp = *reinterpret_cast<const uint4*>(row + dp);
+    }
     if (slot < 0) {
       if (slot < -1 && g == 0) raise_flag(err_flags, PA_DEVERR_SLOT);
       continue;
@@ -42,23 +65,16 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
     }
     int32_t b;
     int64_t pos;
-    if (!locate_token(t, cumseq, past, num_seqs, g == 0 ? err_flags : nullptr, &b, &pos))
+    if (!locate_token(t, cum, past, num_seqs, g == 0 ? err_flags : nullptr, &b, &pos))
       continue;
     if (rd > 0 && (pos < 0 || pos >= cos_rows)) {  // whole row skipped
       if (g == 0) raise_flag(err_flags, pos < 0 ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
       continue;
     }
-    const T* row = key + t * hs;
-    const int d0 = g << 3;
-    uint4 v = *reinterpret_cast<const uint4*>(row + d0);
-    if (rd > 0 && d0 >= ro && d0 < ro + rd) {
+    if (rot) {
       float x[8], xp[8];
       unpack8<T>(v, x);
-      if (!interleaved) {
-        const int half = rd >> 1;
-        const int dp = (d0 - ro < half) ? d0 + half : d0 - half;
-        unpack8<T>(*reinterpret_cast<const uint4*>(row + dp), xp);
-      }
+      unpack8<T>(vp, xp);
       const T* crow = cos_cache + pos * (rd >> 1);
       const T* srow = sin_cache + pos * (rd >> 1);
       rope8<T>(x, xp, d0, ro, rd, interleaved, crow, srow);
@@ -80,14 +96,15 @@ cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
   const int64_t cap = (int64_t)g.num_sms * 16;
   if (blocks > cap) blocks = cap;
   const int64_t num_slots = (int64_t)g.num_blocks * g.bs;
+  const size_t smem = num_seqs <= kStagedSeqs ? (size_t)(num_seqs + 1) * sizeof(int32_t) : 0;
   if (g.dtype == PA_DTYPE_BF16) {
-    latent_write_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, stream>>>(
+    latent_write_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, smem, stream>>>(
         (const __nv_bfloat16*)key, (const __nv_bfloat16*)cos_cache,
         (const __nv_bfloat16*)sin_cache, slot_mapping, cumseq, past, num_seqs,
         (__nv_bfloat16*)key_cache, num_tokens, g.hs, g.ro, g.rd, g.interleaved, g.cos_rows,
         num_slots, err_flags);
   } else {
-    latent_write_kernel<__half><<<(unsigned)blocks, threads, 0, stream>>>(
+    latent_write_kernel<__half><<<(unsigned)blocks, threads, smem, stream>>>(
         (const __half*)key, (const __half*)cos_cache, (const __half*)sin_cache, slot_mapping,
         cumseq, past, num_seqs, (__half*)key_cache, num_tokens, g.hs, g.ro, g.rd,
         g.interleaved, g.cos_rows, num_slots, err_flags);
