@@ -84,7 +84,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         } else {
           w.t = q0;
           w.pos = P.past[w.b];
+          w.ntok = 1;
         }
+      }
+    } else if (P.tpc > 1) {
+      w = prefill_group_warp(P, unit, P.tpc);
+      if (w.status == 0) {
+        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, w.pos - P.window) : 0;
+        w.t_begin = lo_key / N;
+        w.t_end = (w.pos + w.ntok - 1) / N + 1;
       }
     } else {
       int32_t b;
@@ -98,19 +106,23 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         w.b = b;
         w.t = unit;
         w.pos = pos;
+        w.ntok = 1;
         const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
         w.t_begin = lo_key / N;
         w.t_end = pos / N + 1;
       }
     }
     if (w.status == 0) {
-      const bool bad_ctx = P.past[w.b] < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
-      const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
+      const int64_t pos_hi = w.pos + w.ntok - 1;  // the unit's last token
+      const bool bad_ctx = P.past[w.b] < 0 || pos_hi >= (int64_t)P.max_blocks * P.bs ||
+                           w.t + w.ntok > P.num_tokens;
+      const bool bad_pos = P.rd > 0 && pos_hi >= P.cos_rows;
       if (bad_ctx || bad_pos) {
         if (lane == 0 && g == 0)
           raise_flag(P.err_flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
         T* out_row = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs;
-        for (int i = lane; i < P.H * VG; i += 32) {
+        const int rows = min((int64_t)w.ntok, P.num_tokens - w.t) * P.H;
+        for (int i = lane; i < rows * VG; i += 32) {
           const int h = i / VG, c = i % VG;
           out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
         }
@@ -154,18 +166,27 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) PA_TRACE(1);
 
   if (W.status == 0) {
+    // The unit's rows are ntok consecutive tokens' heads (row r: token t +
+    // r / H at position pos + r / H). Keys any row sees lie in [lo, pos_hi];
+    // every row sees at least [lo_hi, pos].
     const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
     const int32_t b = W.b;
-    const int splits = W.splits;
+    const int splits = W.splits, ntok = W.ntok, rows = W.ntok * P.H;
+    const int64_t pos_hi = pos + ntok - 1;
     const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    const int64_t lo_hi = P.window >= 0 ? max((int64_t)0, pos_hi - P.window) : 0;
     const int n = (int)max((int64_t)0, W.t_end - t_begin);
     const int64_t part = (int64_t)unit * G + g;  // partial slot (decode splits)
     T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
 
     if (warp < 4) {
       // =================== softmax / epilogue warps ===================
-      const int row = tid;                 // TMEM lane == head
-      const bool live = warp * 32 < P.H;   // warp holds at least one real head
+      const int row = tid;                 // TMEM lane == query row
+      const bool live = warp * 32 < rows;  // warp holds at least one real row
+      // this row's token position and first visible key (rows past the unit:
+      // nothing visible)
+      const int64_t pos_r = row < rows ? pos + row / P.H : -1;
+      const int64_t lo_r = P.window >= 0 ? max((int64_t)0, pos_r - P.window) : 0;
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
       float m_used = -INFINITY, l = 0.f;
       bool ok = true;
@@ -184,9 +205,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // channels [64s, 64s+64); row r's 16-byte chunk c sits at c ^ (r&7));
           // each thread then rotates its own row's rotary channels in place.
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
-          if (ok && P.rd > 0 && row < P.H) {
-            const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
-            const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+          if (ok && P.rd > 0 && row < rows) {
+            const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos_r * (P.rd >> 1);
+            const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos_r * (P.rd >> 1);
             auto at = [&](int d0) -> uint4* {
               const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
               return reinterpret_cast<uint4*>(q_s + slab * C::kQBox + row * 128 +
@@ -221,7 +242,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         const int sb = k & 1;
         const int64_t j0 = (t_begin + k) * N;
-        const bool edge = !dry && (j0 < lo || j0 + N - 1 > pos);   // uniform across the CTA
+        // a tile with keys that some row must not see (uniform across the CTA)
+        const bool edge = !dry && (j0 < lo_hi || j0 + N - 1 > pos);
         if (!dry) {
           ok = __all_sync(0xffffffffu,
                           wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
@@ -254,7 +276,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 float v = __uint_as_float(r[e]);
                 if (P.softcap_on) v = P.cap_out * tanhf(v * P.cap_in);
                 const int64_t j = j0 + c + e;
-                if (edge && (j < lo || j > pos)) v = -INFINITY;
+                if (edge && (j < lo_r || j > pos_r)) v = -INFINITY;
                 r[e] = __float_as_uint(v);
               }
               tmem_st32(s_addr + c, r);
@@ -267,7 +289,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (dry) {
           } else if (k == 0) {
             m_used = mt;
-          } else if (mt > m_used + kRescaleLog2) {
+          } else if (mt > m_used + kRescaleLog2) {  // (also when no key was visible before)
             factor = ex2(m_used - mt);
             m_used = mt;
             l *= factor;
@@ -275,8 +297,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
 
-        // Keys outside [lo, pos] in a boundary tile: zero their value rows so
-        // stale or unwritten cache slots cannot reach the PV product.
+        // Keys no row sees (outside [lo, pos_hi]) in a boundary tile: zero
+        // their value rows so stale or unwritten cache slots cannot reach
+        // the PV product (rows that mask a key seen by another row give it
+        // probability 0, and its value row is a written, finite row).
         if (edge) {
           uint8_t* kst = k_s + (k % STAGES) * C::kStageBytes;
           constexpr int kVSlabs = VG / 64;
@@ -285,7 +309,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             const int rem = i - rr * (kVSlabs * 8);
             const int slab = g * kVSlabs + rem / 8, ch = rem & 7;
             const int64_t j = j0 + rr;
-            if (j < lo || j > pos)
+            if (j < lo || j > pos_hi)
               *reinterpret_cast<uint4*>(kst + slab * C::kKBox + rr * 128 + ch * 16) =
                   make_uint4(0, 0, 0, 0);
           }
@@ -301,6 +325,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (live) {
           tc_fence_after();
           float lsum = 0.f;
+          // a row that has seen no key yet (several tokens per unit, window)
+          // has every score at -inf: its probabilities are 0, not NaN
+          const float mu = m_used == -INFINITY ? 0.f : m_used;
 #pragma unroll 1
           for (int c = 0; c < N; c += 32) {
             uint32_t r[32], pk[16];
@@ -309,8 +336,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             reg_fence(r);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -m_used));
-              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -m_used));
+              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -mu));
+              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -mu));
               lsum += p0 + p1;
               pk[e] = pack2<T>(p0, p1);
             }
@@ -361,7 +388,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           for (int c = 0; c < VG; c += 16) {
             uint32_t r[16];
             tmem_ld16(lane_addr + C::kColO + c, r);
-            if (row < P.H) {
+            if (row < rows) {
               uint4 o[2];
               uint32_t* ow = reinterpret_cast<uint32_t*>(o);
 #pragma unroll
@@ -379,7 +406,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           for (int c = 0; c < VG; c += 16) {
             uint32_t r[16];
             tmem_ld16(lane_addr + C::kColO + c, r);
-            if (row < P.H) {
+            if (row < rows) {
               float4* dst = reinterpret_cast<float4*>(wo + c);
 #pragma unroll
               for (int e = 0; e < 4; ++e)
@@ -387,7 +414,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                                      __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
             }
           }
-          if (row < P.H) {
+          if (row < rows) {
             // a NaN max marks a split that read an invalid block
             P.ws_ml[(part * kRows + row) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : m_used;
             P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
@@ -422,7 +449,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
         if (lane < nsub) {
           const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
-          if (key0 <= pos && key0 + P.box_rows - 1 >= lo) {
+          if (key0 <= pos_hi && key0 + P.box_rows - 1 >= lo) {
             const int32_t phys = bt[key0 / P.bs];
             if (phys >= 0 && phys < P.num_blocks) {
               y = (int)((int64_t)phys * P.bs + key0 % P.bs);
@@ -558,10 +585,14 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-bool pick(const Geometry& g, Shape* s) {
+bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.H > kRows) return false;
   if (g.hs == 192 && g.vhs == 128) {
-    *s = g.H <= 64 ? Shape{192, 128, 1, 128, 4, 64} : Shape{192, 128, 1, 128, 3, 128};
+    // Decode with H <= 64 keeps a 64-row query tile and four key stages;
+    // otherwise (and for prefill, whose units hold 128 / H tokens) the
+    // query tile has 128 rows and there are three stages.
+    *s = (ph == Phase::kDecode && g.H <= 64) ? Shape{192, 128, 1, 128, 4, 64}
+                                             : Shape{192, 128, 1, 128, 3, 128};
     return true;
   }
   if (g.hs == 576 && g.vhs == 512) {
@@ -620,30 +651,35 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
 }  // namespace tc
 
 bool tc_supported(const Geometry& g, Phase ph) {
-  (void)ph;
   tc::Shape s;
-  return tc::pick(g, &s);
+  return tc::pick(g, ph, &s);
 }
 
 size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t num_tokens) {
   (void)num_tokens;
   tc::Shape s;
-  if (ph == Phase::kPrefill || num_seqs <= 0 || !tc::pick(g, &s)) return 0;
+  if (ph == Phase::kPrefill || num_seqs <= 0 || !tc::pick(g, ph, &s)) return 0;
   return tc::decode_ws_bytes(s, tc::decode_units(g, s, num_seqs), num_seqs);
 }
 
 size_t tc_call_workspace(const Geometry& g, Phase ph, const ReadArgs& a) {
   tc::Shape s;
-  if (ph == Phase::kPrefill || !tc::pick(g, &s)) return 0;
+  if (ph == Phase::kPrefill || !tc::pick(g, ph, &s)) return 0;
   const int64_t nq = (int64_t)(a.seq_end - a.seq_begin);
   return tc::decode_ws_bytes(s, tc::decode_units(g, s, nq), nq);
 }
 
 cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   tc::Shape s;
-  if (!tc::pick(g, &s)) return cudaErrorNotSupported;
-  const int64_t nq = ph == Phase::kDecode ? (int64_t)(a.seq_end - a.seq_begin) : a.num_tokens;
-  if (nq <= 0) return cudaSuccess;
+  if (!tc::pick(g, ph, &s)) return cudaErrorNotSupported;
+  // prefill units: 128 / H consecutive tokens of one sequence (one token on
+  // the CTA pair); at most ceil(T / tpc) + nseq units are needed
+  const int tpc = (ph == Phase::kPrefill && s.groups == 1) ? tc::kRows / g.H : 1;
+  const int64_t nseq = (int64_t)(a.seq_end - a.seq_begin);
+  const int64_t nq = ph == Phase::kDecode ? nseq
+                     : tpc > 1             ? (a.num_tokens + tpc - 1) / tpc + nseq
+                                           : a.num_tokens;
+  if (nq <= 0 || (ph == Phase::kPrefill && a.num_tokens <= 0)) return cudaSuccess;
   tc::Params P;
   P.query = a.query;
   P.out = a.out;
@@ -675,6 +711,7 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.decode = ph == Phase::kDecode ? 1 : 0;
   P.box_rows = s.n < g.bs ? s.n : g.bs;
   P.early = (g.flags & PA_FLAG_AFTER_WRITE) ? 1 : 0;
+  P.tpc = tpc;
   P.ws_o = nullptr;
   P.ws_ml = nullptr;
   P.ws_plan = nullptr;

@@ -234,6 +234,7 @@ struct Params {
   int box_rows;      // rows per TMA box: min(N, bs)
   int early;         // the previous kernel is the write phase: inputs other than
                      // the cache may be read before griddepcontrol.wait
+  int tpc;           // prefill: consecutive tokens per work unit (rows = tpc * H <= 128)
 };
 
 // QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
@@ -271,8 +272,9 @@ struct Barriers {
 
 // Resolved work of one CTA (written by warp 0 during the prologue).
 struct Work {
-  int64_t t, pos, t_begin, t_end;
+  int64_t t, pos, t_begin, t_end;  // t, pos: the unit's first token and its position
   int b, splits, first, split;
+  int ntok;    // consecutive tokens of sequence b in the unit (rows = ntok * H)
   int status;  // 0 = run, 1 = idle, 2 = error already reported (write nothing more)
 };
 
@@ -488,6 +490,51 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
 // Merges the key splits of each decode sequence (plan written by the
 // attention kernel): M = max_s m_s, out = sum_s 2^(m_s-M) O_s / sum_s
 // 2^(m_s-M) l_s; zero when a split read an invalid block.
+// Prefill work unit `unit` with up to `tpc` consecutive tokens of one
+// sequence per unit (the query tile then holds tpc tokens' heads, which share
+// every key tile). Sequences of [seq_begin, seq_end) get ceil(q_b / tpc)
+// units each, numbered in sequence order; run by one full warp.
+__device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, int tpc) {
+  const int lane = threadIdx.x & 31;
+  const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin;
+  Work w;
+  w.status = 1;
+  w.splits = 1;
+  w.ntok = 0;
+  int run = 0;
+  for (int base = 0; base < nseq; base += 32) {
+    const int i = base + lane;
+    int cnt = 0, q0 = 0, q = 0;
+    if (i < nseq) {
+      q0 = P.cumseq[seq_begin + i];
+      q = P.cumseq[seq_begin + i + 1] - q0;
+      cnt = q > 0 ? ceil_div32(q, tpc) : 0;
+    }
+    int incl = cnt;
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int start = run + incl - cnt;
+    const unsigned who = __ballot_sync(0xffffffffu, cnt > 0 && unit >= start && unit < start + cnt);
+    if (who) {
+      const int src = __ffs(who) - 1;
+      const int grp = __shfl_sync(0xffffffffu, unit - start, src);
+      const int first = __shfl_sync(0xffffffffu, q0, src);
+      const int len = __shfl_sync(0xffffffffu, q, src);
+      w.b = seq_begin + base + src;
+      w.t = first + (int64_t)grp * tpc;
+      w.ntok = min(tpc, len - grp * tpc);
+      w.pos = (int64_t)P.past[w.b] + grp * tpc;
+      w.status = 0;
+      return w;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return w;  // idle unit
+}
+
 template <typename T, int VG, int G>
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ Params P) {
   grid_dep_wait();  // the attention kernel's partials are complete and visible
