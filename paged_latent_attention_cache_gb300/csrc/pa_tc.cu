@@ -274,7 +274,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
                 float v = __uint_as_float(r[e]);
-                if (P.softcap_on) v = P.cap_out * tanhf(v * P.cap_in);
+                if (P.softcap_on) v = P.cap_out * tanh_ex2(v * P.cap_in);
                 const int64_t j = j0 + c + e;
                 if (edge && (j < lo_r || j > pos_r)) v = -INFINITY;
                 r[e] = __float_as_uint(v);

@@ -170,6 +170,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// tanh from its definition, tanh(y) = 1 - 2 / (1 + e^(2y)), with one
+// ex2.approx and one rcp.approx: absolute error about 1e-7 (the final
+// subtraction's rounding), so a softcapped score c*tanh(s/c) is off by
+// about c * 1e-7. Saturates to +-1 (e^(2y) -> inf gives 1 - 0, -> 0 gives -1).
+__device__ __forceinline__ float tanh_ex2(float y) {
+  const float e = ex2(y * (2.f * kLog2e));
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return fmaf(-2.f, r, 1.f);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format):
 // start address, leading / stride byte offsets (>> 4), version 1, layout 2.
 __device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {

@@ -377,7 +377,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           float mt = -INFINITY;
           if (P.softcap_on) {
 #pragma unroll
-            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanhf(s[c] * P.cap_in);
+            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanh_ex2(s[c] * P.cap_in);
           }
           if (edge) {
 #pragma unroll
