@@ -86,6 +86,15 @@ typedef enum pa_dtype {
  * it on the first read call after the write only (a second read call
  * follows a read, not the write). */
 #define PA_FLAG_AFTER_WRITE 0x2
+/* PA_FLAG_OWN_SLOTS (read calls, together with PA_FLAG_AFTER_WRITE): the
+ * caller promises that every slot_mapping[t] >= 0 of the preceding write is
+ * the cache row of token t's own position in its own sequence
+ * (block_table[b][pos / bs] * bs + pos % bs), and that no sequence of this
+ * read reads a row another sequence's token writes. The rows a sequence b
+ * reads below its first new position past[b] are then untouched by the
+ * write, and the read kernel loads them without waiting for the write
+ * kernel; it waits only before the tiles at or after past[b]. */
+#define PA_FLAG_OWN_SLOTS 0x4
 
 /*
  * Operator attributes and cache geometry (the PagedAttention node

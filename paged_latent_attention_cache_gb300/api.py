@@ -21,7 +21,8 @@ class PagedLatentAttention:
                  rotary_interleaved: int = 0, cos_rows: int = 1, block_size: int,
                  num_blocks: int, max_blocks_per_seq: int, scale: float = 0.0,
                  softcap: float = 0.0, local_window_size: int = -1, max_seqs: int,
-                 max_tokens: int, device="cuda", portable: bool = False):
+                 max_tokens: int, device="cuda", portable: bool = False,
+                 own_slots: bool = False):
         self.dtype = dtype
         self.num_heads = num_heads
         self.head_size = head_size
@@ -37,22 +38,29 @@ class PagedLatentAttention:
         if s != B.PA_OK:
             raise B.PaError(s, B.last_error())
         # the same parameters for the first read call after the write phase
+        # (own_slots: every slot is its token's own position, see
+        # PA_FLAG_OWN_SLOTS)
         self.params_after_write = B.pa_latent_params.from_buffer_copy(self.params)
-        self.params_after_write.flags |= B.PA_FLAG_AFTER_WRITE
+        self.params_after_write.flags |= B.PA_FLAG_AFTER_WRITE | (
+            B.PA_FLAG_OWN_SLOTS if own_slots else 0)
         self.device = torch.device(device)
         self.max_seqs, self.max_tokens = max_seqs, max_tokens
         self.workspace = B.alloc_workspace(self.params, max_seqs, max_tokens, self.device)
         self.err_flags = torch.zeros(1, dtype=torch.int32, device=self.device)
 
     @classmethod
-    def from_workload(cls, w, device="cuda", portable=False) -> "PagedLatentAttention":
+    def from_workload(cls, w, device="cuda", portable=False,
+                      own_slots=True) -> "PagedLatentAttention":
+        """Operator for a generated workload; its slot mappings point every
+        token at its own position (see ``workloads.make_workload``)."""
         return cls(dtype=w.dtype, num_heads=w.num_heads, head_size=w.head_size,
                    v_head_size=w.v_head_size, rotary_offset=w.rotary_offset,
                    rotary_dim=w.rotary_dim, rotary_interleaved=w.rotary_interleaved,
                    cos_rows=w.cos_rows, block_size=w.block_size, num_blocks=w.num_blocks,
                    max_blocks_per_seq=w.max_blocks_per_seq, scale=w.scale, softcap=w.softcap,
                    local_window_size=w.local_window_size, max_seqs=w.num_seqs,
-                   max_tokens=max(w.num_tokens, 1), device=device, portable=portable)
+                   max_tokens=max(w.num_tokens, 1), device=device, portable=portable,
+                   own_slots=own_slots)
 
     def kernel_family(self, phase: int) -> int:
         return B.pa_latent_kernel_family(self.params, phase)

@@ -38,6 +38,7 @@ PA_DEVERR_TIMEOUT = 0x40
 
 PA_FLAG_PORTABLE = 0x1
 PA_FLAG_AFTER_WRITE = 0x2
+PA_FLAG_OWN_SLOTS = 0x4
 
 EXPORTED = ("pa_latent_validate", "pa_latent_write", "pa_latent_decode", "pa_latent_prefill",
             "pa_latent_decode_noalloc", "pa_latent_workspace_size", "pa_latent_kernel_family",

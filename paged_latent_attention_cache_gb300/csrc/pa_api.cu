@@ -102,7 +102,7 @@ pa_status resolve(const pa_latent_params* p, Geometry* g) {
     scale = 1.0f / sqrtf((float)hs);
   }
   if (!isfinite(p->softcap)) return fail(PA_ERR_INVALID_ARGUMENT, "softcap must be finite");
-  if (p->flags & ~(PA_FLAG_PORTABLE | PA_FLAG_AFTER_WRITE))
+  if (p->flags & ~(PA_FLAG_PORTABLE | PA_FLAG_AFTER_WRITE | PA_FLAG_OWN_SLOTS))
     return fail(PA_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", p->flags);
 
   g->dtype = p->dtype;

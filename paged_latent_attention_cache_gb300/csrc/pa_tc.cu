@@ -429,12 +429,21 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         for (int slab = 0; slab < C::kBoxes; ++slab)
           tma_load_2d(smem_u32(q_s) + slab * C::kQBox, &qmap, slab * 64, (int)(t * P.H), qb);
       }
-      if (P.early) grid_dep_wait();  // the write phase's cache rows are complete and visible
+      // With P.early the write grid may still run: cache rows are read only
+      // after griddepcontrol.wait, except (P.own_slots) the tiles below the
+      // sequence's first new position, which the write does not touch.
+      int dirty_from = 0;
+      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, P.past[b] / N - t_begin);
+      bool waited = !P.early;
       const int nsub = N / P.box_rows;
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int stage = k % STAGES;
+        if (!waited && k >= dirty_from) {
+          grid_dep_wait();  // the write phase's cache rows are complete and visible
+          waited = true;
+        }
         if (k >= STAGES) {
           bool okw = true;
           if (lane == 0)
@@ -472,6 +481,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         issued = k + 1;
         __syncwarp();
       }
+      if (!waited) grid_dep_wait();  // the grid completes after the write grid
       if (*abort && lane == 0) {
         // copies still in flight must land before the CTA exits
         drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
@@ -712,6 +722,7 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.box_rows = s.n < g.bs ? s.n : g.bs;
   P.early = (g.flags & PA_FLAG_AFTER_WRITE) ? 1 : 0;
   P.tpc = tpc;
+  P.own_slots = (g.flags & PA_FLAG_OWN_SLOTS) ? 1 : 0;
   P.ws_o = nullptr;
   P.ws_ml = nullptr;
   P.ws_plan = nullptr;
@@ -753,6 +764,13 @@ extern "C" int pa_trace_clear(void) {
   static unsigned long long zero[8192][16];  // >= sizeof either trace array
   cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
   return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
+}
+extern "C" int pa_trace_combine(void* host, int reset) {
+  if (reset) {
+    const unsigned long long init[3] = {~0ull, ~0ull, 0ull};
+    return (int)cudaMemcpyToSymbol(pa::tc::g_ctrace, init, sizeof(init));
+  }
+  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_ctrace, sizeof(pa::tc::g_ctrace));
 }
 extern "C" int pa_trace_tile_dump(void* host) {
   return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));

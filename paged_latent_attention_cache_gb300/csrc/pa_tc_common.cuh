@@ -209,6 +209,8 @@ __device__ __forceinline__ void trace_tile(int k, int slot) {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   if (blockIdx.x < 2 && k < 256) g_trace_tile[blockIdx.x][k][slot] = t;
 }
+// combine kernel: first start, first return from the grid wait, last end
+static __device__ unsigned long long g_ctrace[3];
 #define PA_TRACE(slot) trace(slot)
 #define PA_TRACE_TILE(k, slot) trace_tile(k, slot)
 #else
@@ -246,6 +248,7 @@ struct Params {
   int early;         // the previous kernel is the write phase: inputs other than
                      // the cache may be read before griddepcontrol.wait
   int tpc;           // prefill: consecutive tokens per work unit (rows = tpc * H <= 128)
+  int own_slots;     // with early: the write touches no row below a sequence's past
 };
 
 // QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
@@ -548,7 +551,19 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
 
 template <typename T, int VG, int G>
 __global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ Params P) {
+#ifdef PA_TC_TRACE
+  if (threadIdx.x == 0) atomicMin(&g_ctrace[0], globaltimer());
+#endif
   grid_dep_wait();  // the attention kernel's partials are complete and visible
+#ifdef PA_TC_TRACE
+  if (threadIdx.x == 0) atomicMin(&g_ctrace[1], globaltimer());
+  struct End {
+    __device__ ~End() {
+      __syncthreads();
+      if (threadIdx.x == 0) atomicMax(&g_ctrace[2], globaltimer());
+    }
+  } end_stamp;
+#endif
   const int x = blockIdx.x;
   const int h = blockIdx.y;
   const int2 plan = P.ws_plan[x];

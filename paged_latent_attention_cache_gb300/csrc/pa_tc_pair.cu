@@ -148,8 +148,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) PA_TRACE(0);
 
   // ---- prologue (same plan in both CTAs of the pair) ----
+  // With P.early (the previous kernel is the write phase) only the producer
+  // waits for the previous grid, before its first cache load.
   if (warp == 0) {
-    grid_dep_wait();
+    if (!P.early) grid_dep_wait();
     Work w;
     if (P.decode) {
       // the query region is free until the query load that follows the plan
@@ -230,7 +232,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
-  if (warp != 0) grid_dep_wait();
+  if (warp != 0 && !P.early) grid_dep_wait();
   tc_fence_before();
   cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
   tc_fence_after();
@@ -514,11 +516,21 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                       (int)(t * P.H), qb);
         tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
       }
+      // With P.early the write grid may still run: cache rows are read only
+      // after griddepcontrol.wait, except (P.own_slots) the tiles below the
+      // sequence's first new position, which the write does not touch.
+      int dirty_from = 0;
+      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, P.past[b] / N - t_begin);
+      bool waited = !P.early;
       const int nsub = N / P.box_rows;
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int stage = k % STAGES;
+        if (!waited && k >= dirty_from) {
+          grid_dep_wait();  // the write phase's cache rows are complete and visible
+          waited = true;
+        }
         if (k >= STAGES) {
           bool okw = true;
           if (lane == 0)
@@ -553,6 +565,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         issued = k + 1;
         __syncwarp();
       }
+      if (!waited) grid_dep_wait();  // the grid completes after the write grid
       if (*abort && lane == 0) {
         drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
         for (int st = 0; st < STAGES && st < issued; ++st) {

@@ -111,15 +111,18 @@ def test_deterministic_and_graph_replay_bit_equal():
     assert op.error_flags() == 0
 
 
-@pytest.mark.parametrize("name", ["glm_decode", "mixed_serving", "dsv3_decode"])
-def test_after_write_flag_bit_equal(name):
+@pytest.mark.parametrize("own_slots", [False, True], ids=["after_write", "own_slots"])
+@pytest.mark.parametrize("name", ["glm_decode", "mixed_serving", "dsv3_decode", "tiny"])
+def test_after_write_flag_bit_equal(name, own_slots):
     """The first read call after the write phase may start early
-    (PA_FLAG_AFTER_WRITE); its output is bit-equal to the same calls made
-    without the flag, eagerly and inside a CUDA graph."""
+    (PA_FLAG_AFTER_WRITE, and with PA_FLAG_OWN_SLOTS load the rows below
+    each sequence's new tokens before the write completes); its output is
+    bit-equal to the same calls made without the flags, eagerly and inside a
+    CUDA graph."""
     w = Hn.workload(name)
     d = w.to("cuda")
     from paged_latent_attention_cache_gb300.api import PagedLatentAttention
-    op = PagedLatentAttention.from_workload(w)
+    op = PagedLatentAttention.from_workload(w, own_slots=own_slots)
     base = d.key_cache.clone()
     shape = (w.num_tokens, w.num_heads * w.v_head_size)
     nd = w.num_decode_seqs
@@ -157,6 +160,45 @@ def test_after_write_flag_bit_equal(name):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, res[False][0]) and torch.equal(cache, res[False][1])
+    assert op.error_flags() == 0
+
+
+@pytest.mark.parametrize("name", ["glm_decode", "dsv3_decode"])
+def test_workspace_reuse_across_batch_sizes(name):
+    """Decode splits publish partials and count finished splits in the
+    workspace; the last split of a sequence merges. One workspace serves
+    calls over different sequence ranges in a row: a repeated full call is
+    bit-equal to the first, and a call over a sub-range (a different split
+    plan, so different rounding) agrees with it within the output tolerance.
+    A counter left non-zero would drop or duplicate partials."""
+    w = Hn.workload(name)
+    d = w.to("cuda")
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    op = PagedLatentAttention.from_workload(w)
+    cache = d.key_cache.clone()
+    op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
+    shape = (w.num_tokens, w.num_heads * w.v_head_size)
+    nd = w.num_decode_seqs
+
+    def run(lo, hi):
+        out = torch.full(shape, float("nan"), dtype=w.dtype, device="cuda")
+        op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past, d.block_table,
+                  out, lo, hi)
+        torch.cuda.synchronize()
+        return out
+
+    ref = run(0, nd)
+    assert torch.isfinite(ref.float()).all()
+    tol = Hn.TOL[w.dtype]
+    for lo, hi in [(0, nd // 2), (nd // 2, nd), (1, 2), (0, nd), (3, nd - 5), (0, nd)]:
+        got = run(lo, hi)
+        rows = slice(lo, hi)  # decode-first: sequence b's token is row b
+        if (lo, hi) == (0, nd):
+            assert torch.equal(got, ref), (lo, hi)
+        else:
+            g, r = got[rows].float(), ref[rows].float()
+            assert torch.isfinite(g).all(), (lo, hi)
+            assert (g - r).abs().max().item() <= tol, (lo, hi)
     assert op.error_flags() == 0
 
 
