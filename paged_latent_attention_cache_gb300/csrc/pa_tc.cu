@@ -654,7 +654,10 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(kThreads), smem, a.stream,
                              map, qmap, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
-  return launch_pdl(tc_combine_kernel<T, VG, G>, dim3((unsigned)nq, (unsigned)g.H), dim3(128), 0,
+  return launch_pdl(tc_combine_kernel<T, VG, G, CombineShape<VG, G>::kCPT>,
+                    dim3((unsigned)nq, (unsigned)((g.H + CombineShape<VG, G>::kHPB - 1) /
+                                                  CombineShape<VG, G>::kHPB)),
+                    dim3(256), 0,
                     a.stream, P);
 }
 

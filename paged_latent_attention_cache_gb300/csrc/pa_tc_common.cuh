@@ -549,51 +549,102 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
   return w;  // idle unit
 }
 
-template <typename T, int VG, int G>
-__global__ void __launch_bounds__(128) tc_combine_kernel(const __grid_constant__ Params P) {
+// Log-sum-exp merge of a decode sequence's key splits:
+//   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s
+// (log2-domain maxima, unnormalised partial outputs). A NaN partial maximum
+// marks a split that read an invalid block: the row becomes zeros, as does a
+// row that saw no key (sum = 0). Thread = CPT consecutive channels of one
+// head; each thread issues the loads of a round of splits together and folds
+// them with a running maximum, so the merge costs the plan load plus one
+// round trip per round of splits.
+template <typename T, int VG, int G, int CPT>
+__global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ Params P) {
 #ifdef PA_TC_TRACE
   if (threadIdx.x == 0) atomicMin(&g_ctrace[0], globaltimer());
 #endif
   grid_dep_wait();  // the attention kernel's partials are complete and visible
 #ifdef PA_TC_TRACE
   if (threadIdx.x == 0) atomicMin(&g_ctrace[1], globaltimer());
-  struct End {
-    __device__ ~End() {
-      __syncthreads();
-      if (threadIdx.x == 0) atomicMax(&g_ctrace[2], globaltimer());
-    }
-  } end_stamp;
 #endif
+  constexpr int kTPH = G * VG / CPT;         // threads per head
+  constexpr int kHPB = 256 / kTPH;           // heads per CTA
+  constexpr int kRound = CPT >= 16 ? 4 : 8;  // splits whose loads are in flight together
+  static_assert(CPT % 4 == 0 && 256 % kTPH == 0, "combine shape");
   const int x = blockIdx.x;
-  const int h = blockIdx.y;
+  const int h = blockIdx.y * kHPB + (int)threadIdx.x / kTPH;
+  const int c0 = ((int)threadIdx.x % kTPH) * CPT;  // channel in [0, G*VG)
+  const int g = c0 / VG, cc = c0 - g * VG;
   const int2 plan = P.ws_plan[x];
+  const int32_t q0 = P.cumseq[P.seq_begin + x];
   const int S = plan.y;
-  if (S <= 1) return;  // single split: the attention kernel wrote the output
-  const int32_t b = P.seq_begin + x;
-  const int32_t q0 = P.cumseq[b];
-  T* dst = reinterpret_cast<T*>(P.out) + (int64_t)q0 * P.H * P.vhs + (int64_t)h * P.vhs;
-  for (int c = threadIdx.x; c < G * VG; c += blockDim.x) {
-    const int g = c / VG, cc = c - g * VG;
-    float M = -INFINITY;
+  if (S > 1 && h < P.H) {  // (one split: the attention kernel wrote the output)
+    float M = -INFINITY, L = 0.f, o[CPT];
+#pragma unroll
+    for (int e = 0; e < CPT; ++e) o[e] = 0.f;
     bool bad = false;
-    for (int s = 0; s < S; ++s) {
-      const float m = P.ws_ml[(((int64_t)(plan.x + s) * G + g) * kRows + h) * 2];
-      bad |= isnan(m);
-      M = fmaxf(M, m);
-    }
-    float L = 0.f, o = 0.f;
-    for (int s = 0; s < S && !bad; ++s) {
-      const int64_t slot = ((int64_t)(plan.x + s) * G + g) * kRows + h;
-      const float l = P.ws_ml[slot * 2 + 1];
-      if (l > 0.f) {
-        const float w = ex2(P.ws_ml[slot * 2] - M);
-        L += w * l;
-        o += w * P.ws_o[slot * VG + cc];
+    for (int s0 = 0; s0 < S; s0 += kRound) {
+      float2 ml[kRound];
+      float4 ov[kRound][CPT / 4];
+#pragma unroll
+      for (int i = 0; i < kRound; ++i) {
+        if (s0 + i < S) {
+          const int64_t slot = ((int64_t)(plan.x + s0 + i) * G + g) * kRows + h;
+          ml[i] = reinterpret_cast<const float2*>(P.ws_ml)[slot];
+          const float4* src = reinterpret_cast<const float4*>(P.ws_o + slot * VG + cc);
+#pragma unroll
+          for (int q = 0; q < CPT / 4; ++q) ov[i][q] = src[q];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kRound; ++i) {
+        if (s0 + i < S) {
+          const float m = ml[i].x, l = ml[i].y;
+          bad |= isnan(m);
+          if (l > 0.f && !isnan(m)) {
+            if (m > M) {  // new running maximum: rescale what is folded so far
+              const float f = ex2(M - m);
+              L *= f;
+#pragma unroll
+              for (int e = 0; e < CPT; ++e) o[e] *= f;
+              M = m;
+            }
+            const float w = ex2(m - M);
+            L += w * l;
+#pragma unroll
+            for (int q = 0; q < CPT / 4; ++q) {
+              o[4 * q] += w * ov[i][q].x; o[4 * q + 1] += w * ov[i][q].y;
+              o[4 * q + 2] += w * ov[i][q].z; o[4 * q + 3] += w * ov[i][q].w;
+            }
+          }
+        }
       }
     }
-    dst[c] = Half<T>::from_f32(L > 0.f && !bad ? o / L : 0.f);
+    const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
+    uint32_t pk[CPT / 2];
+#pragma unroll
+    for (int e = 0; e < CPT / 2; ++e) pk[e] = pack2<T>(o[2 * e] * inv, o[2 * e + 1] * inv);
+    T* dst = reinterpret_cast<T*>(P.out) + ((int64_t)q0 * P.H + h) * P.vhs + g * VG + cc;
+    if (CPT == 4) {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < CPT / 8; ++q)
+        reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                      pk[4 * q + 3]);
+    }
   }
+#ifdef PA_TC_TRACE
+  __syncthreads();
+  if (threadIdx.x == 0) atomicMax(&g_ctrace[2], globaltimer());
+#endif
 }
+
+// Combine launch shape: CPT channels per thread, heads per CTA.
+template <int VG, int G>
+struct CombineShape {
+  static constexpr int kCPT = G * VG >= 512 ? 16 : 4;
+  static constexpr int kHPB = 256 / (G * VG / kCPT);
+};
 
 // ---------------------------------------------------------------------------
 // Host-side helpers

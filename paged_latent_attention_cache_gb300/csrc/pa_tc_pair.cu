@@ -724,7 +724,10 @@ cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& 
   cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(kThreads), smem, a.stream,
                              map, qmap, qmap64, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
-  return launch_pdl(tc_combine_kernel<T, 256, 2>, dim3((unsigned)nq, (unsigned)g.H), dim3(128), 0,
+  return launch_pdl(tc_combine_kernel<T, 256, 2, CombineShape<256, 2>::kCPT>,
+                    dim3((unsigned)nq, (unsigned)((g.H + CombineShape<256, 2>::kHPB - 1) /
+                                                  CombineShape<256, 2>::kHPB)),
+                    dim3(256), 0,
                     a.stream, P);
 }
 
