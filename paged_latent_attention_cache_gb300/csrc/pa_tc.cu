@@ -38,11 +38,11 @@ namespace tc {
 // ---------------------------------------------------------------------------
 // The attention kernel
 // ---------------------------------------------------------------------------
-template <typename T, int HS, int VG, int G, int N, int STAGES, int QR>
+template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ Params P) {
-  using C = Cfg<HS, VG, G, N, STAGES, QR>;
+  using C = Cfg<HS, VG, G, N, STAGES, QR, NB>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Work work;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -240,13 +240,13 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (tid == 0) PA_TRACE(3);
           if (!ok) break;
         }
-        const int sb = k & 1;
+        const int sb = NB == 2 ? (k & 1) : 0;
         const int64_t j0 = (t_begin + k) * N;
         // a tile with keys that some row must not see (uniform across the CTA)
         const bool edge = !dry && (j0 < lo_hi || j0 + N - 1 > pos);
         if (!dry) {
           ok = __all_sync(0xffffffffu,
-                          wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
+                          wait_bar(smem_u32(&bars->s_full[sb]), (k / NB) & 1, abort, P.err_flags));
           if (!ok) break;
           if (tid == 0 && k == 0) PA_TRACE(4);
           if (tid == 0) PA_TRACE_TILE(k, 0);
@@ -316,10 +316,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           fence_proxy_async();
         }
 
-        // P buffer sb is free once PV(k-2) has completed.
-        if (k >= 2) {
+        // P buffer sb is free once PV(k-NB) has completed.
+        if (k >= NB) {
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]),
-                                                ((k - 2) >> 1) & 1, abort, P.err_flags));
+                                                ((k - NB) / NB) & 1, abort, P.err_flags));
           if (!ok) break;
         }
         if (live) {
@@ -346,8 +346,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (!dry) l += lsum;
           if (__any_sync(0xffffffffu, rescale)) {
             // O may only be touched once PV(k-1) has completed.
-            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
-                                                  ((k - 1) >> 1) & 1, abort, P.err_flags));
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(k - 1) % NB]),
+                                                  ((k - 1) / NB) & 1, abort, P.err_flags));
             if (ok) {
               tc_fence_after();
 #pragma unroll 1
@@ -377,8 +377,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       named_sync(2, 160);  // the producer has finished issuing (bad-block flag final)
       ok = __all_sync(0xffffffffu, ok && !*abort);
       if (ok)
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
-                                              ((n - 1) >> 1) & 1, abort, P.err_flags));
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) % NB]),
+                                              ((n - 1) / NB) & 1, abort, P.err_flags));
       if (ok && live) {
         tc_fence_after();
         const bool bad = bars->bad != 0;
@@ -505,7 +505,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           tc_fence_after();
           PA_TRACE(10);
           // Event loop: QK^T(k) needs its key tile (full) and a free S buffer
-          // (s_free of k-2); PV(k) needs P(k) (p_full). Issue whichever is
+          // (s_free of k-NB); PV(k) needs P(k) (p_full). Issue whichever is
           // ready, QK^T first, so neither waits behind the other's inputs.
           int kq = 0, kp = 0;
           const uint64_t t0 = globaltimer();
@@ -514,8 +514,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             bool progressed = false;
             // PV first: it is short and releases the key stage to the producer.
             if (kp < kq) {
-              const int stage = kp % STAGES, sb = kp & 1;
-              if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
+              const int stage = kp % STAGES, sb = kp % NB;
+              if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp / NB) & 1)) {
                 tc_fence_after();
                 const uint32_t vb = k_base + stage * C::kStageBytes + (g * (VG / 64)) * C::kKBox;
                 // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox
@@ -535,10 +535,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               }
             }
             // QK^T(kq): needs its key tile and a free S buffer.
-            if (kq < n && kq < kp + 2) {
-              const int stage = kq % STAGES, sb = kq & 1;
+            if (kq < n && kq < kp + NB) {
+              const int stage = kq % STAGES, sb = kq % NB;
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
-                  (kq < 2 || mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - 2) >> 1) & 1))) {
+                  (kq < NB ||
+                   mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NB) / NB) & 1))) {
                 PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 const uint32_t kb = k_base + stage * C::kStageBytes;
@@ -598,29 +599,32 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
 bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.H > kRows) return false;
   if (g.hs == 192 && g.vhs == 128) {
-    // Decode with H <= 64 keeps a 64-row query tile and four key stages;
-    // otherwise (and for prefill, whose units hold 128 / H tokens) the
-    // query tile has 128 rows and there are three stages.
-    *s = (ph == Phase::kDecode && g.H <= 64) ? Shape{192, 128, 1, 128, 4, 64}
-                                             : Shape{192, 128, 1, 128, 3, 128};
+    // Decode with H <= 64 keeps a 64-row query tile and four 128-key stages.
+    // Prefill with H <= 64 (units of 128 / H tokens, each a short chain of a
+    // few key tiles) runs two CTAs per SM: 64-key tiles, two stages and a
+    // single S/P buffer (97 KB of shared memory, 256 TMEM columns each).
+    // Otherwise: a 128-row query tile, three 128-key stages, double S/P.
+    if (ph == Phase::kDecode && g.H <= 64) *s = Shape{192, 128, 1, 128, 4, 64, 2};
+    else if (ph == Phase::kPrefill && g.H <= 64) *s = Shape{192, 128, 1, 64, 2, 128, 1};
+    else *s = Shape{192, 128, 1, 128, 3, 128, 2};
     return true;
   }
   if (g.hs == 576 && g.vhs == 512) {
     // CTA-pair kernel (pa_tc_pair.cu): each CTA rotates the query channels it
     // holds, so the rotary channels must lie in one CTA's range.
     if (!(g.rd == 0 || g.ro >= 320 || g.ro + g.rd <= 256)) return false;
-    *s = {576, 256, 2, 64, 2, 128};
+    *s = {576, 256, 2, 64, 2, 128, 2};
     return true;
   }
   return false;
 }
 
-template <typename T, int HS, int VG, int G, int N, int STAGES, int QR>
+template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB>
 cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
-  using C = Cfg<HS, VG, G, N, STAGES, QR>;
+  using C = Cfg<HS, VG, G, N, STAGES, QR, NB>;
   const size_t smem = C::kSmemData + sizeof(Barriers) + 1024;
   static bool configured[64] = {false};
-  auto kern = tc_attn_kernel<T, HS, VG, G, N, STAGES, QR>;
+  auto kern = tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB>;
   if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
@@ -745,12 +749,16 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   }
   const bool bf16 = g.dtype == PA_DTYPE_BF16;
   if (s.hs == 192 && s.qr == 64) {
-    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 4, 64>(g, ph, a, P, nq)
-                : tc::launch_shape<__half, 192, 128, 1, 128, 4, 64>(g, ph, a, P, nq);
+    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 4, 64, 2>(g, ph, a, P, nq)
+                : tc::launch_shape<__half, 192, 128, 1, 128, 4, 64, 2>(g, ph, a, P, nq);
+  }
+  if (s.hs == 192 && s.nb == 1) {
+    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 64, 2, 128, 1>(g, ph, a, P, nq)
+                : tc::launch_shape<__half, 192, 128, 1, 64, 2, 128, 1>(g, ph, a, P, nq);
   }
   if (s.hs == 192) {
-    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq)
-                : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128>(g, ph, a, P, nq);
+    return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq)
+                : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq);
   }
   return bf16 ? tc::launch_pair<__nv_bfloat16>(g, ph, a, P, nq)
               : tc::launch_pair<__half>(g, ph, a, P, nq);

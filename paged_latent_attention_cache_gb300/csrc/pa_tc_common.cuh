@@ -253,7 +253,7 @@ struct Params {
 
 // QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
 // MMA then reads rows 64-127 from the next slab, rows that are never stored).
-template <int HS, int VG, int G, int N, int STAGES, int QR>
+template <int HS, int VG, int G, int N, int STAGES, int QR, int NB>
 struct Cfg {
   static constexpr int kBoxes = HS / 64;                  // 64-channel slabs
   static constexpr int kQBytes = QR * HS * 2;
@@ -261,17 +261,19 @@ struct Cfg {
   static constexpr int kKBox = N * 128;                    // bytes per K slab
   static constexpr int kStageBytes = N * HS * 2;
   static constexpr int kSmemData = kQBytes + STAGES * kStageBytes;
-  // TMEM columns: O | S0 | S1 | P0 | P1   (P is 16-bit: N/2 columns each)
+  // TMEM columns: O | S x NB | P x NB   (P is 16-bit: N/2 columns each);
+  // NB = 2 double-buffers S and P, NB = 1 leaves room for two CTAs per SM
   static constexpr int kColO = 0;
   static constexpr int kColS = VG;
-  static constexpr int kColP = VG + 2 * N;
-  static constexpr int kCols = VG + 2 * N + N;
+  static constexpr int kColP = VG + NB * N;
+  static constexpr int kCols = VG + NB * N + NB * N / 2;
   static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
                                    : kCols <= 256 ? 256 : 512;
   static_assert(kCols <= 512, "TMEM budget");
   static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 128, "shape");
   static_assert(STAGES <= 8, "stages");
   static_assert(QR == 64 || QR == 128, "query rows");
+  static_assert(NB == 1 || NB == 2, "S/P buffers");
 };
 
 struct Barriers {
@@ -668,7 +670,7 @@ inline EncodeTiledFn encode_fn() {
 }
 
 struct Shape {
-  int hs, vg, groups, n, stages, qr;
+  int hs, vg, groups, n, stages, qr, nb;
 };
 
 // Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
