@@ -99,12 +99,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       int64_t pos;
       w.status = 1;
       w.splits = 1;
-      if (locate_token(unit, P.cumseq, P.past, P.num_seqs,
+      // CTA `unit` takes token T - 1 - unit: the tokens with the most keys
+      // (the last of each sequence) start first, short ones fill in behind
+      const int64_t tok = P.num_tokens - 1 - unit;
+      if (locate_token(tok, P.cumseq, P.past, P.num_seqs,
                        (lane == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos) &&
           b >= P.seq_begin && b < P.seq_end) {
         w.status = 0;
         w.b = b;
-        w.t = unit;
+        w.t = tok;
         w.pos = pos;
         w.ntok = 1;
         const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
@@ -760,6 +763,9 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
     return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq)
                 : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq);
   }
+  if (ph == Phase::kPrefill)
+    return bf16 ? tc::launch_pair_xw<__nv_bfloat16>(g, ph, a, P, nq)
+                : tc::launch_pair_xw<__half>(g, ph, a, P, nq);
   return bf16 ? tc::launch_pair<__nv_bfloat16>(g, ph, a, P, nq)
               : tc::launch_pair<__half>(g, ph, a, P, nq);
 }

@@ -509,7 +509,9 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
 // Prefill work unit `unit` with up to `tpc` consecutive tokens of one
 // sequence per unit (the query tile then holds tpc tokens' heads, which share
 // every key tile). Sequences of [seq_begin, seq_end) get ceil(q_b / tpc)
-// units each, numbered in sequence order; run by one full warp.
+// units each, numbered in sequence order; CTA `unit` takes number
+// total - 1 - unit, so the units with the most keys (the last tokens) start
+// first and short ones fill in behind them. Run by one full warp.
 __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, int tpc) {
   const int lane = threadIdx.x & 31;
   const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin;
@@ -517,6 +519,15 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
   w.status = 1;
   w.splits = 1;
   w.ntok = 0;
+  int total = 0;
+  for (int i = lane; i < nseq; i += 32) {
+    const int q = P.cumseq[seq_begin + i + 1] - P.cumseq[seq_begin + i];
+    total += q > 0 ? ceil_div32(q, tpc) : 0;
+  }
+#pragma unroll 1
+  for (int o = 16; o > 0; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+  if (unit >= total) return w;  // idle unit
+  unit = total - 1 - unit;
   int run = 0;
   for (int base = 0; base < nseq; base += 32) {
     const int i = base + lane;
@@ -705,6 +716,8 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 // CTA-pair kernel for the 576/512 geometry (pa_tc_pair.cu).
 template <typename T>
 cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq);
+template <typename T>
+cudaError_t launch_pair_xw(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq);
 
 }  // namespace tc
 }  // namespace pa

@@ -1,0 +1,722 @@
+// Prefill read phase for the 576/512 latent geometry on a CTA pair, with
+// dedicated exchange warps.
+//
+// The work split is the decode pair kernel's (pa_tc_pair.cu): a cluster of
+// two CTAs handles one token; CTA c holds the query channels [288c,
+// 288c+288) and V channels [256c, 256c+256), computes the partial scores
+// S_c over its channels and owns its half of the output. Here the exchange
+// of partial scores runs in four extra warps (6-9, one per TMEM lane
+// quadrant) instead of in the softmax warps: per tile they read S_c from
+// TMEM, send it to the peer (st.async, completing on the peer's mbarrier),
+// add the peer's rows (S_0 + S_1 in that order in both CTAs) and write the
+// sum back for the softmax warps, so the exchange of tile k+1 overlaps the
+// softmax of tile k. Three S buffers (O 256 + 3 x 64 + P 2 x 32 = 512 TMEM
+// columns). In prefill the key tiles come from L2, the stage ring turns over
+// quickly, and the overlap pays (about 5 % over the decode kernel on the
+// DeepSeek prefill shape); with key tiles from HBM (decode) it does not.
+//
+// Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
+// TMA producer, warp 5 TMEM allocation + the MMA-issuing thread, warps 6-9
+// score exchange. Key tiles of 64 keys, 3 stages; every wait is bounded.
+#include "pa_tc_cluster.cuh"
+
+namespace pa {
+namespace tc {
+
+template <int N, int STAGES>
+struct XwCfg {
+  static constexpr int kThreads = 320;              // warps 0-3, 4, 5, 6-9 (see above)
+  static constexpr int kSlabs = 5;                  // 64-channel slabs per CTA (of 9)
+  static constexpr int kSteps = 18;                 // 16-channel QK^T K-steps per CTA
+  static constexpr int kQBox = kRows * 128;         // bytes per full query slab (SW128)
+  static constexpr int kQHalf = kRows * 64;         // the 32 channels of slab 4 (SW64)
+  static constexpr int kQBytes = 4 * kQBox + kQHalf;
+  static constexpr int kKBox = N * 128;             // bytes per key slab of a stage
+  static constexpr int kStageBytes = kSlabs * kKBox;
+  static constexpr int kXBytes = kRows * N * 4;     // incoming partial-S rows
+  static constexpr int kSmemData = kQBytes + STAGES * kStageBytes + kXBytes;
+  static constexpr int kVG = 256;                   // output channels per CTA
+  static constexpr int kSBufs = 3;                  // S buffers in TMEM
+  static constexpr int kColO = 0;
+  static constexpr int kColS = kVG;
+  static constexpr int kColP = kVG + kSBufs * N;
+  static constexpr int kTmemCols = 512;
+  static_assert(kVG + kSBufs * N + N <= 512, "TMEM budget");
+  static_assert(N % 32 == 0 && N <= 128, "key tile");
+};
+
+struct XwBarriers {
+  uint64_t full[4], empty[4];
+  uint64_t s_part[3];  // QK^T(k) has written this CTA's partial S (tcgen05.commit)
+  uint64_t s_sum[3];   // the exchange warps have written S_0 + S_1 back (128 arrivals)
+  uint64_t s_free[3];  // the softmax warps are done with the S buffer (128 arrivals)
+  uint64_t p_full[2], pv_done[2];
+  uint64_t q_tma, q_full;
+  uint64_t x_in;    // x_s holds the peer's partial rows (local expect_tx + the
+                    // peer's st.async complete_tx bytes)
+  uint64_t x_out;   // the peer has read the rows this CTA sent into its x_s
+  uint64_t drain;
+  uint32_t tmem_base;
+  int bad;
+  int abort;
+};
+
+template <typename T, int N, int STAGES>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(XwCfg<N, STAGES>::kThreads, 1)
+tc_pair_xw_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
+               const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
+  using C = XwCfg<N, STAGES>;
+  constexpr int G = 2, VG = C::kVG, NS = C::kSBufs;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Work work;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~(uintptr_t)1023);
+  uint8_t* q_s = smem;
+  uint8_t* k_s = smem + C::kQBytes;
+  float* x_s = reinterpret_cast<float*>(smem + C::kQBytes + STAGES * C::kStageBytes);
+  XwBarriers* bars = reinterpret_cast<XwBarriers*>(smem + C::kSmemData);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t g = cluster_rank();         // channel half == value group
+  const uint32_t peer = g ^ 1u;
+  const int unit = blockIdx.x / G;
+  const int vhs = P.vhs;
+  if (tid == 0) PA_TRACE(0);
+
+  // ---- prologue (same plan in both CTAs of the pair) ----
+  // As in the single-CTA kernel: inputs are read only after griddepcontrol.wait,
+  // except with P.early (the previous kernel is the write phase), where the
+  // producer waits before its first cache load.
+  if (warp == 0) {
+    if (!P.early) grid_dep_wait();
+    Work w;
+    if (P.decode) {
+      // the query region is free until the query load after the plan
+      w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), C::kQBytes / 4);
+      if (w.status == 0) {
+        const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
+        if (lane == 0 && w.split == 0 && g == 0)
+          P.ws_plan[w.b - P.seq_begin] = make_int2(w.first, w.splits);
+        if (q1 - q0 != 1) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_DECODE_QLEN);
+          w.status = 2;
+        } else if (q0 < 0 || q0 >= P.num_tokens) {
+          if (lane == 0 && g == 0) raise_flag(P.err_flags, PA_DEVERR_CUMSEQ);
+          w.status = 2;
+        } else {
+          w.t = q0;
+          w.pos = P.past[w.b];
+        }
+      }
+    } else {
+      int32_t b;
+      int64_t pos;
+      w.status = 1;
+      w.splits = 1;
+      // CTA `unit` takes token T - 1 - unit: the tokens with the most keys
+      // (the last of each sequence) start first, short ones fill in behind
+      const int64_t tok = P.num_tokens - 1 - unit;
+      if (locate_token(tok, P.cumseq, P.past, P.num_seqs,
+                       (lane == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos) &&
+          b >= P.seq_begin && b < P.seq_end) {
+        w.status = 0;
+        w.b = b;
+        w.t = tok;
+        w.pos = pos;
+        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        w.t_begin = lo_key / N;
+        w.t_end = pos / N + 1;
+      }
+    }
+    if (w.status == 0) {
+      const bool bad_ctx = P.past[w.b] < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
+      const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
+      if (bad_ctx || bad_pos) {
+        if (lane == 0 && g == 0)
+          raise_flag(P.err_flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
+        T* out_row = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs;
+        for (int i = lane; i < P.H * VG; i += 32) {
+          const int h = i / VG, c = i % VG;
+          out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
+        }
+        w.status = 2;
+      }
+    }
+    if (lane == 0) work = w;
+  } else if (warp == 1 && lane == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&bars->full[s]), 1);
+      mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bars->s_part[i]), 1);
+      mbar_init(smem_u32(&bars->s_sum[i]), kRows);
+      mbar_init(smem_u32(&bars->s_free[i]), kRows);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->p_full[i]), kRows);
+      mbar_init(smem_u32(&bars->pv_done[i]), 1);
+    }
+    mbar_init(smem_u32(&bars->q_tma), 1);
+    mbar_init(smem_u32(&bars->q_full), kRows);
+    mbar_init(smem_u32(&bars->x_in), 1);
+    mbar_init(smem_u32(&bars->x_out), 1);
+    mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);  // armed for tile 0
+    mbar_init(smem_u32(&bars->drain), 1);
+    bars->bad = 0;
+    bars->abort = 0;
+    fence_barrier_init();
+  } else if (warp == 4 && lane == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&qmap64);
+  } else if (warp == 5) {
+    tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp != 0 && !P.early) grid_dep_wait();
+  tc_fence_before();
+  cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  volatile int* abort = &bars->abort;
+  const Work W = work;
+  if (tid == 0) PA_TRACE(1);
+
+  if (W.status == 0) {
+    const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
+    const int32_t b = W.b;
+    const int splits = W.splits;
+    const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    const int n = (int)max((int64_t)0, W.t_end - t_begin);
+    const int64_t part = (int64_t)unit * G + g;
+    T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
+    const int slab0 = 4 * (int)g;  // global slab of local key slab 0
+    // Query layout in shared memory: CTA 0 holds full slabs 0-3 (SW128) then
+    // channels 256-287 as a 64-byte-swizzled half slab; CTA 1 holds channels
+    // 288-319 as the half slab, then full slabs 5-8.
+    const int q_full0 = g ? 5 : 0;                         // global slab of full slab 0
+    const int q_full_off = g ? C::kQHalf : 0;              // byte offset of full slab 0
+    const int q_half_off = g ? 0 : 4 * C::kQBox;           // byte offset of the half slab
+
+    if (warp < 4) {
+      // =================== softmax / epilogue ===================
+      const int row = tid;
+      const bool live = warp * 32 < P.H;
+      const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      // Pass k = -1 runs the tile code once with every wait, arrive, shared
+      // memory write and state update switched off, on whatever TMEM holds:
+      // it brings the loop's instructions into the instruction cache while
+      // the query and the first key tile are still in flight. (The opaque
+      // start keeps the compiler from peeling it into a copy of its own.)
+      int k_first = -1;
+      asm volatile("" : "+r"(k_first));
+      for (int k = k_first; k < n && ok; ++k) {
+        const bool dry = k < 0;
+        if (k == 0) {  // every work item has n >= 1 tiles
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+          // RoPE in place on this CTA's slabs (the pair kernel only runs when
+          // the rotary channels and their partners lie inside one CTA's slabs).
+          if (ok && P.rd > 0 && row < P.H) {
+            const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;  // full query slabs only
+            if (P.ro >= c_lo && P.ro + P.rd <= c_hi) {
+              const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
+              const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+              auto at = [&](int d0) -> uint4* {
+                const int slab = (d0 >> 6) - q_full0, ch = (d0 >> 3) & 7;
+                return reinterpret_cast<uint4*>(q_s + q_full_off + slab * C::kQBox + row * 128 +
+                                                ((ch ^ (row & 7)) << 4));
+              };
+              if (!P.interleaved) {
+                const int half = P.rd >> 1;
+                for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
+                  float a[8], bb[8], na[8], nb[8];
+                  unpack8<T>(*at(d0), a);
+                  unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+                  rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
+                  rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
+                  *at(d0) = pack8<T>(na);
+                  *at(d0 + half) = pack8<T>(nb);
+                }
+              } else {
+                for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
+                  float a[8], dummy[8];
+                  unpack8<T>(*at(d0), a);
+                  rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
+                  *at(d0) = pack8<T>(a);
+                }
+              }
+            }
+          }
+          fence_proxy_async();
+          mbar_arrive(smem_u32(&bars->q_full));
+          if (tid == 0) PA_TRACE(3);
+          if (!ok) break;
+        }
+        const int sb = dry ? 0 : k % NS;   // S buffer
+        const int pb = dry ? 1 : k & 1;    // P buffer
+        const int64_t j0 = (t_begin + k) * N;
+        const bool edge = !dry && (j0 < lo || j0 + N - 1 > pos);
+        if (!dry) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_sum[sb]), (k / NS) & 1, abort,
+                                                P.err_flags));
+          if (!ok) break;
+          if (tid == 0) PA_TRACE_TILE(k, 0);
+          if (tid == 0 && k == 0) PA_TRACE(4);
+        }
+        // The tile is handled in 32-column chunks read from TMEM twice (row
+        // maximum, then exponentials), which keeps the loop body short.
+        float factor = 1.f;
+        bool rescale = false;
+        const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        const uint32_t s_addr = lane_addr + C::kColS + sb * N;
+        if (live) {
+          tc_fence_after();
+          float mt = -INFINITY;
+          const bool rewrite = P.softcap_on || edge;
+#pragma unroll 1
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[32];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            if (rewrite) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                float v = __uint_as_float(r[e]);
+                if (P.softcap_on) v = P.cap_out * tanhf(v * P.cap_in);
+                const int64_t j = j0 + c + e;
+                if (edge && (j < lo || j > pos)) v = -INFINITY;
+                r[e] = __float_as_uint(v);
+              }
+              tmem_st32(s_addr + c, r);
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
+          }
+          if (rewrite) tmem_wait_st();
+          mt *= sl;
+          if (dry) {
+          } else if (k == 0) {
+            m_used = mt;
+          } else if (mt > m_used + kRescaleLog2) {
+            factor = ex2(m_used - mt);
+            m_used = mt;
+            l *= factor;
+            rescale = true;
+          }
+        }
+        if (edge) {  // zero value rows of masked keys (stale cache slots)
+          uint8_t* kst = k_s + (k % STAGES) * C::kStageBytes;
+          for (int i = tid; i < N * 4 * 8; i += 128) {
+            const int rr = i / 32, rem = i - rr * 32;
+            const int slab = rem / 8, ch = rem & 7;
+            const int64_t j = j0 + rr;
+            if (j < lo || j > pos)
+              *reinterpret_cast<uint4*>(kst + slab * C::kKBox + rr * 128 + ch * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async();
+        }
+        if (k >= 2) {  // P buffer pb is free once PV(k-2) has completed
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[pb]),
+                                                ((k - 2) >> 1) & 1, abort, P.err_flags));
+          if (!ok) break;
+        }
+        if (live) {
+          tc_fence_after();
+          float lsum = 0.f;
+#pragma unroll 1
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[32], pk[16];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -m_used));
+              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -m_used));
+              lsum += p0 + p1;
+              pk[e] = pack2<T>(p0, p1);
+            }
+            tmem_st16(lane_addr + C::kColP + pb * (N / 2) + c / 2, pk);
+          }
+          if (!dry) l += lsum;
+          if (__any_sync(0xffffffffu, rescale)) {
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[pb ^ 1]),
+                                                  ((k - 1) >> 1) & 1, abort, P.err_flags));
+            if (ok) {
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < VG; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + C::kColO + c, r);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  r[e] = __float_as_uint(__uint_as_float(r[e]) * factor);
+                tmem_st16(lane_addr + C::kColO + c, r);
+              }
+            }
+          }
+          tmem_wait_st();
+        }
+        if (!ok) break;
+        tc_fence_before();
+        if (dry) continue;
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+        mbar_arrive(smem_u32(&bars->p_full[pb]));
+        if (tid == 0) PA_TRACE_TILE(k, 1);
+      }
+
+      // ---- epilogue ----
+      if (tid == 0) PA_TRACE(5);
+      grid_dep_launch();
+      named_sync(2, 160);
+      ok = __all_sync(0xffffffffu, ok && !*abort);
+      if (ok)
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
+                                              ((n - 1) >> 1) & 1, abort, P.err_flags));
+      if (ok && live) {
+        tc_fence_after();
+        const bool bad = bars->bad != 0;
+        if (splits == 1) {
+          const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
+#pragma unroll 1
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              uint4 o[2];
+              uint32_t* ow = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+              for (int e = 0; e < 8; ++e)
+                ow[e] = pack2<T>(__uint_as_float(r[2 * e]) * inv,
+                                 __uint_as_float(r[2 * e + 1]) * inv);
+              uint4* dst = reinterpret_cast<uint4*>(out_row + (int64_t)row * vhs + g * VG + c);
+              dst[0] = o[0];
+              dst[1] = o[1];
+            }
+          }
+        } else {
+          float* wo = P.ws_o + (part * kRows + row) * VG;
+#pragma unroll 1
+          for (int c = 0; c < VG; c += 16) {
+            uint32_t r[16];
+            tmem_ld16(lane_addr + C::kColO + c, r);
+            if (row < P.H) {
+              float4* dst = reinterpret_cast<float4*>(wo + c);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                     __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+            }
+          }
+          if (row < P.H) {
+            P.ws_ml[(part * kRows + row) * 2 + 0] = bad ? __int_as_float(0x7fc00000) : m_used;
+            P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
+          }
+        }
+      }
+    } else if (warp >= 6) {
+      // =================== partial-score exchange ===================
+      // Warp w handles TMEM lanes 32*(w%4)..+31 (the quadrant its SM
+      // sub-partition may access). Per tile: read this CTA's partial S rows,
+      // send them to the peer's x_s with st.async (the bytes complete on the
+      // peer's x_in), wait for the peer's rows, form S_0 + S_1 (that order in
+      // both CTAs) and write the sum back into the S buffer for the softmax
+      // warps. x_s is chunk-major: 16-byte chunk q of row r at [q][r], so a
+      // warp's store of one chunk for its 32 rows is 512 contiguous bytes.
+      constexpr int kChunks = N / 4;
+      const int xq = warp & 3, xrow = xq * 32 + lane, xt = tid - 192;  // xt: 0..127
+      const uint32_t lane_addr = tmem + ((uint32_t)(xq * 32) << 16);
+      float* x_row = x_s + xrow * 4;
+      const uint32_t x_peer = map_peer(smem_u32(x_row), peer);
+      const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in), peer);
+      const uint32_t x_out_peer = map_peer(smem_u32(&bars->x_out), peer);
+      bool ok = true;
+      for (int k = 0; k < n && ok; ++k) {
+        const int sb = k % NS;
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
+                                              P.err_flags));
+        if (!ok) break;
+        if (xt == 0) PA_TRACE_TILE(k, 8);
+        tc_fence_after();
+        uint32_t r[N / 32][32];
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c)
+          tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
+        if (k >= 1) {  // the peer has read tile k-1 from its x_s
+          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out), (k - 1) & 1,
+                                                        abort, P.err_flags));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q)
+          st_async_b32x4(x_peer + q * kRows * 16, r[q / 8][(4 * q) & 31], r[q / 8][(4 * q + 1) & 31],
+                      r[q / 8][(4 * q + 2) & 31], r[q / 8][(4 * q + 3) & 31], x_in_peer);
+        if (xt == 0) PA_TRACE_TILE(k, 9);
+        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in), k & 1, abort,
+                                                      P.err_flags));
+        if (!ok) break;
+        if (xt == 0) PA_TRACE_TILE(k, 12);
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(x_row + q * kRows * 4);
+          uint32_t* d = &r[q / 8][(4 * q) & 31];
+          const float pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float mine = __uint_as_float(d[e]);
+            d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+          }
+        }
+        named_sync(3, 128);  // every row of x_s has been read
+        if (xt == 0) {
+          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);
+          arrive_peer_relaxed(x_out_peer);
+        }
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_sum[sb]));
+        if (xt == 0) PA_TRACE_TILE(k, 11);
+      }
+    } else if (warp == 4) {
+      // =================== TMA producer ===================
+      if (lane == 0) {  // this CTA's five query slabs (QR = 128 rows: the token's heads)
+        const uint32_t qb = smem_u32(&bars->q_tma);
+        mbar_expect_tx(qb, C::kQBytes);
+        for (int j = 0; j < 4; ++j)
+          tma_load_2d(smem_u32(q_s) + q_full_off + j * C::kQBox, &qmap, (q_full0 + j) * 64,
+                      (int)(t * P.H), qb);
+        tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
+      }
+      if (P.early) grid_dep_wait();  // the write phase's cache rows are complete and visible
+      const int nsub = N / P.box_rows;
+      const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
+      // First cache row of this lane's box (one cache block) of tile kk, or
+      // -1 when the box holds no visible key or its block id is invalid.
+      auto box_row = [&](int kk, bool report) -> int {
+        const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
+        if (key0 > pos || key0 + P.box_rows - 1 < lo) return -1;
+        const int32_t phys = bt[key0 / P.bs];
+        if (phys < 0 || phys >= P.num_blocks) {
+          if (report) {
+            bars->bad = 1;
+            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+          }
+          return -1;
+        }
+        return (int)((int64_t)phys * P.bs + key0 % P.bs);
+      };
+      int issued = 0;
+      for (int k = 0; k < n; ++k) {
+        const int stage = k % STAGES;
+        if (k >= STAGES) {
+          bool okw = true;
+          if (lane == 0)
+            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
+                           P.err_flags);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
+        }
+        int y = (int)P.num_slots;  // out of range: TMA fills zeros
+        if (lane < nsub) {
+          const int yy = box_row(k, true);
+          if (yy >= 0) y = yy;
+        }
+        if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
+        if (lane == 0) PA_TRACE_TILE(k, 5);
+        __syncwarp();
+        if (lane < nsub) {
+          const uint32_t full = smem_u32(&bars->full[stage]);
+          const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
+#pragma unroll 1
+          for (int j = 0; j < C::kSlabs; ++j)
+            tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+        }
+        issued = k + 1;
+        __syncwarp();
+      }
+      if (*abort && lane == 0) {
+        drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
+        for (int st = 0; st < STAGES && st < issued; ++st) {
+          const int kl = issued - 1 - ((issued - 1 - st) % STAGES);
+          drain_wait(smem_u32(&bars->full[st]), (kl / STAGES) & 1, P.err_flags);
+        }
+      }
+      __syncwarp();
+      named_arrive(2, 160);
+    } else if (warp == 5) {
+      // =================== MMA issuer ===================
+      if (lane == 0) {
+        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
+        constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
+        const uint32_t q_base = smem_u32(q_s);
+        const uint32_t k_base = smem_u32(k_s);
+        bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
+        if (ok) {
+          tc_fence_after();
+          int kq = 0, kp = 0;
+          const uint64_t t0 = globaltimer();
+          uint32_t spins = 0;
+          while (kp < n) {
+            bool progressed = false;
+            if (kp < kq) {
+              const int stage = kp % STAGES, pb = kp & 1;
+              if (mbar_test_wait(smem_u32(&bars->p_full[pb]), (kp >> 1) & 1)) {
+                tc_fence_after();
+                const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
+#pragma unroll
+                for (int kk = 0; kk < N / 16; ++kk) {
+                  const uint64_t bdesc = sdesc(vb + kk * 16 * 128, C::kKBox, 1024);
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (N / 2) + kk * 8, bdesc, kIdPV,
+                         (kp > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->pv_done[pb]));
+                tc_commit(smem_u32(&bars->empty[stage]));
+                PA_TRACE_TILE(kp, 3);
+                ++kp;
+                progressed = true;
+              }
+            }
+            // QK^T(kq): needs its key tile and a free S buffer (s_free of kq-NS)
+            if (kq < n && kq < kp + NS) {
+              const int stage = kq % STAGES, sb = kq % NS;
+              if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
+                  (kq < NS ||
+                   mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NS) / NS) & 1))) {
+                PA_TRACE_TILE(kq, 4);
+                tc_fence_after();
+                const uint32_t kb = k_base + stage * C::kStageBytes;
+#pragma unroll
+                for (int i = 0; i < C::kSteps; ++i) {
+                  // CTA g covers K steps [18g, 18g+18) = channels [288g, 288g+288):
+                  // the key operand is local slab e>>2, step e&3 (e = i + 2g); the
+                  // query operand is a full slab, or the 32-channel half slab.
+                  const int e = i + 2 * (int)g;
+                  const int kslab = e >> 2, w = (e & 3) * 32;
+                  const bool half = g ? (i < 2) : (i >= 16);
+                  uint64_t a;
+                  if (half) {
+                    a = sdesc64(q_base + q_half_off + (g ? i : i - 16) * 32);
+                  } else {
+                    const int j = g ? (i - 2) >> 2 : i >> 2;
+                    const int wq = (g ? (i - 2) & 3 : i & 3) * 32;
+                    a = sdesc(q_base + q_full_off + j * C::kQBox + wq, 16, 1024);
+                  }
+                  const uint64_t bdesc = sdesc(kb + kslab * C::kKBox + w, 16, 1024);
+                  mma_ss(tmem + C::kColS + sb * N, a, bdesc, kIdQK, i > 0 ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&bars->s_part[sb]));
+                PA_TRACE_TILE(kq, 2);
+                ++kq;
+                progressed = true;
+              }
+            }
+            if (progressed) {
+              spins = 0;
+              continue;
+            }
+            if ((++spins & 15u) == 0) {
+              if (*abort) { ok = false; break; }
+              if (globaltimer() - t0 > kWaitLimitNs * 4) {
+                *abort = 1;
+                raise_flag(P.err_flags, PA_DEVERR_TIMEOUT);
+                ok = false;
+                break;
+              }
+            }
+          }
+        }
+        tc_commit(smem_u32(&bars->drain));
+        drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
+      }
+      __syncwarp();
+    }
+  }
+
+  if (W.status != 0) grid_dep_launch();
+  if (tid == 0) PA_TRACE(6);
+  tc_fence_before();
+  cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if (tid == 0) PA_TRACE(7);
+}
+
+template <typename T>
+cudaError_t launch_pair_xw(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
+  constexpr int N = 64, STAGES = 3;
+  using C = XwCfg<N, STAGES>;
+  const size_t smem = C::kSmemData + sizeof(XwBarriers) + 1024;
+  static bool configured[64] = {false};
+  auto kern = tc_pair_xw_kernel<T, N, STAGES>;
+  if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    configured[g.device] = true;
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
+                                     ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUtensorMap map, qmap;
+  const cuuint64_t dims[2] = {576, (cuuint64_t)g.num_blocks * g.bs};
+  const cuuint64_t strides[1] = {576 * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const cuuint64_t qdims[2] = {576, (cuuint64_t)a.num_tokens * g.H};
+  const cuuint32_t qbox[2] = {64, (cuuint32_t)kRows};
+  r = enc(&qmap, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // 32-channel boxes (64-byte rows, 64-byte swizzle) for the half query slab
+  CUtensorMap qmap64;
+  const cuuint32_t qbox64[2] = {32, (cuuint32_t)kRows};
+  r = enc(&qmap64, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox64, estr,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
+  return launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem, a.stream, map,
+                    qmap, qmap64, P);
+}
+
+template cudaError_t launch_pair_xw<__nv_bfloat16>(const Geometry&, Phase, const ReadArgs&, Params&,
+                                                int64_t);
+template cudaError_t launch_pair_xw<__half>(const Geometry&, Phase, const ReadArgs&, Params&,
+                                         int64_t);
+
+}  // namespace tc
+}  // namespace pa
+
+
+#ifdef PA_TC_TRACE
+extern "C" int pa_trace_xw_dump(void* host, void* tile_host) {
+  cudaMemcpyFromSymbol(tile_host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
+  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, sizeof(pa::tc::g_trace));
+}
+extern "C" int pa_trace_xw_clear(void) {
+  static unsigned long long zero[8192][16];
+  cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
+  return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
+}
+#endif
