@@ -589,7 +589,9 @@ tc_pair_xw_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constan
               }
             }
             // QK^T(kq): needs its key tile and a free S buffer (s_free of kq-NS)
-            if (kq < n && kq < kp + NS) {
+            // (at most two tiles ahead of PV: a PV queued behind more QK^T
+            // in the in-order tensor pipe would hold its key stage longer)
+            if (kq < n && kq < kp + 2) {
               const int stage = kq % STAGES, sb = kq % NS;
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
                   (kq < NS ||
