@@ -763,9 +763,6 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
     return bf16 ? tc::launch_shape<__nv_bfloat16, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq)
                 : tc::launch_shape<__half, 192, 128, 1, 128, 3, 128, 2>(g, ph, a, P, nq);
   }
-  if (ph == Phase::kPrefill)
-    return bf16 ? tc::launch_pair_xw<__nv_bfloat16>(g, ph, a, P, nq)
-                : tc::launch_pair_xw<__half>(g, ph, a, P, nq);
   return bf16 ? tc::launch_pair<__nv_bfloat16>(g, ph, a, P, nq)
               : tc::launch_pair<__half>(g, ph, a, P, nq);
 }

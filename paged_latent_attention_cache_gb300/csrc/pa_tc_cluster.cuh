@@ -1,4 +1,4 @@
-// Helpers shared by the CTA-pair kernels (pa_tc_pair.cu, pa_tc_pair_xw.cu):
+// Helpers of the CTA-pair kernel (pa_tc_pair.cu):
 // cluster rank and barrier, distributed-shared-memory addressing, remote
 // stores that complete on the peer's mbarrier, and bounded cluster-scope waits.
 #pragma once

@@ -716,8 +716,6 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
 // CTA-pair kernel for the 576/512 geometry (pa_tc_pair.cu).
 template <typename T>
 cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq);
-template <typename T>
-cudaError_t launch_pair_xw(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq);
 
 }  // namespace tc
 }  // namespace pa

@@ -6,20 +6,24 @@
 // and a 128 x 576 query tile most of its shared memory, so one token is
 // handled by a cluster of two CTAs on two SMs that split the latent channels:
 //
-//   CTA c in {0,1} holds query slabs (64 channels each) 4c..4c+4 and loads
-//   the same five slabs of every key tile. Its QK^T covers 18 of the 36
-//   16-channel K steps (channels [288c, 288c+288)), so S = S_0 + S_1 with
-//   S_c its partial; each softmax thread sends its row of S_c to the peer
-//   through distributed shared memory and adds the peer's row (both CTAs
-//   form S_0 + S_1 in the same order, so they hold bit-identical S, P, m, l).
-//   CTA c then accumulates O[:, 256c : 256c+256] = P @ V with V = its slabs
-//   0-3 (global slabs 4c..4c+3), i.e. each output half on one SM and no
+//   CTA c in {0,1} holds the query channels [288c, 288c+288) (four 64-channel
+//   slabs and a 32-channel half slab) and loads five 64-channel slabs of
+//   every key tile. Its QK^T covers 18 of the 36 16-channel K steps, so
+//   S = S_0 + S_1 with S_c its partial. CTA c accumulates O[:, 256c : 256c+256]
+//   = P @ V with V = four of its key slabs: each output half on one SM and no
 //   product computed twice.
 //
-// Roles per CTA as in pa_tc.cu: warps 0-3 softmax/epilogue (thread = head
-// row = TMEM lane), warp 4 TMA producer, warp 5 TMEM allocation + the
-// MMA-issuing thread. Key tiles of 64 keys, 2 stages; S and P
-// double-buffered in TMEM; every wait is bounded.
+// The partial scores are exchanged by four dedicated warps (6-9, one per
+// TMEM lane quadrant): per tile they read S_c from TMEM, send it to the peer
+// through distributed shared memory (st.async, completing on the peer's
+// mbarrier), add the peer's rows (S_0 + S_1 in that order in both CTAs, so
+// both hold bit-identical S, P, m and l) and write the sum back for the
+// softmax warps; the exchange of tile k+1 overlaps the softmax of tile k.
+// Three S buffers: O 256 + 3 x 64 + P 2 x 32 = 512 TMEM columns.
+//
+// Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
+// TMA producer, warp 5 TMEM allocation + the MMA-issuing thread, warps 6-9
+// score exchange. Key tiles of 64 keys, 3 stages; every wait is bounded.
 #include "pa_tc_cluster.cuh"
 
 namespace pa {
@@ -27,6 +31,7 @@ namespace tc {
 
 template <int N, int STAGES>
 struct PairCfg {
+  static constexpr int kThreads = 320;              // warps 0-3, 4, 5, 6-9 (see above)
   static constexpr int kSlabs = 5;                  // 64-channel slabs per CTA (of 9)
   static constexpr int kSteps = 18;                 // 16-channel QK^T K-steps per CTA
   static constexpr int kQBox = kRows * 128;         // bytes per full query slab (SW128)
@@ -37,17 +42,21 @@ struct PairCfg {
   static constexpr int kXBytes = kRows * N * 4;     // incoming partial-S rows
   static constexpr int kSmemData = kQBytes + STAGES * kStageBytes + kXBytes;
   static constexpr int kVG = 256;                   // output channels per CTA
+  static constexpr int kSBufs = 3;                  // S buffers in TMEM
   static constexpr int kColO = 0;
   static constexpr int kColS = kVG;
-  static constexpr int kColP = kVG + 2 * N;
+  static constexpr int kColP = kVG + kSBufs * N;
   static constexpr int kTmemCols = 512;
-  static_assert(kVG + 3 * N <= 512, "TMEM budget");
+  static_assert(kVG + kSBufs * N + N <= 512, "TMEM budget");
   static_assert(N % 32 == 0 && N <= 128, "key tile");
 };
 
 struct PairBarriers {
   uint64_t full[4], empty[4];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
+  uint64_t s_part[3];  // QK^T(k) has written this CTA's partial S (tcgen05.commit)
+  uint64_t s_sum[3];   // the exchange warps have written S_0 + S_1 back (128 arrivals)
+  uint64_t s_free[3];  // the softmax warps are done with the S buffer (128 arrivals)
+  uint64_t p_full[2], pv_done[2];
   uint64_t q_tma, q_full;
   uint64_t x_in;    // x_s holds the peer's partial rows (local expect_tx + the
                     // peer's st.async complete_tx bytes)
@@ -59,11 +68,11 @@ struct PairBarriers {
 };
 
 template <typename T, int N, int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<N, STAGES>::kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
   using C = PairCfg<N, STAGES>;
-  constexpr int G = 2, VG = C::kVG;
+  constexpr int G = 2, VG = C::kVG, NS = C::kSBufs;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Work work;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -81,13 +90,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) PA_TRACE(0);
 
   // ---- prologue (same plan in both CTAs of the pair) ----
-  // With P.early (the previous kernel is the write phase) only the producer
-  // waits for the previous grid, before its first cache load.
+  // As in the single-CTA kernel: inputs are read only after griddepcontrol.wait,
+  // except with P.early (the previous kernel is the write phase), where the
+  // producer waits before its first cache load.
   if (warp == 0) {
     if (!P.early) grid_dep_wait();
     Work w;
     if (P.decode) {
-      // the query region is free until the query load that follows the plan
+      // the query region is free until the query load after the plan
       w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), C::kQBytes / 4);
       if (w.status == 0) {
         const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
@@ -139,15 +149,17 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
     }
     if (lane == 0) work = w;
-    fence_proxy_async();  // scratch stores before the query load reuses the region
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->s_full[i]), 1);
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&bars->s_part[i]), 1);
+      mbar_init(smem_u32(&bars->s_sum[i]), kRows);
       mbar_init(smem_u32(&bars->s_free[i]), kRows);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->p_full[i]), kRows);
       mbar_init(smem_u32(&bars->pv_done[i]), 1);
     }
@@ -194,140 +206,108 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     const int q_half_off = g ? 0 : 4 * C::kQBox;           // byte offset of the half slab
 
     if (warp < 4) {
-      // =================== softmax / exchange / epilogue ===================
+      // =================== softmax / epilogue ===================
       const int row = tid;
       const bool live = warp * 32 < P.H;
-      bool ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
-      // RoPE in place on this CTA's slabs (the pair kernel only runs when the
-      // rotary channels and their partners lie inside one CTA's slabs).
-      if (ok && P.rd > 0 && row < P.H) {
-        const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;  // full query slabs only
-        if (P.ro >= c_lo && P.ro + P.rd <= c_hi) {
-          const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
-          const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
-          auto at = [&](int d0) -> uint4* {
-            const int slab = (d0 >> 6) - q_full0, ch = (d0 >> 3) & 7;
-            return reinterpret_cast<uint4*>(q_s + q_full_off + slab * C::kQBox + row * 128 +
-                                            ((ch ^ (row & 7)) << 4));
-          };
-          if (!P.interleaved) {
-            const int half = P.rd >> 1;
-            for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
-              float a[8], bb[8], na[8], nb[8];
-              unpack8<T>(*at(d0), a);
-              unpack8<T>(*at(d0 + half), bb);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
-              rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
-              rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
-              *at(d0) = pack8<T>(na);
-              *at(d0 + half) = pack8<T>(nb);
-            }
-          } else {
-            for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
-              float a[8], dummy[8];
-              unpack8<T>(*at(d0), a);
-              rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
-              *at(d0) = pack8<T>(a);
-            }
-          }
-        }
-      }
-      fence_proxy_async();
-      mbar_arrive(smem_u32(&bars->q_full));
-      if (tid == 0) PA_TRACE(3);
-
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      // incoming partial rows (two buffers), chunk-major: 16-byte chunk q of
-      // row r at [q][r], so a warp's store or load of one chunk for its 32
-      // rows is 512 contiguous bytes (one coalesced transfer to the peer)
-      constexpr int kChunks = N / 4;
       float m_used = -INFINITY, l = 0.f;
-      for (int k = 0; k < n && ok; ++k) {
-        const int sb = k & 1;
-        const int64_t j0 = (t_begin + k) * N;
-        const bool edge = j0 < lo || j0 + N - 1 > pos;
-        ok = __all_sync(0xffffffffu,
-                        wait_bar(smem_u32(&bars->s_full[sb]), (k >> 1) & 1, abort, P.err_flags));
-        if (!ok) break;
-        if (tid == 0) PA_TRACE_TILE(k, 0);
-        if (tid == 0 && k == 0) PA_TRACE(4);
-        float s[N];
-        {
-          tc_fence_after();
-          uint32_t r[N / 32][32];
+      bool ok = true;
+      // Pass k = -1 runs the tile code once with every wait, arrive, shared
+      // memory write and state update switched off, on whatever TMEM holds:
+      // it brings the loop's instructions into the instruction cache while
+      // the query and the first key tile are still in flight. (The opaque
+      // start keeps the compiler from peeling it into a copy of its own.)
+      int k_first = -1;
+      asm volatile("" : "+r"(k_first));
+      for (int k = k_first; k < n && ok; ++k) {
+        const bool dry = k < 0;
+        if (k == 0) {  // every work item has n >= 1 tiles
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+          // RoPE in place on this CTA's slabs (the pair kernel only runs when
+          // the rotary channels and their partners lie inside one CTA's slabs).
+          if (ok && P.rd > 0 && row < P.H) {
+            const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;  // full query slabs only
+            if (P.ro >= c_lo && P.ro + P.rd <= c_hi) {
+              const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
+              const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * (P.rd >> 1);
+              auto at = [&](int d0) -> uint4* {
+                const int slab = (d0 >> 6) - q_full0, ch = (d0 >> 3) & 7;
+                return reinterpret_cast<uint4*>(q_s + q_full_off + slab * C::kQBox + row * 128 +
+                                                ((ch ^ (row & 7)) << 4));
+              };
+              if (!P.interleaved) {
+                const int half = P.rd >> 1;
+                for (int d0 = P.ro; d0 < P.ro + half; d0 += 8) {
+                  float a[8], bb[8], na[8], nb[8];
+                  unpack8<T>(*at(d0), a);
+                  unpack8<T>(*at(d0 + half), bb);
 #pragma unroll
-          for (int c = 0; c < N / 32; ++c)
-            tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < N / 32; ++c) {
-            reg_fence(r[c]);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(r[c][e]);
+                  for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+                  rope8<T>(na, bb, d0, P.ro, P.rd, 0, crow, srow);
+                  rope8<T>(nb, a, d0 + half, P.ro, P.rd, 0, crow, srow);
+                  *at(d0) = pack8<T>(na);
+                  *at(d0 + half) = pack8<T>(nb);
+                }
+              } else {
+                for (int d0 = P.ro; d0 < P.ro + P.rd; d0 += 8) {
+                  float a[8], dummy[8];
+                  unpack8<T>(*at(d0), a);
+                  rope8<T>(a, dummy, d0, P.ro, P.rd, 1, crow, srow);
+                  *at(d0) = pack8<T>(a);
+                }
+              }
+            }
           }
-          tc_fence_before();
-        }
-        mbar_arrive(smem_u32(&bars->s_free[sb]));
-        // Send this row's partial into the peer's buffer b = k%2 with st.async
-        // (each store completes its bytes on the peer's x_in[b]); buffer b is
-        // free once the peer has read tile k-2 from it.
-        float* x_buf = x_s + row * 4;
-        const uint32_t x_peer = map_peer(smem_u32(x_buf), peer);
-        const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in), peer);
-        if (k >= 1) {  // the peer has read tile k-1 from its x_s
-          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out), (k - 1) & 1,
-                                                        abort, P.err_flags));
+          fence_proxy_async();
+          mbar_arrive(smem_u32(&bars->q_full));
+          if (tid == 0) PA_TRACE(3);
           if (!ok) break;
         }
-        if (tid == 0) PA_TRACE_TILE(k, 8);
-#pragma unroll
-        for (int q = 0; q < kChunks; ++q)
-          st_async_v4(x_peer + q * kRows * 16, s[4 * q], s[4 * q + 1], s[4 * q + 2], s[4 * q + 3],
-                      x_in_peer);
-        if (tid == 0) PA_TRACE_TILE(k, 9);
-        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in), k & 1, abort,
-                                                      P.err_flags));
-        if (!ok) break;
-        if (tid == 0) PA_TRACE_TILE(k, 12);
-        // S = S_0 + S_1 in that order in both CTAs
-#pragma unroll
-        for (int q = 0; q < kChunks; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(x_buf + q * kRows * 4);
-          if (g == 0) {
-            s[4 * q] += v.x; s[4 * q + 1] += v.y; s[4 * q + 2] += v.z; s[4 * q + 3] += v.w;
-          } else {
-            s[4 * q] = v.x + s[4 * q]; s[4 * q + 1] = v.y + s[4 * q + 1];
-            s[4 * q + 2] = v.z + s[4 * q + 2]; s[4 * q + 3] = v.w + s[4 * q + 3];
-          }
+        const int sb = dry ? 0 : k % NS;   // S buffer
+        const int pb = dry ? 1 : k & 1;    // P buffer
+        const int64_t j0 = (t_begin + k) * N;
+        const bool edge = !dry && (j0 < lo || j0 + N - 1 > pos);
+        if (!dry) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_sum[sb]), (k / NS) & 1, abort,
+                                                P.err_flags));
+          if (!ok) break;
+          if (tid == 0) PA_TRACE_TILE(k, 0);
+          if (tid == 0 && k == 0) PA_TRACE(4);
         }
-        named_sync(3, 128);  // every row of x_s has been read
-        if (tid == 0) {
-          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);
-          arrive_peer_relaxed(map_peer(smem_u32(&bars->x_out), peer));
-        }
-        if (tid == 0) PA_TRACE_TILE(k, 6);
-
+        // The tile is handled in 32-column chunks read from TMEM twice (row
+        // maximum, then exponentials), which keeps the loop body short.
         float factor = 1.f;
         bool rescale = false;
         const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        const uint32_t s_addr = lane_addr + C::kColS + sb * N;
         if (live) {
+          tc_fence_after();
           float mt = -INFINITY;
-          if (P.softcap_on) {
+          const bool rewrite = P.softcap_on || edge;
+#pragma unroll 1
+          for (int c = 0; c < N; c += 32) {
+            uint32_t r[32];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
+            if (rewrite) {
 #pragma unroll
-            for (int c = 0; c < N; ++c) s[c] = P.cap_out * tanh_ex2(s[c] * P.cap_in);
-          }
-          if (edge) {
-#pragma unroll
-            for (int c = 0; c < N; ++c) {
-              const int64_t j = j0 + c;
-              if (j < lo || j > pos) s[c] = -INFINITY;
+              for (int e = 0; e < 32; ++e) {
+                float v = __uint_as_float(r[e]);
+                if (P.softcap_on) v = P.cap_out * tanhf(v * P.cap_in);
+                const int64_t j = j0 + c + e;
+                if (edge && (j < lo || j > pos)) v = -INFINITY;
+                r[e] = __float_as_uint(v);
+              }
+              tmem_st32(s_addr + c, r);
             }
-          }
 #pragma unroll
-          for (int c = 0; c < N; ++c) mt = fmaxf(mt, s[c]);
+            for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
+          }
+          if (rewrite) tmem_wait_st();
           mt *= sl;
-          if (k == 0) {
+          if (dry) {
+          } else if (k == 0) {
             m_used = mt;
           } else if (mt > m_used + kRescaleLog2) {
             factor = ex2(m_used - mt);
@@ -348,29 +328,32 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           fence_proxy_async();
         }
-        if (k >= 2) {
-          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]),
+        if (k >= 2) {  // P buffer pb is free once PV(k-2) has completed
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[pb]),
                                                 ((k - 2) >> 1) & 1, abort, P.err_flags));
           if (!ok) break;
         }
         if (live) {
           tc_fence_after();
           float lsum = 0.f;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < N; c += 32) {
-            uint32_t r[16];
+            uint32_t r[32], pk[16];
+            tmem_ld32_nowait(s_addr + c, r);
+            tmem_wait_ld();
+            reg_fence(r);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(s[c + 2 * e], sl, -m_used));
-              const float p1 = ex2(fmaf(s[c + 2 * e + 1], sl, -m_used));
+              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -m_used));
+              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -m_used));
               lsum += p0 + p1;
-              r[e] = pack2<T>(p0, p1);
+              pk[e] = pack2<T>(p0, p1);
             }
-            tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, r);
+            tmem_st16(lane_addr + C::kColP + pb * (N / 2) + c / 2, pk);
           }
-          l += lsum;
+          if (!dry) l += lsum;
           if (__any_sync(0xffffffffu, rescale)) {
-            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb ^ 1]),
+            ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[pb ^ 1]),
                                                   ((k - 1) >> 1) & 1, abort, P.err_flags));
             if (ok) {
               tc_fence_after();
@@ -389,7 +372,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         if (!ok) break;
         tc_fence_before();
-        mbar_arrive(smem_u32(&bars->p_full[sb]));
+        if (dry) continue;
+        mbar_arrive(smem_u32(&bars->s_free[sb]));
+        mbar_arrive(smem_u32(&bars->p_full[pb]));
         if (tid == 0) PA_TRACE_TILE(k, 1);
       }
 
@@ -442,6 +427,74 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
+    } else if (warp >= 6) {
+      // =================== partial-score exchange ===================
+      // Warp w handles TMEM lanes 32*(w%4)..+31 (the quadrant its SM
+      // sub-partition may access). Per tile: read this CTA's partial S rows,
+      // send them to the peer's x_s with st.async (the bytes complete on the
+      // peer's x_in), wait for the peer's rows, form S_0 + S_1 (that order in
+      // both CTAs) and write the sum back into the S buffer for the softmax
+      // warps. x_s is chunk-major: 16-byte chunk q of row r at [q][r], so a
+      // warp's store of one chunk for its 32 rows is 512 contiguous bytes.
+      constexpr int kChunks = N / 4;
+      const int xq = warp & 3, xrow = xq * 32 + lane, xt = tid - 192;  // xt: 0..127
+      const uint32_t lane_addr = tmem + ((uint32_t)(xq * 32) << 16);
+      float* x_row = x_s + xrow * 4;
+      const uint32_t x_peer = map_peer(smem_u32(x_row), peer);
+      const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in), peer);
+      const uint32_t x_out_peer = map_peer(smem_u32(&bars->x_out), peer);
+      bool ok = true;
+      for (int k = 0; k < n && ok; ++k) {
+        const int sb = k % NS;
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
+                                              P.err_flags));
+        if (!ok) break;
+        if (xt == 0) PA_TRACE_TILE(k, 8);
+        tc_fence_after();
+        uint32_t r[N / 32][32];
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c)
+          tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
+        if (k >= 1) {  // the peer has read tile k-1 from its x_s
+          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out), (k - 1) & 1,
+                                                        abort, P.err_flags));
+          if (!ok) break;
+        }
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q)
+          st_async_b32x4(x_peer + q * kRows * 16, r[q / 8][(4 * q) & 31], r[q / 8][(4 * q + 1) & 31],
+                      r[q / 8][(4 * q + 2) & 31], r[q / 8][(4 * q + 3) & 31], x_in_peer);
+        if (xt == 0) PA_TRACE_TILE(k, 9);
+        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in), k & 1, abort,
+                                                      P.err_flags));
+        if (!ok) break;
+        if (xt == 0) PA_TRACE_TILE(k, 12);
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(x_row + q * kRows * 4);
+          uint32_t* d = &r[q / 8][(4 * q) & 31];
+          const float pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float mine = __uint_as_float(d[e]);
+            d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+          }
+        }
+        named_sync(3, 128);  // every row of x_s has been read
+        if (xt == 0) {
+          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);
+          arrive_peer_relaxed(x_out_peer);
+        }
+#pragma unroll
+        for (int c = 0; c < N / 32; ++c) tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_sum[sb]));
+        if (xt == 0) PA_TRACE_TILE(k, 11);
+      }
     } else if (warp == 4) {
       // =================== TMA producer ===================
       if (lane == 0) {  // this CTA's five query slabs (QR = 128 rows: the token's heads)
@@ -460,6 +513,21 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       bool waited = !P.early;
       const int nsub = N / P.box_rows;
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
+      // First cache row of this lane's box (one cache block) of tile kk, or
+      // -1 when the box holds no visible key or its block id is invalid.
+      auto box_row = [&](int kk, bool report) -> int {
+        const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
+        if (key0 > pos || key0 + P.box_rows - 1 < lo) return -1;
+        const int32_t phys = bt[key0 / P.bs];
+        if (phys < 0 || phys >= P.num_blocks) {
+          if (report) {
+            bars->bad = 1;
+            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+          }
+          return -1;
+        }
+        return (int)((int64_t)phys * P.bs + key0 % P.bs);
+      };
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int stage = k % STAGES;
@@ -474,19 +542,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                            P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
-        const int64_t j0 = (t_begin + k) * N;
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
         if (lane < nsub) {
-          const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
-          if (key0 <= pos && key0 + P.box_rows - 1 >= lo) {
-            const int32_t phys = bt[key0 / P.bs];
-            if (phys >= 0 && phys < P.num_blocks) {
-              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
-            } else {
-              bars->bad = 1;
-              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
-            }
-          }
+          const int yy = box_row(k, true);
+          if (yy >= 0) y = yy;
         }
         if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
         if (lane == 0) PA_TRACE_TILE(k, 5);
@@ -528,28 +587,31 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           while (kp < n) {
             bool progressed = false;
             if (kp < kq) {
-              const int stage = kp % STAGES, sb = kp & 1;
-              if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp >> 1) & 1)) {
+              const int stage = kp % STAGES, pb = kp & 1;
+              if (mbar_test_wait(smem_u32(&bars->p_full[pb]), (kp >> 1) & 1)) {
                 tc_fence_after();
                 const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
-                // descriptor address field (bytes / 16) advances 2048 / 16 per 16
-                // keys
+                // descriptor address field (bytes / 16) advances 2048 / 16 per 16 keys
                 const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
 #pragma unroll
                 for (int kk = 0; kk < N / 16; ++kk)
-                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8,
+                  mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (N / 2) + kk * 8,
                          b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(smem_u32(&bars->pv_done[sb]));
+                tc_commit(smem_u32(&bars->pv_done[pb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
                 PA_TRACE_TILE(kp, 3);
                 ++kp;
                 progressed = true;
               }
             }
+            // QK^T(kq): needs its key tile and a free S buffer (s_free of kq-NS)
+            // (at most two tiles ahead of PV: a PV queued behind more QK^T
+            // in the in-order tensor pipe would hold its key stage longer)
             if (kq < n && kq < kp + 2) {
-              const int stage = kq % STAGES, sb = kq & 1;
+              const int stage = kq % STAGES, sb = kq % NS;
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
-                  (kq < 2 || mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - 2) >> 1) & 1))) {
+                  (kq < NS ||
+                   mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NS) / NS) & 1))) {
                 PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 const uint32_t kb = k_base + stage * C::kStageBytes;
@@ -577,7 +639,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                   mma_ss(tmem + C::kColS + sb * N, a, b0 + (kslab * (C::kKBox >> 4) + w), kIdQK,
                          i > 0 ? 1u : 0u);
                 }
-                tc_commit(smem_u32(&bars->s_full[sb]));
+                tc_commit(smem_u32(&bars->s_part[sb]));
                 PA_TRACE_TILE(kq, 2);
                 ++kq;
                 progressed = true;
@@ -657,14 +719,13 @@ cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& 
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
-  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(kThreads), smem, a.stream,
-                             map, qmap, qmap64, P);
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem,
+                             a.stream, map, qmap, qmap64, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
   return launch_pdl(tc_combine_kernel<T, 256, 2, CombineShape<256, 2>::kCPT>,
                     dim3((unsigned)nq, (unsigned)((g.H + CombineShape<256, 2>::kHPB - 1) /
                                                   CombineShape<256, 2>::kHPB)),
-                    dim3(256), 0,
-                    a.stream, P);
+                    dim3(256), 0, a.stream, P);
 }
 
 template cudaError_t launch_pair<__nv_bfloat16>(const Geometry&, Phase, const ReadArgs&, Params&,
@@ -675,13 +736,14 @@ template cudaError_t launch_pair<__half>(const Geometry&, Phase, const ReadArgs&
 }  // namespace tc
 }  // namespace pa
 
+
 #ifdef PA_TC_TRACE
 extern "C" int pa_trace_pair_dump(void* host, void* tile_host) {
   cudaMemcpyFromSymbol(tile_host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
   return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, sizeof(pa::tc::g_trace));
 }
 extern "C" int pa_trace_pair_clear(void) {
-  static unsigned long long zero[8192][16];  // >= sizeof either trace array
+  static unsigned long long zero[8192][16];
   cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
   return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
 }
