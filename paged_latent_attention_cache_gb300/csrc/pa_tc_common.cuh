@@ -431,9 +431,9 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
   if (lane == 0) PA_TRACE(13);
   // Smallest T with sum_b ceil(n_b / T) <= units. Since n_b / T <=
   // ceil(n_b / T) <= n_b / T + 1, it lies in [ceil(total / units),
-  // ceil(total / (units - nseq))] (total = sum_b n_b; units >= nseq, and
-  // units == nseq forces T = the longest sequence), so a bisection over
-  // that bracket takes a step or two.
+  // ceil(total / (units - nseq))] (total = sum_b n_b; units >= nseq), and
+  // T = the longest sequence (one split each) always fits, so a bisection
+  // over [ceil(total / units), min(that bound, longest)] takes a few steps.
   int total = lane < nseq ? max(own, 0) : 0, longest = total;
   for (int i = lane + 32; i < nseq; i += 32) {
     const int t = (int)decode_tiles(P, seq_begin + i, N);
@@ -448,7 +448,8 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
     longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
   }
   int lo = max(1, ceil_div32(total, units));
-  int hi = units > nseq ? max(lo, ceil_div32(total, units - nseq)) : max(lo, longest);
+  int hi = units > nseq ? min(ceil_div32(total, units - nseq), longest) : longest;
+  hi = max(lo, hi);
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
     if (warp_splits<N>(P, own, mid, nseq, seq_begin, more, cap) <= units) hi = mid; else lo = mid + 1;
