@@ -30,6 +30,9 @@
 // double-buffered in TMEM. Every mbarrier wait is bounded: on expiry the
 // CTA sets PA_DEVERR_TIMEOUT in the error word, drains what it issued and
 // exits without trapping.
+#include <cfloat>
+#include <cmath>
+
 #include "pa_tc_common.cuh"
 
 namespace pa {
@@ -38,7 +41,7 @@ namespace tc {
 // ---------------------------------------------------------------------------
 // The attention kernel
 // ---------------------------------------------------------------------------
-template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB>
+template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB, bool CAP>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ Params P) {
@@ -83,7 +86,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           w.status = 2;
         } else {
           w.t = q0;
-          w.pos = P.past[w.b];
+          w.past = P.past[w.b];
+          w.pos = w.past;
           w.ntok = 1;
         }
       }
@@ -109,6 +113,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         w.b = b;
         w.t = tok;
         w.pos = pos;
+        w.past = P.past[b];
         w.ntok = 1;
         const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
         w.t_begin = lo_key / N;
@@ -117,7 +122,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     if (w.status == 0) {
       const int64_t pos_hi = w.pos + w.ntok - 1;  // the unit's last token
-      const bool bad_ctx = P.past[w.b] < 0 || pos_hi >= (int64_t)P.max_blocks * P.bs ||
+      const bool bad_ctx = w.past < 0 || pos_hi >= (int64_t)P.max_blocks * P.bs ||
                            w.t + w.ntok > P.num_tokens;
       const bool bad_pos = P.rd > 0 && pos_hi >= P.cos_rows;
       if (bad_ctx || bad_pos) {
@@ -255,40 +260,64 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (tid == 0) PA_TRACE_TILE(k, 0);
         }
         // The tile is handled in 32-column chunks read from TMEM twice (row
-        // maximum, then exponentials), which keeps the loop body short:
-        // the first tile then does not wait long for its instructions.
+        // maximum of the raw scores, then probabilities), which keeps the
+        // loop body short: the first tile then does not wait long for its
+        // instructions. The softcap c*tanh(x/c) is increasing, so the
+        // maximum of the capped scores is the cap of the raw maximum and
+        // only pass 2 applies it, per element.
         float factor = 1.f;
         bool rescale = false;
-        // Scores in the log2 domain are x * sl (sl = scale*log2e) without
-        // softcap; with softcap they are rewritten in place and sl = 1.
-        const float sl = P.softcap_on ? 1.f : P.scale_log2;
+        // Scores in the log2 domain: v * sl (sl = scale*log2e) without
+        // softcap, cap_out * tanh(v * cap_in) with it.
+        const float sl = CAP ? 1.f : P.scale_log2;
         const uint32_t s_addr = lane_addr + C::kColS + sb * N;
+        // this row's visible columns [clo, chi] of the tile
+        int clo = 0, chi = N - 1;
+        if (edge) {
+          clo = (int)min((int64_t)N, max((int64_t)0, lo_r - j0));
+          chi = (int)max((int64_t)-1, min((int64_t)(N - 1), pos_r - j0));
+        }
+        int mode = 2;  // softcap in pass 2: 1 series, 2 tanh_ex2
         if (live) {
           tc_fence_after();
-          float mt = -INFINITY;
-          const bool rewrite = P.softcap_on || edge;
+          float vmax = -INFINITY, vmin = INFINITY;  // over the visible raw scores
 #pragma unroll 1
           for (int c = 0; c < N; c += 32) {
             uint32_t r[32];
             tmem_ld32_nowait(s_addr + c, r);
             tmem_wait_ld();
             reg_fence(r);
-            if (rewrite) {
+            if (c >= clo && c + 31 <= chi) {
+              if (CAP) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                  vmax = fmaxf(vmax, __uint_as_float(r[e]));
+                  vmin = fminf(vmin, __uint_as_float(r[e]));
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) vmax = fmaxf(vmax, __uint_as_float(r[e]));
+              }
+            } else {
 #pragma unroll
               for (int e = 0; e < 32; ++e) {
-                float v = __uint_as_float(r[e]);
-                if (P.softcap_on) v = P.cap_out * tanh_ex2(v * P.cap_in);
-                const int64_t j = j0 + c + e;
-                if (edge && (j < lo_r || j > pos_r)) v = -INFINITY;
-                r[e] = __float_as_uint(v);
+                if (c + e >= clo && c + e <= chi) {
+                  vmax = fmaxf(vmax, __uint_as_float(r[e]));
+                  vmin = fminf(vmin, __uint_as_float(r[e]));
+                }
               }
-              tmem_st32(s_addr + c, r);
             }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(r[e]));
           }
-          if (rewrite) tmem_wait_st();
-          mt *= sl;  // order-preserving (sl > 0)
+          float mt;  // the tile's row maximum in the log2 domain
+          if (CAP) {
+            mt = vmax == -INFINITY ? -INFINITY : P.cap_out * tanh_ex2(vmax * P.cap_in);
+            // the series serves the whole warp's tile when every real row's
+            // scores are small (the dry pass takes it to warm its code)
+            const bool small = row >= rows || fmaxf(vmax, -vmin) <= P.cap_vlim;
+            mode = (P.cap_poly && __all_sync(0xffffffffu, small || dry)) ? 1 : 2;
+          } else {
+            mt = vmax * sl;
+          }
           if (dry) {
           } else if (k == 0) {
             m_used = mt;
@@ -331,19 +360,22 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // a row that has seen no key yet (several tokens per unit, window)
           // has every score at -inf: its probabilities are 0, not NaN
           const float mu = m_used == -INFINITY ? 0.f : m_used;
+          const ExpArgs A{sl, mu, P.cap_in, P.cap_out, P.cap_a[0], P.cap_a[1], P.cap_a[2],
+                          P.cap_a[3], P.cap_a[4]};
 #pragma unroll 1
           for (int c = 0; c < N; c += 32) {
             uint32_t r[32], pk[16];
             tmem_ld32_nowait(s_addr + c, r);
             tmem_wait_ld();
             reg_fence(r);
+            if (!(c >= clo && c + 31 <= chi)) {  // masked keys: v = -inf
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -mu));
-              const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -mu));
-              lsum += p0 + p1;
-              pk[e] = pack2<T>(p0, p1);
+              for (int e = 0; e < 32; ++e)
+                if (c + e < clo || c + e > chi) r[e] = __float_as_uint(-INFINITY);
             }
+            if (!CAP) lsum += exp_chunk<T, 0>(r, pk, A);
+            else if (mode == 1) lsum += exp_chunk<T, 1>(r, pk, A);
+            else lsum += exp_chunk<T, 2>(r, pk, A);
             tmem_st16(lane_addr + C::kColP + sb * (N / 2) + c / 2, pk);
           }
           if (!dry) l += lsum;
@@ -436,9 +468,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // after griddepcontrol.wait, except (P.own_slots) the tiles below the
       // sequence's first new position, which the write does not touch.
       int dirty_from = 0;
-      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, P.past[b] / N - t_begin);
+      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, W.past / N - t_begin);
       bool waited = !P.early;
       const int nsub = N / P.box_rows;
+      // (Block ids are looked up tile by tile here: fetching them ahead, as
+      // the CTA-pair kernel does, issues the first stages of every CTA at
+      // once, and the first tiles then arrive later behind that burst.)
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
@@ -454,13 +489,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                            P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
-        const int64_t j0 = (t_begin + k) * N;
         if (lane == 0 && k == 0) PA_TRACE(8);
         if (lane == 0 && k == n - 1) PA_TRACE(9);
         // coordinates of the nsub boxes of rows (one cache block each)
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
         if (lane < nsub) {
-          const int64_t key0 = j0 + (int64_t)lane * P.box_rows;
+          const int64_t key0 = (t_begin + k) * N + (int64_t)lane * P.box_rows;
           if (key0 <= pos_hi && key0 + P.box_rows - 1 >= lo) {
             const int32_t phys = bt[key0 / P.bs];
             if (phys >= 0 && phys < P.num_blocks) {
@@ -626,13 +660,16 @@ template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB>
 cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
   using C = Cfg<HS, VG, G, N, STAGES, QR, NB>;
   const size_t smem = C::kSmemData + sizeof(Barriers) + 1024;
-  static bool configured[64] = {false};
-  auto kern = tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB>;
-  if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
+  // the softcap code is compiled only into the kernels that use it
+  static bool configured[2][64] = {};
+  const int cap = P.softcap_on ? 1 : 0;
+  auto kern = cap ? tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB, true>
+                  : tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB, false>;
+  if (g.device >= 0 && g.device < 64 && !configured[cap][g.device]) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    configured[g.device] = true;
+    configured[cap][g.device] = true;
   }
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -727,6 +764,29 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.softcap_on = g.softcap > 0.f ? 1 : 0;
   P.cap_in = g.softcap > 0.f ? g.scale / g.softcap : 0.f;
   P.cap_out = g.softcap * tc::kLog2e;
+  // Series coefficients a_(2i+1) = softcap * log2(e) * t_(2i+1) * (scale /
+  // softcap)^(2i+1), t = 1, -1/3, 2/15, -17/315, 62/2835 (the Maclaurin
+  // coefficients of tanh); the series is used only when all are normal floats.
+  P.cap_poly = 0;
+  P.cap_vlim = 0.f;
+  for (int i = 0; i < 5; ++i) P.cap_a[i] = 0.f;
+  if (g.softcap > 0.f) {
+    const double ci = (double)g.scale / (double)g.softcap;
+    const double co = (double)g.softcap * 1.4426950408889634;
+    const double t[5] = {1.0, -1.0 / 3.0, 2.0 / 15.0, -17.0 / 315.0, 62.0 / 2835.0};
+    bool normal = true;
+    double pw = ci;
+    for (int i = 0; i < 5; ++i) {
+      const double a = co * t[i] * pw;
+      normal = normal && std::isfinite(a) && std::fabs(a) >= (double)FLT_MIN &&
+               std::fabs(a) <= (double)FLT_MAX;
+      P.cap_a[i] = (float)a;
+      pw *= ci * ci;
+    }
+    const double vlim = 0.25 / ci;
+    P.cap_poly = normal && vlim <= (double)FLT_MAX ? 1 : 0;
+    P.cap_vlim = P.cap_poly ? (float)vlim : 0.f;
+  }
   P.window = g.window;
   P.decode = ph == Phase::kDecode ? 1 : 0;
   P.box_rows = s.n < g.bs ? s.n : g.bs;

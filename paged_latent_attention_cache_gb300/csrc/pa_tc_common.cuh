@@ -241,6 +241,13 @@ struct Params {
   float cap_in;      // scale / softcap   (softcap > 0)
   float cap_out;     // softcap * log2(e)
   int softcap_on;
+  // Softcap by its odd series in the raw score v: cap_out * tanh(v * cap_in)
+  // = v * (cap_a[0] + v^2 (cap_a[1] + ... + v^2 cap_a[4])), used where
+  // |v| <= cap_vlim (|v * cap_in| <= 1/4) when cap_poly (coefficients
+  // representable as normal floats).
+  float cap_a[5];
+  float cap_vlim;
+  int cap_poly;
   int window;
   int units;         // decode: CTA units (per value group) the grid provides
   int decode;
@@ -289,9 +296,49 @@ struct Barriers {
 // Resolved work of one CTA (written by warp 0 during the prologue).
 struct Work {
   int64_t t, pos, t_begin, t_end;  // t, pos: the unit's first token and its position
+  int64_t past;                    // past_seqlens[b]: the sequence's first new position
   int b, splits, first, split;
   int ntok;    // consecutive tokens of sequence b in the unit (rows = ntok * H)
   int status;  // 0 = run, 1 = idle, 2 = error already reported (write nothing more)
+};
+
+// Block ids of the key boxes a producer warp copies, requested 32 boxes at
+// a time ahead of use. Box i of the CTA's key range starts at key
+// key0 + i * box_rows and lies in one cache block; lane l holds the id of
+// box 32 * j + l of the batch j in use, and batch j + 1 is requested as soon
+// as batch j comes into use, so the block-table load is normally complete
+// before a tile's copies are issued instead of on every tile's path.
+// Boxes with no visible key (outside [lo, hi]) or past the range are not
+// looked up.
+struct BlockIds {
+  const int32_t* bt;  // the sequence's block-table row
+  int64_t key0, lo, hi;
+  int box_rows, bs, nbox;
+  int cur, nxt, batch;
+  __device__ __forceinline__ bool visible(int i) const {
+    const int64_t key = key0 + (int64_t)i * box_rows;
+    return i < nbox && key <= hi && key + box_rows - 1 >= lo;
+  }
+  __device__ __forceinline__ int fetch(int i) const {
+    return visible(i) ? bt[(key0 + (int64_t)i * box_rows) / bs] : 0;
+  }
+  __device__ __forceinline__ void start(int lane) {
+    batch = 0;
+    cur = fetch(lane);
+    nxt = fetch(32 + lane);
+  }
+  // Id of box `first + sub` (first: a multiple of the boxes per tile, which
+  // divides 32; sub < boxes per tile). Called by the whole warp with
+  // boxes in increasing order.
+  __device__ __forceinline__ int get(int first, int sub, int lane) {
+    const int j = first >> 5;
+    if (j != batch) {  // the next batch (uniform across the warp)
+      batch = j;
+      cur = nxt;
+      nxt = fetch(32 * (j + 1) + lane);
+    }
+    return __shfl_sync(0xffffffffu, cur, (first & 31) + sub);
+  }
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -363,6 +410,49 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Probabilities of one 32-column chunk of a row's scores (softmax pass 2):
+// p = 2^(s - mu) with s the log2-domain score of the raw product v, packed
+// to 16 bits in pk; returns their sum. A masked key arrives as v = -inf and
+// gets p = 0 in every mode. MODE 0: no softcap, s = v * sl. MODE 1:
+// softcap by the Maclaurin series of tanh truncated after the ninth power,
+// s = v * (a1 + v^2 (a3 + v^2 (a5 + v^2 (a7 + v^2 a9)))); for
+// |v * cap_in| <= 1/4 the series alternates with decreasing terms, so the
+// truncation error is below its next term, 1382/155925 * 4^-11 < 3e-9
+// (relative to softcap), under the rounding of the evaluation; v = -inf
+// gives q = +inf (a9 > 0) and s = -inf. MODE 2: softcap through tanh_ex2
+// (any score), with v = -inf mapped to s = -inf explicitly.
+struct ExpArgs {
+  float sl, mu, cap_in, cap_out, a1, a3, a5, a7, a9;
+};
+template <typename T, int MODE>
+__device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], uint32_t (&pk)[16],
+                                           const ExpArgs& A) {
+  float lsum = 0.f;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    float p[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float v = __uint_as_float(r[2 * e + h]);
+      float x;
+      if (MODE == 0) {
+        x = fmaf(v, A.sl, -A.mu);
+      } else if (MODE == 1) {
+        const float v2 = v * v;
+        const float q = fmaf(fmaf(fmaf(fmaf(A.a9, v2, A.a7), v2, A.a5), v2, A.a3), v2, A.a1);
+        x = fmaf(v, q, -A.mu);
+      } else {
+        x = fmaf(A.cap_out, tanh_ex2(v * A.cap_in), -A.mu);
+        if (v == -INFINITY) x = -INFINITY;
+      }
+      p[h] = ex2(x);
+    }
+    lsum += p[0] + p[1];
+    pk[e] = pack2<T>(p[0], p[1]);
+  }
+  return lsum;
 }
 
 // ---------------------------------------------------------------------------
@@ -554,7 +644,8 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
       w.b = seq_begin + base + src;
       w.t = first + (int64_t)grp * tpc;
       w.ntok = min(tpc, len - grp * tpc);
-      w.pos = (int64_t)P.past[w.b] + grp * tpc;
+      w.past = P.past[w.b];
+      w.pos = w.past + grp * tpc;
       w.status = 0;
       return w;
     }

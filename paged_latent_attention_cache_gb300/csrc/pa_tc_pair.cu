@@ -111,7 +111,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           w.status = 2;
         } else {
           w.t = q0;
-          w.pos = P.past[w.b];
+          w.past = P.past[w.b];
+          w.pos = w.past;
         }
       }
     } else {
@@ -129,13 +130,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         w.b = b;
         w.t = tok;
         w.pos = pos;
+        w.past = P.past[b];
         const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
         w.t_begin = lo_key / N;
         w.t_end = pos / N + 1;
       }
     }
     if (w.status == 0) {
-      const bool bad_ctx = P.past[w.b] < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
+      const bool bad_ctx = w.past < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
       const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
       if (bad_ctx || bad_pos) {
         if (lane == 0 && g == 0)
@@ -509,25 +511,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // after griddepcontrol.wait, except (P.own_slots) the tiles below the
       // sequence's first new position, which the write does not touch.
       int dirty_from = 0;
-      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, P.past[b] / N - t_begin);
+      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, W.past / N - t_begin);
       bool waited = !P.early;
       const int nsub = N / P.box_rows;
-      const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
-      // First cache row of this lane's box (one cache block) of tile kk, or
-      // -1 when the box holds no visible key or its block id is invalid.
-      auto box_row = [&](int kk, bool report) -> int {
-        const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
-        if (key0 > pos || key0 + P.box_rows - 1 < lo) return -1;
-        const int32_t phys = bt[key0 / P.bs];
-        if (phys < 0 || phys >= P.num_blocks) {
-          if (report) {
-            bars->bad = 1;
-            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
-          }
-          return -1;
-        }
-        return (int)((int64_t)phys * P.bs + key0 % P.bs);
-      };
+      BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
+                   P.box_rows, P.bs, n * nsub};
+      ids.start(lane);
       int issued = 0;
       for (int k = 0; k < n; ++k) {
         const int stage = k % STAGES;
@@ -543,9 +532,15 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
-        if (lane < nsub) {
-          const int yy = box_row(k, true);
-          if (yy >= 0) y = yy;
+        const int phys = ids.get(k * nsub, lane & (nsub - 1), lane);
+        if (lane < nsub && ids.visible(k * nsub + lane)) {
+          if (phys >= 0 && phys < P.num_blocks) {
+            const int64_t key0 = (t_begin + k) * N + (int64_t)lane * P.box_rows;
+            y = (int)((int64_t)phys * P.bs + key0 % P.bs);
+          } else {
+            bars->bad = 1;
+            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+          }
         }
         if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
         if (lane == 0) PA_TRACE_TILE(k, 5);

@@ -32,6 +32,7 @@ VARIANTS = {
     "window_5": dict(local_window_size=5),
     "window_huge": dict(local_window_size=1 << 20),
     "softcap_3": dict(softcap=3.0),
+    "softcap_tight": dict(softcap=0.5, scale=0.3),
     "fp16": dict(dtype=torch.float16),
     "rotary_at_0": dict(rotary_offset=0, rotary_dim=32),
 }
