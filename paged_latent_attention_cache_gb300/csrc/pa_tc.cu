@@ -26,6 +26,8 @@
 //   warp 4     TMA producer: per key tile, one 2-D box (64 channels x rows of
 //              one cache block) per 64-channel slab, 128-byte swizzle.
 //   warp 5     TMEM allocation and the single MMA-issuing thread.
+//   (With 64 query rows the producer and MMA warps are 6 and 7, on other
+//   scheduler partitions than the two softmax warps that hold rows.)
 // Pipelines: K tiles in a STAGES-deep ring (full/empty mbarriers), S and P
 // double-buffered in TMEM. Every mbarrier wait is bounded: on expiry the
 // CTA sets PA_DEVERR_TIMEOUT in the error word, drains what it issued and
@@ -42,7 +44,7 @@ namespace tc {
 // The attention kernel
 // ---------------------------------------------------------------------------
 template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB, bool CAP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((Cfg<HS, VG, G, N, STAGES, QR, NB>::kThreads), 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ Params P) {
   using C = Cfg<HS, VG, G, N, STAGES, QR, NB>;
@@ -157,10 +159,10 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     bars->bad = 0;
     bars->abort = 0;
     fence_barrier_init();
-  } else if (warp == 4 && lane == 0) {
+  } else if (warp == C::kProdWarp && lane == 0) {
     prefetch_tmap(&kmap);
     prefetch_tmap(&qmap);
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
@@ -456,7 +458,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
-    } else if (warp == 4) {
+    } else if (warp == C::kProdWarp) {
       // =================== TMA producer ===================
       if (lane == 0) {  // Q: one box of QR rows (this token's heads) per 64-channel slab
         const uint32_t qb = smem_u32(&bars->q_tma);
@@ -529,7 +531,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       }
       __syncwarp();
       named_arrive(2, 160);
-    } else if (warp == 5) {
+    } else if (warp == C::kMmaWarp) {
       // =================== MMA issuer ===================
       if (lane == 0) {
         constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -623,7 +625,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (tid == 0) PA_TRACE(6);
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
@@ -695,7 +697,7 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
-  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(kThreads), smem, a.stream,
+  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(C::kThreads), smem, a.stream,
                              map, qmap, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
   return launch_pdl(tc_combine_kernel<T, VG, G, CombineShape<VG, G>::kCPT>,

@@ -280,6 +280,13 @@ struct Cfg {
   static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 128, "shape");
   static_assert(STAGES <= 8, "stages");
   static_assert(QR == 64 || QR == 128, "query rows");
+  // Warp roles: 0-3 softmax; producer and MMA issuer on warps 4 and 5, or,
+  // with 64 query rows (only softmax warps 0 and 1 hold rows), on warps 6
+  // and 7, which share no scheduler partition (warp % 4) with a live
+  // softmax warp; warps 4 and 5 then have no role.
+  static constexpr int kProdWarp = QR == 64 ? 6 : 4;
+  static constexpr int kMmaWarp = kProdWarp + 1;
+  static constexpr int kThreads = 32 * (kMmaWarp + 1);
   static_assert(NB == 1 || NB == 2, "S/P buffers");
 };
 
