@@ -41,6 +41,33 @@ namespace pa {
 namespace tc {
 
 // ---------------------------------------------------------------------------
+// MMA issue sequences. Not inlined: the MMA warp runs each once on scratch
+// operands during the prologue (see the MMA issuer), which brings these
+// instructions into the instruction cache and starts the tensor pipe
+// before the first key tile lands, while the memory system is still idle.
+// ---------------------------------------------------------------------------
+// S(d) = Q K^T over HS channels: K-steps of 16 (32 bytes) within each
+// 128-byte slab; the descriptors' address fields (bytes / 16) advance.
+template <int HS, int QBOX, int KBOX, uint32_t kId>
+__device__ __noinline__ void issue_qk(uint32_t d, uint64_t a0, uint64_t b0) {
+#pragma unroll
+  for (int kk = 0; kk < HS / 16; ++kk) {
+    const uint32_t col = (uint32_t)(kk & 3) * 2;  // 32 bytes / 16
+    const uint32_t slab = (uint32_t)(kk >> 2);
+    mma_ss(d, a0 + (slab * (QBOX >> 4) + col), b0 + (slab * (KBOX >> 4) + col), kId,
+           kk > 0 ? 1u : 0u);
+  }
+}
+// O(d) (+)= P(a) V over N keys: K-steps of 16 keys (8 TMEM columns of
+// packed 16-bit P; 2048 bytes of MN-major V, 128 in the address field).
+template <int N, uint32_t kId>
+__device__ __noinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t b0, uint32_t acc0) {
+#pragma unroll
+  for (int kk = 0; kk < N / 16; ++kk)
+    mma_ts(d, a + kk * 8, b0 + (uint64_t)(kk * 128), kId, (acc0 || kk > 0) ? 1u : 0u);
+}
+
+// ---------------------------------------------------------------------------
 // The attention kernel
 // ---------------------------------------------------------------------------
 template <typename T, int HS, int VG, int G, int N, int STAGES, int QR, int NB, bool CAP>
@@ -539,6 +566,16 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
         const uint32_t q_base = smem_u32(q_s);
         const uint32_t k_base = smem_u32(k_s);
+        const uint32_t v_off = (g * (VG / 64)) * C::kKBox;  // this group's value slabs
+        // Warm-up: one QK^T into S buffer NB-1 and one PV into O, on whatever
+        // shared memory and TMEM hold. Both are overwritten before they are
+        // read (QK^T(NB-1) and PV(0) start without accumulation; the
+        // softmax's dry pass reads S buffer NB-1 as scratch), and every later
+        // commit also tracks them.
+        issue_qk<HS, C::kQBox, C::kKBox, kIdQK>(tmem + C::kColS + (NB - 1) * N,
+                                                sdesc(q_base, 16, 1024), sdesc(k_base, 16, 1024));
+        issue_pv<N, kIdPV>(tmem + C::kColO, tmem + C::kColP + (NB - 1) * (N / 2),
+                           sdesc(k_base + v_off, C::kKBox, 1024), 0u);
         bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
         if (ok) {
           tc_fence_after();
@@ -556,16 +593,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const int stage = kp % STAGES, sb = kp % NB;
               if (mbar_test_wait(smem_u32(&bars->p_full[sb]), (kp / NB) & 1)) {
                 tc_fence_after();
-                const uint32_t vb = k_base + stage * C::kStageBytes + (g * (VG / 64)) * C::kKBox;
-                // B = V[keys 16kk.., channels]: MN-major, 64-channel slabs kKBox
-                // apart (leading offset), 8-key groups 1024 bytes apart (stride).
-                // The descriptor's address field (bytes / 16) advances by 2048 / 16
-                // per 16 keys.
-                const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
-#pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk)
-                  mma_ts(tmem + C::kColO, tmem + C::kColP + sb * (N / 2) + kk * 8,
-                         b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
+                // B = V[keys, channels]: MN-major, 64-channel slabs kKBox apart
+                // (leading offset), 8-key groups 1024 bytes apart (stride).
+                issue_pv<N, kIdPV>(tmem + C::kColO, tmem + C::kColP + sb * (N / 2),
+                                   sdesc(k_base + stage * C::kStageBytes + v_off, C::kKBox, 1024),
+                                   kp > 0 ? 1u : 0u);
                 tc_commit(smem_u32(&bars->pv_done[sb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
                 PA_TRACE_TILE(kp, 3);
@@ -581,16 +613,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                    mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NB) / NB) & 1))) {
                 PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
-                const uint32_t kb = k_base + stage * C::kStageBytes;
-                const uint64_t a0 = sdesc(q_base, 16, 1024), b0 = sdesc(kb, 16, 1024);
-#pragma unroll
-                for (int kk = 0; kk < HS / 16; ++kk) {
-                  // step kk: slab kk/4, 32-byte column (kk%4) of the 128-byte rows
-                  const uint32_t col = (uint32_t)(kk & 3) * 2;  // 32 bytes / 16
-                  const uint32_t slab = (uint32_t)(kk >> 2);
-                  mma_ss(tmem + C::kColS + sb * N, a0 + (slab * (C::kQBox >> 4) + col),
-                         b0 + (slab * (C::kKBox >> 4) + col), kIdQK, kk > 0 ? 1u : 0u);
-                }
+                issue_qk<HS, C::kQBox, C::kKBox, kIdQK>(
+                    tmem + C::kColS + sb * N, sdesc(q_base, 16, 1024),
+                    sdesc(k_base + stage * C::kStageBytes, 16, 1024));
                 tc_commit(smem_u32(&bars->s_full[sb]));
                 PA_TRACE_TILE(kq, 2);
                 ++kq;

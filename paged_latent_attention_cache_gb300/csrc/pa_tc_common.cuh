@@ -472,9 +472,10 @@ __device__ __forceinline__ float exp_chunk(const uint32_t (&r)[32], uint32_t (&p
 // trip or separate planning launch is needed.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int64_t decode_tiles(const Params& P, int b, int n_tile) {
+  // (the three loads are issued together: b is a valid sequence index)
   const int32_t q0 = P.cumseq[b], q1 = P.cumseq[b + 1];
-  if (q1 - q0 != 1 || q0 < 0 || q0 >= P.num_tokens) return 0;
   const int64_t pos = P.past[b];
+  if (q1 - q0 != 1 || q0 < 0 || q0 >= P.num_tokens) return 0;
   if (pos < 0 || pos >= (int64_t)P.max_blocks * P.bs || (P.rd > 0 && pos >= P.cos_rows)) return 0;
   const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
   return pos / n_tile - lo / n_tile + 1;
