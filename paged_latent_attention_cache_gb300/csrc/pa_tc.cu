@@ -788,6 +788,13 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.num_blocks = g.num_blocks;
   P.max_blocks = g.max_blocks;
   P.scale_log2 = g.scale * tc::kLog2e;
+  {
+    int e = 0;
+    if (P.scale_log2 > 0.f && std::isfinite(P.scale_log2)) e = std::ilogb(P.scale_log2);
+    e = e < -60 ? -60 : e > 60 ? 60 : e;
+    P.xscale = std::ldexp(1.f, e);
+    P.xunscale = std::ldexp(1.f, -e);
+  }
   P.softcap_on = g.softcap > 0.f ? 1 : 0;
   P.cap_in = g.softcap > 0.f ? g.scale / g.softcap : 0.f;
   P.cap_out = g.softcap * tc::kLog2e;

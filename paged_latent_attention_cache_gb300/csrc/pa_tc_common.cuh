@@ -238,6 +238,9 @@ struct Params {
   int num_seqs, seq_begin, seq_end;
   int H, vhs, ro, rd, interleaved, cos_rows, bs, num_blocks, max_blocks;
   float scale_log2;  // scale * log2(e)
+  float xscale, xunscale;  // a power of two near scale_log2, and its inverse (CTA-pair
+                           // score exchange in 16 bits: partial scores travel as
+                           // fp16(S_c * xscale))
   float cap_in;      // scale / softcap   (softcap > 0)
   float cap_out;     // softcap * log2(e)
   int softcap_on;

@@ -19,6 +19,9 @@
 // mbarrier), add the peer's rows (S_0 + S_1 in that order in both CTAs, so
 // both hold bit-identical S, P, m and l) and write the sum back for the
 // softmax warps; the exchange of tile k+1 overlaps the softmax of tile k.
+// With bf16 inputs the partials travel as fp16 in units of a power of two
+// near scale*log2e (16 KB per tile, two tiles in flight); fp16 inputs send
+// f32 partials (32 KB, one tile in flight).
 // Three S buffers: O 256 + 3 x 64 + P 2 x 32 = 512 TMEM columns.
 //
 // Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
@@ -58,9 +61,9 @@ struct PairBarriers {
   uint64_t s_free[3];  // the softmax warps are done with the S buffer (128 arrivals)
   uint64_t p_full[2], pv_done[2];
   uint64_t q_tma, q_full;
-  uint64_t x_in;    // x_s holds the peer's partial rows (local expect_tx + the
-                    // peer's st.async complete_tx bytes)
-  uint64_t x_out;   // the peer has read the rows this CTA sent into its x_s
+  uint64_t x_in[2];   // x_s buffer b holds the peer's partial rows (local expect_tx +
+                       // the peer's st.async complete_tx bytes)
+  uint64_t x_out[2];  // the peer has read the rows this CTA sent into its buffer b
   uint64_t drain;
   uint32_t tmem_base;
   int bad;
@@ -73,6 +76,17 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
   using C = PairCfg<N, STAGES>;
   constexpr int G = 2, VG = C::kVG, NS = C::kSBufs;
+  // Score exchange format. bf16 inputs: partial scores travel as fp16 in
+  // units of xscale (a power of two near scale*log2e), 16 KB per tile, and
+  // x_s holds two tiles, so a tile is sent without waiting for the peer to
+  // have read the previous one. The 16-bit rounding of a partial logit L is
+  // at most |L| * 2^-11, below the rounding P itself gets as bf16 (2^-9
+  // relative) for |L| < 4 and of that order beyond. fp16 inputs (P kept to
+  // 2^-11): f32 partials, 32 KB per tile, one buffer.
+  constexpr bool kHalfX = std::is_same<T, __nv_bfloat16>::value;
+  constexpr int kXBufs = kHalfX ? 2 : 1;
+  constexpr int kXTile = kHalfX ? kRows * N * 2 : kRows * N * 4;  // bytes per tile
+  static_assert(kXBufs * kXTile <= C::kXBytes, "exchange buffers");
   extern __shared__ uint8_t smem_raw[];
   __shared__ Work work;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -167,9 +181,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     mbar_init(smem_u32(&bars->q_tma), 1);
     mbar_init(smem_u32(&bars->q_full), kRows);
-    mbar_init(smem_u32(&bars->x_in), 1);
-    mbar_init(smem_u32(&bars->x_out), 1);
-    mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);  // armed for tile 0
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bars->x_in[i]), 1);
+      mbar_init(smem_u32(&bars->x_out[i]), 1);
+    }
+    // armed for tiles 0 (and 1 with two exchange buffers)
+    mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
+    if (kXBufs == 2) mbar_expect_tx(smem_u32(&bars->x_in[1]), kXTile);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->bad = 0;
     bars->abort = 0;
@@ -437,17 +455,23 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // peer's x_in), wait for the peer's rows, form S_0 + S_1 (that order in
       // both CTAs) and write the sum back into the S buffer for the softmax
       // warps. x_s is chunk-major: 16-byte chunk q of row r at [q][r], so a
-      // warp's store of one chunk for its 32 rows is 512 contiguous bytes.
-      constexpr int kChunks = N / 4;
+      // warp's store of one chunk for its 32 rows is 512 contiguous bytes;
+      // with the 16-bit format it holds two such tiles (buffers 0 and 1).
+      // The sum is exact up to one rounding and the same in both CTAs.
+      constexpr int kChunks = kHalfX ? N / 8 : N / 4;  // 16-byte chunks per row and tile
       const int xq = warp & 3, xrow = xq * 32 + lane, xt = tid - 192;  // xt: 0..127
       const uint32_t lane_addr = tmem + ((uint32_t)(xq * 32) << 16);
-      float* x_row = x_s + xrow * 4;
-      const uint32_t x_peer = map_peer(smem_u32(x_row), peer);
-      const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in), peer);
-      const uint32_t x_out_peer = map_peer(smem_u32(&bars->x_out), peer);
+      const uint32_t x_row = smem_u32(x_s) + xrow * 16;  // chunk 0 of this row, buffer 0
+      const uint32_t x_peer = map_peer(x_row, peer);
+      const uint32_t x_in_peer0 = map_peer(smem_u32(&bars->x_in[0]), peer);
+      const uint32_t x_in_peer1 = map_peer(smem_u32(&bars->x_in[1]), peer);
+      const uint32_t x_out_peer0 = map_peer(smem_u32(&bars->x_out[0]), peer);
+      const uint32_t x_out_peer1 = map_peer(smem_u32(&bars->x_out[1]), peer);
+      const float xs = P.xscale, xu = P.xunscale;
       bool ok = true;
       for (int k = 0; k < n && ok; ++k) {
         const int sb = k % NS;
+        const int xb = kXBufs == 2 ? (k & 1) : 0;  // exchange buffer of tile k
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
                                               P.err_flags));
         if (!ok) break;
@@ -460,35 +484,75 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         tmem_wait_ld();
 #pragma unroll
         for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
-        if (k >= 1) {  // the peer has read tile k-1 from its x_s
-          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out), (k - 1) & 1,
-                                                        abort, P.err_flags));
-          if (!ok) break;
-        }
+        // 16-bit format: round this CTA's partial the way the peer will see
+        // it, and keep the rounded values (in xscale units) for the sum
+        uint32_t hx[kHalfX ? N / 2 : 1];
+        if (kHalfX) {
 #pragma unroll
-        for (int q = 0; q < kChunks; ++q)
-          st_async_b32x4(x_peer + q * kRows * 16, r[q / 8][(4 * q) & 31], r[q / 8][(4 * q + 1) & 31],
-                      r[q / 8][(4 * q + 2) & 31], r[q / 8][(4 * q + 3) & 31], x_in_peer);
-        if (xt == 0) PA_TRACE_TILE(k, 9);
-        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in), k & 1, abort,
-                                                      P.err_flags));
-        if (!ok) break;
-        if (xt == 0) PA_TRACE_TILE(k, 12);
-#pragma unroll
-        for (int q = 0; q < kChunks; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(x_row + q * kRows * 4);
-          uint32_t* d = &r[q / 8][(4 * q) & 31];
-          const float pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float mine = __uint_as_float(d[e]);
-            d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+          for (int j = 0; j < N / 2; ++j) {
+            const int c0 = 2 * j;
+            uint32_t* d = &r[c0 / 32][c0 & 31];
+            __half2 h = __floats2half2_rn(__uint_as_float(d[0]) * xs, __uint_as_float(d[1]) * xs);
+            hx[j] = *reinterpret_cast<uint32_t*>(&h);
+            const float2 f = __half22float2(h);
+            d[0] = __float_as_uint(f.x);
+            d[1] = __float_as_uint(f.y);
           }
         }
-        named_sync(3, 128);  // every row of x_s has been read
+        if (k >= kXBufs) {  // the peer has read tile k - kXBufs from buffer xb
+          ok = __all_sync(0xffffffffu,
+                          wait_bar_cluster(smem_u32(&bars->x_out[xb]), ((k - kXBufs) / kXBufs) & 1,
+                                           abort, P.err_flags));
+          if (!ok) break;
+        }
+        const uint32_t dst = x_peer + xb * kXTile;
+        const uint32_t x_in_p = xb ? x_in_peer1 : x_in_peer0;
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q) {
+          if (kHalfX)
+            st_async_b32x4(dst + q * kRows * 16, hx[4 * q], hx[4 * q + 1], hx[4 * q + 2],
+                           hx[4 * q + 3], x_in_p);
+          else
+            st_async_b32x4(dst + q * kRows * 16, r[q / 8][(4 * q) & 31],
+                           r[q / 8][(4 * q + 1) & 31], r[q / 8][(4 * q + 2) & 31],
+                           r[q / 8][(4 * q + 3) & 31], x_in_p);
+        }
+        if (xt == 0) PA_TRACE_TILE(k, 9);
+        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in[xb]),
+                                                      (k / kXBufs) & 1, abort, P.err_flags));
+        if (!ok) break;
+        if (xt == 0) PA_TRACE_TILE(k, 12);
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(x_s) + xrow * 16 + xb * kXTile;
+#pragma unroll
+        for (int q = 0; q < kChunks; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + q * kRows * 16);
+          if (kHalfX) {
+            // S = (own + peer) / xscale: the same two rounded values in both
+            // CTAs, so both hold bit-identical S (the scaling is exact)
+            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c0 = 8 * q + 2 * e;
+              uint32_t* d = &r[c0 / 32][c0 & 31];
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+              d[0] = __float_as_uint((__uint_as_float(d[0]) + f.x) * xu);
+              d[1] = __float_as_uint((__uint_as_float(d[1]) + f.y) * xu);
+            }
+          } else {
+            uint32_t* d = &r[q / 8][(4 * q) & 31];
+            const float pv[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
+                                 __uint_as_float(v.w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float mine = __uint_as_float(d[e]);
+              d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+            }
+          }
+        }
+        named_sync(3, 128);  // every row of buffer xb has been read
         if (xt == 0) {
-          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in), C::kXBytes);
-          arrive_peer_relaxed(x_out_peer);
+          if (k + kXBufs < n) mbar_expect_tx(smem_u32(&bars->x_in[xb]), kXTile);
+          arrive_peer_relaxed(xb ? x_out_peer1 : x_out_peer0);
         }
 #pragma unroll
         for (int c = 0; c < N / 32; ++c) tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
