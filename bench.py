@@ -54,8 +54,8 @@ UNIT = "TB/s"
 # the roofline reports null traffic until a new capture replaces it.
 KERNEL_SOURCES = ("pa_tc.cu", "pa_tc_common.cuh", "pa_tc_pair.cu")
 NCU_TRAFFIC = {
-    "glm_decode": ("tc_attn_kernel", 54393600, "a7455db383b1746a"),
-    "dsv3_decode": ("tc_pair_kernel", 315290880, "a7455db383b1746a"),
+    "glm_decode": ("tc_attn_kernel", 54376448, "e90789ef106cc122"),
+    "dsv3_decode": ("tc_pair_kernel", 314849024, "e90789ef106cc122"),
 }
 
 
