@@ -517,6 +517,15 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
                            P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
+        } else if (P.decode && k == 2 && nsub <= 2) {
+          // Decode: every CTA starts at once, and with few copies per tile
+          // their first stages would all be in flight together; the first
+          // tile then lands only behind most of that burst. The first two
+          // tiles go out now, the later stages once tile 0 has landed (GLM
+          // decode: 35.6 -> 33.7 us per step).
+          bool okw = true;
+          if (lane == 0) okw = wait_bar(smem_u32(&bars->full[0]), 0, abort, P.err_flags);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
         if (lane == 0 && k == 0) PA_TRACE(8);
         if (lane == 0 && k == n - 1) PA_TRACE(9);
