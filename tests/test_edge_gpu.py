@@ -57,6 +57,19 @@ def test_geometries(hs, vhs, ro, rd, H):
     _check(w)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("bs", [16, 64])
+def test_pair_kernel_exchange_formats(dtype, bs):
+    """The CTA-pair kernel (576/512 latent) with both partial-score exchange
+    formats (fp16 partials for bf16 inputs, f32 for fp16 inputs), one box
+    per key tile (64-row blocks) and four (16-row blocks), over decode and
+    prefill tokens with several key tiles and ragged tails."""
+    w = W.make_workload("pair", q_lens=[1, 1, 70, 1], past_lens=[300, 1, 200, 129],
+                        num_heads=128, **W.DSV3, block_size=bs, seed=31, dtype=dtype,
+                        drop_slots=1)
+    _check(w)
+
+
 def test_long_decode_splits():
     """Long contexts (many key splits merged by the combine step)."""
     w = W.make_workload("long", q_lens=[1, 1, 1], past_lens=[20000, 3, 777], num_heads=16,
