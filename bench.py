@@ -358,8 +358,10 @@ def run_gpu_arm(args, rank, world, device):
             gpu_index = int(vis.split(",")[device.index])
         except ValueError:
             pass
-    os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-    sampler = ClockSampler(gpu_index, os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv"))
+    # the raw clock samples of the timed region (the JSON line carries their summary)
+    clock_dir = os.environ.get("PA_BENCH_CLOCK_DIR", os.path.join(ROOT, "bench_out"))
+    os.makedirs(clock_dir, exist_ok=True)
+    sampler = ClockSampler(gpu_index, os.path.join(clock_dir, f"clocks_r{rank}.csv"))
     time.sleep(0.3)
     barrier(device)
     torch.cuda.synchronize(device)
