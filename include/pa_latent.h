@@ -159,9 +159,9 @@ pa_status pa_latent_write(const pa_latent_params* p, const void* key, int64_t nu
  * softcap*tanh(s_j/softcap) if softcap > 0; out[t, h*vhs:(h+1)*vhs] =
  * sum_j softmax(s)_j K_j[:vhs], rounded to the dtype.
  *
- * Arithmetic: both products accumulate in f32 on the tensor cores, the
- * softmax runs in f32 (base 2, lazily rescaled), and the probabilities
- * are rounded to the dtype for the product with V. With head_size 576 one
+ * Arithmetic (default kernels): both products accumulate in f32 on the
+ * tensor cores, the softmax runs in f32 (base 2, lazily rescaled), and the
+ * probabilities are rounded to the dtype for the product with V. With head_size 576 one
  * token is handled by two SMs that each hold half of the latent channels;
  * with bf16 inputs the two halves' partial scores are exchanged as fp16
  * (each partial logit rounded by at most 2^-11 of its magnitude).
