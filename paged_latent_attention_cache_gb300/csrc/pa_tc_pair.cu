@@ -549,17 +549,25 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             }
           }
         }
-        named_sync(3, 128);  // every row of buffer xb has been read
-        if (xt == 0) {
-          if (k + kXBufs < n) mbar_expect_tx(smem_u32(&bars->x_in[xb]), kXTile);
-          arrive_peer_relaxed(xb ? x_out_peer1 : x_out_peer0);
-        }
+        // Buffer xb is released to the peer once every row of it has been
+        // read. With one buffer the peer's next tile waits for that, so it
+        // goes first; with two the peer sends into the other buffer meanwhile,
+        // and the sum goes to the softmax warps first.
+        auto release = [&]() {
+          named_sync(3, 128);
+          if (xt == 0) {
+            if (k + kXBufs < n) mbar_expect_tx(smem_u32(&bars->x_in[xb]), kXTile);
+            arrive_peer_relaxed(xb ? x_out_peer1 : x_out_peer0);
+          }
+        };
+        if (kXBufs == 1) release();
 #pragma unroll
         for (int c = 0; c < N / 32; ++c) tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->s_sum[sb]));
         if (xt == 0) PA_TRACE_TILE(k, 11);
+        if (kXBufs == 2) release();
       }
     } else if (warp == 4) {
       // =================== TMA producer ===================
