@@ -43,14 +43,6 @@ __device__ __forceinline__ void st_async_b32x4(uint32_t raddr, uint32_t a, uint3
       ::"r"(raddr), "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
       : "memory");
 }
-// Remote 16-byte store whose arrival completes tx bytes on the peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
-                                            uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(raddr), "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
-      : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
