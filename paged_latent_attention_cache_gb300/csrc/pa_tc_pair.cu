@@ -68,6 +68,7 @@ struct PairBarriers {
   uint32_t tmem_base;
   int bad;
   int abort;
+  int xfail;  // an exchange warp's wait failed: all four leave after the tile's barrier
 };
 
 template <typename T, int N, int STAGES>
@@ -191,6 +192,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     mbar_init(smem_u32(&bars->drain), 1);
     bars->bad = 0;
     bars->abort = 0;
+    bars->xfail = 0;
     fence_barrier_init();
   } else if (warp == 4 && lane == 0) {
     prefetch_tmap(&kmap);
@@ -468,106 +470,125 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const uint32_t x_out_peer0 = map_peer(smem_u32(&bars->x_out[0]), peer);
       const uint32_t x_out_peer1 = map_peer(smem_u32(&bars->x_out[1]), peer);
       const float xs = P.xscale, xu = P.xunscale;
+      volatile int* xfail = &bars->xfail;
       bool ok = true;
-      for (int k = 0; k < n && ok; ++k) {
+      for (int k = 0; k < n; ++k) {
         const int sb = k % NS;
         const int xb = kXBufs == 2 ? (k & 1) : 0;  // exchange buffer of tile k
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
                                               P.err_flags));
-        if (!ok) break;
-        if (xt == 0) PA_TRACE_TILE(k, 8);
-        tc_fence_after();
         uint32_t r[N / 32][32];
-#pragma unroll
-        for (int c = 0; c < N / 32; ++c)
-          tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
-        tmem_wait_ld();
-#pragma unroll
-        for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
-        // 16-bit format: round this CTA's partial the way the peer will see
-        // it, and keep the rounded values (in xscale units) for the sum
+        // 16-bit format: this CTA's partial rounded the way the peer will see
+        // it (the rounded values, in xscale units, are kept in r for the sum)
         uint32_t hx[kHalfX ? N / 2 : 1];
-        if (kHalfX) {
+        if (ok) {
+          if (xt == 0) PA_TRACE_TILE(k, 8);
+          tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < N / 2; ++j) {
-            const int c0 = 2 * j;
-            uint32_t* d = &r[c0 / 32][c0 & 31];
-            __half2 h = __floats2half2_rn(__uint_as_float(d[0]) * xs, __uint_as_float(d[1]) * xs);
-            hx[j] = *reinterpret_cast<uint32_t*>(&h);
-            const float2 f = __half22float2(h);
-            d[0] = __float_as_uint(f.x);
-            d[1] = __float_as_uint(f.y);
-          }
-        }
-        if (k >= kXBufs) {  // the peer has read tile k - kXBufs from buffer xb
-          ok = __all_sync(0xffffffffu,
-                          wait_bar_cluster(smem_u32(&bars->x_out[xb]), ((k - kXBufs) / kXBufs) & 1,
-                                           abort, P.err_flags));
-          if (!ok) break;
-        }
-        const uint32_t dst = x_peer + xb * kXTile;
-        const uint32_t x_in_p = xb ? x_in_peer1 : x_in_peer0;
+          for (int c = 0; c < N / 32; ++c)
+            tmem_ld32_nowait(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+          tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < kChunks; ++q) {
-          if (kHalfX)
-            st_async_b32x4(dst + q * kRows * 16, hx[4 * q], hx[4 * q + 1], hx[4 * q + 2],
-                           hx[4 * q + 3], x_in_p);
-          else
-            st_async_b32x4(dst + q * kRows * 16, r[q / 8][(4 * q) & 31],
-                           r[q / 8][(4 * q + 1) & 31], r[q / 8][(4 * q + 2) & 31],
-                           r[q / 8][(4 * q + 3) & 31], x_in_p);
-        }
-        if (xt == 0) PA_TRACE_TILE(k, 9);
-        ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in[xb]),
-                                                      (k / kXBufs) & 1, abort, P.err_flags));
-        if (!ok) break;
-        if (xt == 0) PA_TRACE_TILE(k, 12);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(x_s) + xrow * 16 + xb * kXTile;
-#pragma unroll
-        for (int q = 0; q < kChunks; ++q) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + q * kRows * 16);
+          for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
           if (kHalfX) {
-            // S = (own + peer) / xscale: the same two rounded values in both
-            // CTAs, so both hold bit-identical S (the scaling is exact)
-            const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c0 = 8 * q + 2 * e;
+            for (int j = 0; j < N / 2; ++j) {
+              const int c0 = 2 * j;
               uint32_t* d = &r[c0 / 32][c0 & 31];
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-              d[0] = __float_as_uint((__uint_as_float(d[0]) + f.x) * xu);
-              d[1] = __float_as_uint((__uint_as_float(d[1]) + f.y) * xu);
-            }
-          } else {
-            uint32_t* d = &r[q / 8][(4 * q) & 31];
-            const float pv[4] = {__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z),
-                                 __uint_as_float(v.w)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float mine = __uint_as_float(d[e]);
-              d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+              __half2 h =
+                  __floats2half2_rn(__uint_as_float(d[0]) * xs, __uint_as_float(d[1]) * xs);
+              hx[j] = *reinterpret_cast<uint32_t*>(&h);
+              const float2 f = __half22float2(h);
+              d[0] = __float_as_uint(f.x);
+              d[1] = __float_as_uint(f.y);
             }
           }
+          if (k >= kXBufs)  // the peer has read tile k - kXBufs from buffer xb
+            ok = __all_sync(0xffffffffu,
+                            wait_bar_cluster(smem_u32(&bars->x_out[xb]),
+                                             ((k - kXBufs) / kXBufs) & 1, abort, P.err_flags));
+        }
+        if (ok) {
+          const uint32_t dst = x_peer + xb * kXTile;
+          const uint32_t x_in_p = xb ? x_in_peer1 : x_in_peer0;
+#pragma unroll
+          for (int q = 0; q < kChunks; ++q) {
+            if (kHalfX)
+              st_async_b32x4(dst + q * kRows * 16, hx[4 * q], hx[4 * q + 1], hx[4 * q + 2],
+                             hx[4 * q + 3], x_in_p);
+            else
+              st_async_b32x4(dst + q * kRows * 16, r[q / 8][(4 * q) & 31],
+                             r[q / 8][(4 * q + 1) & 31], r[q / 8][(4 * q + 2) & 31],
+                             r[q / 8][(4 * q + 3) & 31], x_in_p);
+          }
+          if (xt == 0) PA_TRACE_TILE(k, 9);
+          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in[xb]),
+                                                        (k / kXBufs) & 1, abort, P.err_flags));
+        }
+        if (ok) {
+          if (xt == 0) PA_TRACE_TILE(k, 12);
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(x_s) + xrow * 16 + xb * kXTile;
+#pragma unroll
+          for (int q = 0; q < kChunks; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + q * kRows * 16);
+            if (kHalfX) {
+              // S = (own + peer) / xscale: the same two rounded values in both
+              // CTAs, so both hold bit-identical S (the scaling is exact)
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int c0 = 8 * q + 2 * e;
+                uint32_t* d = &r[c0 / 32][c0 & 31];
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
+                d[0] = __float_as_uint((__uint_as_float(d[0]) + f.x) * xu);
+                d[1] = __float_as_uint((__uint_as_float(d[1]) + f.y) * xu);
+              }
+            } else {
+              uint32_t* d = &r[q / 8][(4 * q) & 31];
+              const float pv[4] = {__uint_as_float(v.x), __uint_as_float(v.y),
+                                   __uint_as_float(v.z), __uint_as_float(v.w)};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float mine = __uint_as_float(d[e]);
+                d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
+              }
+            }
+          }
+        } else if (lane == 0) {
+          *xfail = 1;
         }
         // Buffer xb is released to the peer once every row of it has been
-        // read. With one buffer the peer's next tile waits for that, so it
-        // goes first; with two the peer sends into the other buffer meanwhile,
-        // and the sum goes to the softmax warps first.
+        // read (the named barrier). With one buffer the peer's next tile
+        // waits for that, so it goes first; with two the peer sends into the
+        // other buffer meanwhile, and the sum goes to the softmax warps
+        // first. All four exchange warps pass every tile's barrier, a failed
+        // tile's included, and leave the loop together after it.
+        bool leave = false;
         auto release = [&]() {
           named_sync(3, 128);
-          if (xt == 0) {
+          leave = *xfail != 0;
+          if (!leave && xt == 0) {
             if (k + kXBufs < n) mbar_expect_tx(smem_u32(&bars->x_in[xb]), kXTile);
             arrive_peer_relaxed(xb ? x_out_peer1 : x_out_peer0);
           }
         };
-        if (kXBufs == 1) release();
+        if (kXBufs == 1) {
+          release();
+          if (leave) break;
+        }
+        if (ok) {
 #pragma unroll
-        for (int c = 0; c < N / 32; ++c) tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(smem_u32(&bars->s_sum[sb]));
-        if (xt == 0) PA_TRACE_TILE(k, 11);
-        if (kXBufs == 2) release();
+          for (int c = 0; c < N / 32; ++c)
+            tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+          tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(smem_u32(&bars->s_sum[sb]));
+          if (xt == 0) PA_TRACE_TILE(k, 11);
+        }
+        if (kXBufs == 2) {
+          release();
+          if (leave) break;
+        }
       }
     } else if (warp == 4) {
       // =================== TMA producer ===================
