@@ -54,8 +54,8 @@ UNIT = "TB/s"
 # the roofline reports null traffic until a new capture replaces it.
 KERNEL_SOURCES = ("pa_tc.cu", "pa_tc_common.cuh", "pa_tc_pair.cu")
 NCU_TRAFFIC = {
-    "glm_decode": ("tc_attn_kernel", 54255872, "9d33df9a413dc857"),
-    "dsv3_decode": ("tc_pair_kernel", 314825216, "9d33df9a413dc857"),
+    "glm_decode": ("tc_attn_kernel", 54255872, "e0f1913c268e7a95"),
+    "dsv3_decode": ("tc_pair_kernel", 314825216, "e0f1913c268e7a95"),
 }
 
 

@@ -13,11 +13,12 @@
 // and the key tile staged once in shared memory is the B operand of both
 // (K-major for QK^T; its leading value channels read MN-major for PV).
 //
-// CTA = one query token x one group of value channels (2 groups of 256 when
-// vhs = 512: a 128 x 512 f32 accumulator alone fills the 512 TMEM columns, so
-// the two groups live on two SMs and each recomputes S), optionally one
-// split of the token's keys (decode: splits are merged by a log-sum-exp
-// combine kernel). Warp roles:
+// CTA = one work unit: one query token (prefill with H <= 64: 128/H
+// consecutive tokens of one sequence, every row with its own position), or
+// in decode one split of a token's keys (splits are merged by a log-sum-exp
+// combine kernel). The value channels may be cut into G groups on separate
+// CTAs; the 576/512 geometry instead runs on a CTA pair (pa_tc_pair.cu).
+// Warp roles:
 //   warps 0-3  softmax + epilogue; thread i owns row i (TMEM lane i): loads Q
 //              with RoPE into swizzled shared memory, reads S from TMEM,
 //              masks/softcaps, runs the online softmax with lazy rescaling
@@ -29,7 +30,8 @@
 //   (With 64 query rows the producer and MMA warps are 6 and 7, on other
 //   scheduler partitions than the two softmax warps that hold rows.)
 // Pipelines: K tiles in a STAGES-deep ring (full/empty mbarriers), S and P
-// double-buffered in TMEM. Every mbarrier wait is bounded: on expiry the
+// in NB TMEM buffers (two, or one where two CTAs share an SM). Every
+// mbarrier wait is bounded: on expiry the
 // CTA sets PA_DEVERR_TIMEOUT in the error word, drains what it issued and
 // exits without trapping.
 #include <cfloat>
