@@ -37,7 +37,11 @@ numpy casts, RoPE against complex multiplication and the relative-position
 identity, the attention against a naive contiguous dense attention, against
 decomposed multi-head latent attention, placement invariance under a
 permuted block table, untouched cache rows for slot -1, and closed-form
-special cases.
+special cases. ``error_scales`` (a tolerance helper for the parity tests,
+not part of the operator) is pinned by its closed forms on one key and on
+equal probabilities, by a Monte Carlo run of independently perturbed
+probabilities and scores, and by a finite-difference derivative in one
+query channel.
 """
 from __future__ import annotations
 
@@ -244,7 +248,7 @@ def cache_row_index(b: int, j: int, block_table: np.ndarray, block_size: int,
 
 def latent_attend_token(t: int, q_row: np.ndarray, cache, cos_tab: np.ndarray,
                         sin_tab: np.ndarray, cumseq: np.ndarray, past: np.ndarray,
-                        block_table: np.ndarray, p: dict) -> np.ndarray:
+                        block_table: np.ndarray, p: dict, stats: bool = False):
     """Read phase for token t, all heads: returns float64 ``[H, vhs]``.
     ``q_row`` is the token's float64 query row ``[H*hs]``.
 
@@ -252,7 +256,11 @@ def latent_attend_token(t: int, q_row: np.ndarray, cache, cos_tab: np.ndarray,
     visible key j, s_hj = scale * q_h . K_j, then
     s_hj = softcap * tanh(s_hj / softcap) when softcap > 0, a two-pass
     softmax over j, and out_h = sum_j p_hj K_j[:vhs] / sum_j p_hj; zero
-    when no key is visible."""
+    when no key is visible.
+
+    With ``stats=True`` it returns ``(out, scales)``, ``scales`` being the
+    ``error_scales`` of this token (a test-tolerance helper; the operator's
+    result is ``out`` alone)."""
     hs, vhs = _check_geometry(p)
     H = p["num_heads"]
     bs = p["block_size"]
@@ -263,7 +271,8 @@ def latent_attend_token(t: int, q_row: np.ndarray, cache, cos_tab: np.ndarray,
                            bool(p["rotary_interleaved"])) for h in range(H)])
     keys = list(visible_keys(pos, p["local_window_size"]))
     if not keys:
-        return np.zeros((H, vhs))
+        zero = np.zeros((H, vhs))
+        return (zero, np.zeros((3, H, vhs))) if stats else zero
     rows = [cache_row_index(b, j, block_table, bs, num_blocks) for j in keys]
     K = cache.get(rows)                               # [n, hs]
     s = (q @ K.T) * p["scale"]                        # [H, n]
@@ -272,18 +281,60 @@ def latent_attend_token(t: int, q_row: np.ndarray, cache, cos_tab: np.ndarray,
     m = s.max(axis=1, keepdims=True)
     w = np.exp(s - m)
     den = w.sum(axis=1, keepdims=True)
-    return (w @ K[:, :vhs]) / den
+    out = (w @ K[:, :vhs]) / den
+    if not stats:
+        return out
+    return out, error_scales(q, K, w / den, out, p["scale"], vhs)
+
+
+def error_scales(q: np.ndarray, K: np.ndarray, prob: np.ndarray, out: np.ndarray,
+                 scale: float, vhs: int) -> np.ndarray:
+    """How strongly one token's attention output reacts to rounding inside
+    a kernel, per output element. TEST-TOLERANCE HELPER: the operator does
+    not compute this; the parity tests scale their per-element bound by it.
+
+    ``q`` [H, hs] rotated queries, ``K`` [n, hs] visible key rows (V_j =
+    K_j[:vhs]), ``prob`` [H, n] the softmax probabilities, ``out`` [H, vhs].
+    Returns float64 ``[3, H, vhs]``:
+
+    * ``[0]`` n_p = sqrt(sum_j p_j^2 V_jc^2): the standard deviation of the
+      output when every probability is multiplied by an independent
+      (1 + e_j), per unit standard deviation of e_j (rounding P to 16 bits
+      before the product with V).
+    * ``[1]`` n_q = sqrt(sum_j p_j^2 g_j^2 (V_jc - out_c)^2) with
+      g_j = scale * sqrt(sum_d q_d^2 K_jd^2): the same for independent score
+      perturbations of standard deviation g_j per unit (rounding the query
+      operand to 16 bits perturbs score j by about that much, first order:
+      d out_c / d s_j = p_j (V_jc - out_c)).
+    * ``[2]`` n_d = scale * |q_c| * sum_j p_j (V_jc - out_c)^2: the size of
+      d out_c / d log q_c, which is coherent over the keys because query
+      channel c multiplies value channel c (K_jc = V_jc) in every score.
+    """
+    V = K[:, :vhs]
+    V2 = V * V
+    n_p = np.sqrt(np.maximum((prob * prob) @ V2, 0.0))
+    g2 = (scale * scale) * ((q * q) @ (K * K).T)                 # [H, n]
+    a = prob * prob * g2
+    var_a = (a @ V2) - 2.0 * out * (a @ V) + out * out * a.sum(axis=1, keepdims=True)
+    n_q = np.sqrt(np.maximum(var_a, 0.0))
+    var_p = (prob @ V2) - out * out
+    n_d = scale * np.abs(q[:, :vhs]) * np.maximum(var_p, 0.0)
+    return np.stack([n_p, n_q, n_d])
 
 
 def latent_attend(query, cache, cos_tab, sin_tab, cumseq, past, block_table, p,
-                  tokens=None) -> np.ndarray:
+                  tokens=None, stats: bool = False):
     """Read phase for the listed tokens (default: all). ``query`` maps a
     token index to its float64 row (an array ``[T, H*hs]`` or a callable).
-    Returns float64 ``[len(tokens), H, vhs]``."""
+    Returns float64 ``[len(tokens), H, vhs]`` (with ``stats``: and the
+    ``error_scales`` stacked as ``[len(tokens), 3, H, vhs]``)."""
     get_q = query if callable(query) else (lambda t: query[t])
     tokens = range(int(cumseq[-1])) if tokens is None else tokens
-    return np.stack([latent_attend_token(int(t), get_q(int(t)), cache, cos_tab, sin_tab,
-                                         cumseq, past, block_table, p) for t in tokens])
+    res = [latent_attend_token(int(t), get_q(int(t)), cache, cos_tab, sin_tab,
+                               cumseq, past, block_table, p, stats) for t in tokens]
+    if not stats:
+        return np.stack(res)
+    return np.stack([r[0] for r in res]), np.stack([r[1] for r in res])
 
 
 # ---------------------------------------------------------------------------
@@ -291,14 +342,15 @@ def latent_attend(query, cache, cos_tab, sin_tab, cumseq, past, block_table, p,
 # ---------------------------------------------------------------------------
 
 def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cumseq, past,
-                      block_table, slot_mapping, p: dict, tokens=None):
+                      block_table, slot_mapping, p: dict, tokens=None, stats: bool = False):
     """Write then read, on uint16 bit arrays of the operator dtype.
 
     Shapes: query ``[T, H*hs]``, key ``[T, hs]``, cache
     ``[num_blocks, bs, 1, hs]`` (any shape with hs last), cos/sin
     ``[rows, rd/2]``. The read phase sees the cache after the write.
     Returns (new cache bits in the input's shape, output bits
-    ``[len(tokens), H*vhs]``, output float64 before rounding)."""
+    ``[len(tokens), H*vhs]``, output float64 before rounding); with
+    ``stats`` a fourth item, the ``error_scales`` ``[len(tokens), 3, H*vhs]``."""
     dt = p["dtype"]
     hs, _ = _check_geometry(p)
     shape = cache_bits.shape
@@ -307,7 +359,11 @@ def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cums
     sin_tab = bits_to_f64(sin_bits, dt)
     latent_write(lambda t: bits_to_f64(key_bits[t], dt), cos_tab, sin_tab,
                  np.asarray(slot_mapping), cumseq, past, cache, p)
-    out = latent_attend(lambda t: bits_to_f64(query_bits[t], dt), cache, cos_tab, sin_tab,
-                        cumseq, past, block_table, p, tokens)
+    res = latent_attend(lambda t: bits_to_f64(query_bits[t], dt), cache, cos_tab, sin_tab,
+                        cumseq, past, block_table, p, tokens, stats)
+    out = res[0] if stats else res
     out = out.reshape(out.shape[0], -1)
-    return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out
+    if not stats:
+        return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out
+    sc = res[1].reshape(out.shape[0], 3, -1)
+    return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out, sc

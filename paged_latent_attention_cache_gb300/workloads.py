@@ -130,14 +130,16 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
                   max_blocks_per_seq: Optional[int] = None,
                   cos_rows: Optional[int] = None, scale: Optional[float] = None,
                   softcap: float = 0.0, local_window_size: int = -1,
-                  seed: int = 0, std: float = 0.5,
+                  seed: int = 0, std: float = 0.5, query_gain: float = 1.0,
                   drop_slots: int = 0, drop_frac: float = 0.0,
                   num_decode_seqs: Optional[int] = None,
                   block_table_shape: Optional[Sequence[int]] = None) -> Workload:
     """Draw one seeded batch.
 
     ``drop_slots`` / ``drop_frac`` set that many (or that fraction of) seeded
-    slot_mapping entries to -1. ``block_table_shape`` lets a caller ask for a
+    slot_mapping entries to -1. ``query_gain`` multiplies the drawn query
+    (a power of two keeps the scaling exact) so that the logits spread over
+    tens or hundreds and the softmax is peaked instead of near-uniform. ``block_table_shape`` lets a caller ask for a
     block table that is literally a permutation of the whole pool reshaped
     (the tiny configuration's wording)."""
     assert len(q_lens) == len(past_lens)
@@ -190,6 +192,8 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
         slot[idx] = -1
 
     query = _normal((T, num_heads * head_size), gen, std, dtype)
+    if query_gain != 1.0:
+        query = (query.float() * query_gain).to(dtype)
     key = _normal((T, head_size), gen, std, dtype)
     key_cache = _normal((num_blocks, block_size, 1, head_size), gen, std, dtype)
     cos, sin = rope_tables(cos_rows, rotary_dim, dtype)
@@ -210,7 +214,7 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
                     num_decode_seqs=int(num_decode_seqs), query=query, key=key,
                     key_cache=key_cache, cos_cache=cos, sin_cache=sin, cumseq=cumseq,
                     past=past, block_table=block_table, slot_mapping=slot,
-                    meta=dict(seed=seed, std=std))
+                    meta=dict(seed=seed, std=std, query_gain=query_gain))
 
 
 # ---------------------------------------------------------------------------
@@ -291,6 +295,17 @@ def mixed_serving(seed: int = 5, n_decode: int = 48, n_prefill: int = 4,
                          cos_rows=32768, scale=1.0 / math.sqrt(192.0), softcap=50.0,
                          local_window_size=4096, seed=seed, drop_frac=0.05,
                          num_decode_seqs=n_decode)
+
+
+def peaked(w: Workload, gain: float) -> Workload:
+    """A copy of ``w`` whose query is multiplied by ``gain`` (exact for a
+    power of two in range): the logits spread over tens to thousands of
+    units, so the softmax is peaked rather than near-uniform."""
+    out = Workload(**{k: getattr(w, k) for k in w.__dataclass_fields__})
+    out.query = (w.query.float() * gain).to(w.dtype)
+    out.name = f"{w.name}_q{gain:g}"
+    out.meta = dict(w.meta, query_gain=gain)
+    return out
 
 
 WORKLOADS = {

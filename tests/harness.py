@@ -2,8 +2,21 @@
 the oracle on the same seeded inputs, and compare.
 
 Tolerances: cache rows written through RoPE within 1 ulp of the dtype
-(non-rotary channels and untouched rows bit-exact); attention outputs within
-max-abs 2e-3 (fp16) / 1.5e-2 (bf16) of the oracle's float64 result.
+(non-rotary channels and untouched rows bit-exact). Attention outputs meet
+two bounds against the oracle's float64 result:
+
+* the fixed bound max |err| <= 2e-3 (fp16) / 1.5e-2 (bf16);
+* per element, |err| <= K_REL * u * (|ref| + n_p + n_q + n_d), u the unit
+  roundoff of the dtype (2^-8 bf16, 2^-11 fp16) and n_* the oracle's
+  ``error_scales``: the output's sensitivity to rounding the probabilities
+  and the query operand to 16 bits, the two roundings a tensor-core kernel
+  adds to the operator's arithmetic, plus the rounding of the output itself.
+  With independent roundings of at most u the error's standard deviation is
+  about u / sqrt(3) times the sum of the scales; K_REL = 6 leaves room for the
+  largest of some 10^7 elements (about 5.5 standard deviations). Unlike the
+  fixed bound it scales with the output, so it rejects a 1.2x softmax scale
+  or a missing query rotation on the full-size decode batches, whose
+  near-uniform softmax makes every output small.
 """
 from __future__ import annotations
 
@@ -16,6 +29,8 @@ from oracle import pa_oracle as O
 from paged_latent_attention_cache_gb300 import workloads as W
 
 TOL = {torch.float16: 2e-3, torch.bfloat16: 1.5e-2}
+UNIT_ROUNDOFF = {torch.float16: 2.0 ** -11, torch.bfloat16: 2.0 ** -8}
+K_REL = 6.0
 
 
 def run_gpu(w: W.Workload, portable=False, device="cuda", scale=None):
@@ -37,11 +52,11 @@ def run_gpu(w: W.Workload, portable=False, device="cuda", scale=None):
 
 def run_oracle(w: W.Workload, tokens=None):
     p = W.oracle_params(w)
-    cache, out_bits, out = O.run_operator_bits(
+    cache, out_bits, out, scales = O.run_operator_bits(
         W.to_bits(w.query), W.to_bits(w.key), W.to_bits(w.key_cache), W.to_bits(w.cos_cache),
         W.to_bits(w.sin_cache), w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy(),
-        w.slot_mapping.numpy(), p, tokens)
-    return dict(cache=cache, out_bits=out_bits, out=out)
+        w.slot_mapping.numpy(), p, tokens, stats=True)
+    return dict(cache=cache, out_bits=out_bits, out=out, scales=scales)
 
 
 @functools.lru_cache(maxsize=8)
@@ -79,7 +94,18 @@ def check_cache(w: W.Workload, got: np.ndarray, ref: np.ndarray):
     return int((d > 0).sum())
 
 
-def check_out(w: W.Workload, got_bits: np.ndarray, ref_f64: np.ndarray, tokens=None):
+def output_bound(dtype, ref_f64: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Per-element bound K_REL * u * (|ref| + n_p + n_q + n_d) (see above);
+    ``scales`` is the oracle's ``[tokens, 3, H*vhs]`` array."""
+    ref = ref_f64.reshape(scales.shape[0], -1)
+    return K_REL * UNIT_ROUNDOFF[dtype] * (np.abs(ref) + scales.sum(axis=1))
+
+
+def check_out(w: W.Workload, got_bits: np.ndarray, ref_f64: np.ndarray, tokens=None,
+              scales=None):
+    """Both bounds of the module docstring (the scale-aware one when the
+    oracle's ``scales`` are given). Returns (max abs error, largest ratio of
+    an element's error to its scale-aware bound, or None)."""
     dt = W.dtype_tag(w.dtype)
     g = got_bits if tokens is None else got_bits[np.asarray(tokens)]
     gf = O.bits_to_f64(g, dt)
@@ -87,7 +113,18 @@ def check_out(w: W.Workload, got_bits: np.ndarray, ref_f64: np.ndarray, tokens=N
     err = np.abs(gf - ref_f64.reshape(gf.shape))
     tol = TOL[w.dtype]
     assert err.max() <= tol, f"max abs error {err.max():.3e} > {tol}"
-    return float(err.max())
+    ratio = None
+    if scales is not None:
+        bound = output_bound(w.dtype, ref_f64, scales).reshape(err.shape)
+        over = err > bound
+        ratio = float(np.max(err / np.maximum(bound, 1e-300)))
+        if over.any():
+            i = np.unravel_index(np.argmax(err / np.maximum(bound, 1e-300)), err.shape)
+            raise AssertionError(
+                f"{int(over.sum())} of {err.size} outputs exceed the scale-aware bound; worst "
+                f"at {tuple(int(x) for x in i)}: |err| {err[i]:.3e} > {bound[i]:.3e} "
+                f"(ratio {ratio:.2f})")
+    return float(err.max()), ratio
 
 
 def sample_tokens(w: W.Workload, per_seq: int = 24, seed: int = 0):

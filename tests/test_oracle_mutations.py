@@ -29,7 +29,12 @@ MUTANTS = {
                            "r = np.trunc(x / spacing) * spacing"),
     "slot_minus_one_written": ("if slot < 0:\n            continue",
                                "if slot < -1:\n            continue"),
-    "softmax_not_normalised": ("return (w @ K[:, :vhs]) / den", "return (w @ K[:, :vhs])"),
+    "softmax_not_normalised": ("out = (w @ K[:, :vhs]) / den", "out = (w @ K[:, :vhs])"),
+    "scales_prob_not_squared": ("n_p = np.sqrt(np.maximum((prob * prob) @ V2, 0.0))",
+                                "n_p = np.sqrt(np.maximum(prob @ V2, 0.0))"),
+    "scales_score_centre_dropped": ("var_a = (a @ V2) - 2.0 * out * (a @ V)",
+                                    "var_a = (a @ V2) - 0.0 * out * (a @ V)"),
+    "scales_diag_wrong_channel": ("np.abs(q[:, :vhs])", "np.abs(q[:, -vhs:])"),
 }
 
 PINS = [
@@ -44,6 +49,11 @@ PINS = [
     lambda: pins.test_absorbed_equals_decomposed_mla(128, 32, 32, 64, 3),
     lambda: pins.test_slot_minus_one_leaves_cache_untouched(),
     lambda: pins.test_two_key_softcap_closed_form(),
+    lambda: pins.test_error_scales_single_key(),
+    lambda: pins.test_error_scales_equal_probabilities(),
+    lambda: pins.test_error_scales_probability_term_monte_carlo(),
+    lambda: pins.test_error_scales_score_term_monte_carlo(),
+    lambda: pins.test_error_scales_diagonal_term_is_a_derivative(),
 ]
 
 

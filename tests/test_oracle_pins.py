@@ -474,3 +474,109 @@ def test_two_key_softcap_closed_form():
     assert abs(out[0] - (w0 * 1 + w1 * 3)) < 1e-14
     assert abs(out[1] - (w0 * 1 - w1 * 1)) < 1e-14
     assert np.all(out[2:] == 0)
+
+
+# ---------------------------------------------------------------------------
+# error_scales: the tolerance helper of the parity tests (not the operator)
+# ---------------------------------------------------------------------------
+
+def _textbook_attention(q, K, scale, vhs, s_extra=None):
+    """softmax(scale * q K^T (+ s_extra)) @ K[:, :vhs], normalised; written
+    from the definition, independent of the oracle."""
+    s = scale * (q @ K.T)
+    if s_extra is not None:
+        s = s + s_extra
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    return (w @ K[:, :vhs]) / w.sum(axis=1, keepdims=True), w / w.sum(axis=1, keepdims=True)
+
+
+def _scales_case(seed=0, H=3, n=40, hs=32, vhs=16, scale=0.3):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((H, hs))
+    K = rng.standard_normal((n, hs))
+    out, prob = _textbook_attention(q, K, scale, vhs)
+    return q, K, prob, out, scale, vhs
+
+
+def test_error_scales_single_key():
+    """One key: the output is that key's value row; only the probability
+    term is left, equal to |V|."""
+    rng = np.random.default_rng(3)
+    q, K = rng.standard_normal((2, 24)), rng.standard_normal((1, 24))
+    prob = np.ones((2, 1))
+    out = np.repeat(K[:, :8], 2, axis=0)
+    sc = O.error_scales(q, K, prob, out, 0.4, 8)
+    assert np.allclose(sc[0], np.abs(out), rtol=0, atol=1e-15)
+    # (the square roots of cancelling sums: zero to about sqrt(eps))
+    assert np.allclose(sc[1], 0.0, atol=1e-6) and np.allclose(sc[2], 0.0, atol=1e-12)
+
+
+def test_error_scales_equal_probabilities():
+    """q = 0 gives equal probabilities 1/n; with |V_jc| = a the probability
+    term is a / sqrt(n), and nothing depends on the scores."""
+    rng = np.random.default_rng(4)
+    n, a = 50, 0.75
+    K = a * np.sign(rng.standard_normal((n, 16)))
+    q = np.zeros((2, 16))
+    out, prob = _textbook_attention(q, K, 0.5, 8)
+    sc = O.error_scales(q, K, prob, out, 0.5, 8)
+    assert np.allclose(sc[0], a / math.sqrt(n), rtol=1e-12)
+    assert np.allclose(sc[1], 0.0) and np.allclose(sc[2], 0.0)
+
+
+def test_error_scales_probability_term_monte_carlo():
+    """Multiplying each probability by an independent (1 + sigma e_j),
+    e ~ N(0, 1), moves the output by sigma * n_p in standard deviation."""
+    q, K, prob, out, scale, vhs = _scales_case(5)
+    sc = O.error_scales(q, K, prob, out, scale, vhs)
+    rng = np.random.default_rng(6)
+    trials, sigma = 4000, 1e-3
+    e = rng.standard_normal((trials,) + prob.shape)
+    d = np.einsum("thj,jc->thc", prob[None] * sigma * e, K[:, :vhs]) / sigma
+    assert np.allclose(d.std(axis=0), sc[0], rtol=0.06)
+
+
+def test_error_scales_score_term_monte_carlo():
+    """Perturbing score j by an independent sigma * g_j * e_j, with
+    g_j = scale * sqrt(sum_d q_d^2 K_jd^2), moves the softmax output by
+    sigma * n_q in standard deviation (first order)."""
+    q, K, prob, out, scale, vhs = _scales_case(7)
+    sc = O.error_scales(q, K, prob, out, scale, vhs)
+    g = scale * np.sqrt((q * q) @ (K * K).T)
+    rng = np.random.default_rng(8)
+    trials, sigma = 3000, 1e-5
+    d = np.stack([(_textbook_attention(q, K, scale, vhs,
+                                       sigma * g * rng.standard_normal(g.shape))[0] - out)
+                  / sigma for _ in range(trials)])
+    assert np.allclose(d.std(axis=0), sc[1], rtol=0.06)
+
+
+def test_error_scales_diagonal_term_is_a_derivative():
+    """Scaling query channel c by (1 + eps) moves output channel c by
+    eps * n_d (query channel c meets value channel c in every score)."""
+    q, K, prob, out, scale, vhs = _scales_case(9)
+    sc = O.error_scales(q, K, prob, out, scale, vhs)
+    eps = 1e-6
+    for h in range(q.shape[0]):
+        for c in range(vhs):
+            qp, qm = q.copy(), q.copy()
+            qp[h, c] *= 1 + eps
+            qm[h, c] *= 1 - eps
+            d = (_textbook_attention(qp, K, scale, vhs)[0][h, c] -
+                 _textbook_attention(qm, K, scale, vhs)[0][h, c]) / (2 * eps)
+            assert abs(abs(d) - sc[2, h, c]) <= 1e-6 * max(1.0, sc[2, h, c])
+
+
+def test_stats_leave_the_result_unchanged():
+    """The statistics variant returns the same output as the plain read."""
+    w = W.tiny()
+    p = W.oracle_params(w)
+    dt = p["dtype"]
+    cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, w.head_size), dt)
+    cos_t, sin_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt), O.bits_to_f64(W.to_bits(w.sin_cache), dt)
+    q = O.bits_to_f64(W.to_bits(w.query), dt)
+    args = (cache, cos_t, sin_t, w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy(), p)
+    plain = O.latent_attend(q, *args)
+    out, sc = O.latent_attend(q, *args, stats=True)
+    assert np.array_equal(plain, out)
+    assert sc.shape == (w.num_tokens, 3, w.num_heads, w.v_head_size) and (sc >= 0).all()
