@@ -162,9 +162,8 @@ pa_status pa_latent_write(const pa_latent_params* p, const void* key, int64_t nu
  * Arithmetic (default kernels): both products accumulate in f32 on the
  * tensor cores, the softmax runs in f32 (base 2, lazily rescaled), and the
  * probabilities are rounded to the dtype for the product with V. With head_size 576 one
- * token is handled by two SMs that each hold half of the latent channels;
- * with bf16 inputs the two halves' partial scores are exchanged as fp16
- * (each partial logit rounded by at most 2^-11 of its magnitude).
+ * token is handled by two SMs that each hold half of the latent channels
+ * and exchange their f32 partial scores, so the split adds no rounding.
  *
  * Every sequence in [seq_begin, seq_end) must have exactly one new token
  * (cumseq[b+1]-cumseq[b] == 1); a sequence that does not sets
@@ -212,8 +211,11 @@ pa_status pa_latent_prefill(const pa_latent_params* p, const void* query, int64_
  * Same arguments and results as pa_latent_decode, minus the workspace: the
  * split-KV partials go to a scratch array of 32 MiB in device global memory
  * that the library creates when it is loaded on a GPU and holds until the
- * process exits (on every GPU that loads it). A call whose
- * pa_latent_workspace_size exceeds 32 MiB returns PA_ERR_WORKSPACE. The call
+ * process exits (on every GPU that loads it). A call whose sequence range
+ * [seq_begin, seq_end) needs more than 32 MiB of workspace returns
+ * PA_ERR_WORKSPACE: on the tensor-core kernels that is more than 127
+ * sequences with head_size 576 / v_head_size 512, or more than 504 with
+ * 192 / 128 (a larger batch can be decoded in ranges of that size). The call
  * allocates nothing.
  *
  * The first call on each device looks up the scratch address on that device

@@ -89,7 +89,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const int g = blockIdx.x % G;            // value-channel group
   const int unit = blockIdx.x / G;
   const int vhs = P.vhs;
-  if (tid == 0) PA_TRACE(0);
 
   // ---- prologue: warp 0 resolves the work while warps 1/5 set up ----
   // With programmatic dependent launch this CTA may start while the previous
@@ -170,7 +169,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     if (lane == 0) work = w;
     fence_proxy_async();  // scratch stores before the query load reuses the region
-    if (lane == 0) PA_TRACE(12);
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&bars->full[s]), 1);
@@ -202,7 +200,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
   const Work W = work;
-  if (tid == 0) PA_TRACE(1);
 
   if (W.status == 0) {
     // The unit's rows are ntok consecutive tokens' heads (row r: token t +
@@ -276,7 +273,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           fence_proxy_async();
           mbar_arrive(smem_u32(&bars->q_full));
-          if (tid == 0) PA_TRACE(3);
           if (!ok) break;
         }
         const int sb = NB == 2 ? (k & 1) : 0;
@@ -287,8 +283,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           ok = __all_sync(0xffffffffu,
                           wait_bar(smem_u32(&bars->s_full[sb]), (k / NB) & 1, abort, P.err_flags));
           if (!ok) break;
-          if (tid == 0 && k == 0) PA_TRACE(4);
-          if (tid == 0) PA_TRACE_TILE(k, 0);
         }
         // The tile is handled in 32-column chunks read from TMEM twice (row
         // maximum of the raw scores, then probabilities), which keeps the
@@ -434,11 +428,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (dry) continue;
         mbar_arrive(smem_u32(&bars->s_free[sb]));
         mbar_arrive(smem_u32(&bars->p_full[sb]));
-        if (tid == 0) PA_TRACE_TILE(k, 1);
       }
 
       // ---- epilogue ----
-      if (tid == 0) PA_TRACE(5);
       grid_dep_launch();
       named_sync(2, 160);  // the producer has finished issuing (bad-block flag final)
       ok = __all_sync(0xffffffffu, ok && !*abort);
@@ -529,8 +521,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (lane == 0) okw = wait_bar(smem_u32(&bars->full[0]), 0, abort, P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
-        if (lane == 0 && k == 0) PA_TRACE(8);
-        if (lane == 0 && k == n - 1) PA_TRACE(9);
         // coordinates of the nsub boxes of rows (one cache block each)
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
         if (lane < nsub) {
@@ -546,7 +536,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
         if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
-        if (lane == 0) PA_TRACE_TILE(k, 5);
         __syncwarp();
         if (lane < nsub) {  // lane sb issues the boxes of rows sb (every slab)
           const uint32_t full = smem_u32(&bars->full[stage]);
@@ -590,7 +579,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
         if (ok) {
           tc_fence_after();
-          PA_TRACE(10);
           // Event loop: QK^T(k) needs its key tile (full) and a free S buffer
           // (s_free of k-NB); PV(k) needs P(k) (p_full). Issue whichever is
           // ready, QK^T first, so neither waits behind the other's inputs.
@@ -611,7 +599,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                                    kp > 0 ? 1u : 0u);
                 tc_commit(smem_u32(&bars->pv_done[sb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
-                PA_TRACE_TILE(kp, 3);
                 ++kp;
                 progressed = true;
               }
@@ -622,13 +609,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
                   (kq < NB ||
                    mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NB) / NB) & 1))) {
-                PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 issue_qk<HS, C::kQBox, C::kKBox, kIdQK>(
                     tmem + C::kColS + sb * N, sdesc(q_base, 16, 1024),
                     sdesc(k_base + stage * C::kStageBytes, 16, 1024));
                 tc_commit(smem_u32(&bars->s_full[sb]));
-                PA_TRACE_TILE(kq, 2);
                 ++kq;
                 progressed = true;
               }
@@ -648,7 +633,6 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             }
           }
         }
-        PA_TRACE(11);
         // every MMA issued above completes before TMEM is released
         tc_commit(smem_u32(&bars->drain));
         drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
@@ -658,14 +642,12 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   }
 
   if (W.status != 0) grid_dep_launch();
-  if (tid == 0) PA_TRACE(6);
   tc_fence_before();
   __syncthreads();
   if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0) PA_TRACE(7);
 }
 
 // ---------------------------------------------------------------------------
@@ -699,16 +681,14 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   using C = Cfg<HS, VG, G, N, STAGES, QR, NB>;
   const size_t smem = C::kSmemData + sizeof(Barriers) + 1024;
   // the softcap code is compiled only into the kernels that use it
-  static bool configured[2][64] = {};
+  static std::atomic<bool> configured[2][64];
   const int cap = P.softcap_on ? 1 : 0;
   auto kern = cap ? tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB, true>
                   : tc_attn_kernel<T, HS, VG, G, N, STAGES, QR, NB, false>;
-  if (g.device >= 0 && g.device < 64 && !configured[cap][g.device]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[cap][g.device] = true;
-  }
+  cudaError_t e = once_per_device(configured[cap], g.device, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
@@ -733,8 +713,8 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
-  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(C::kThreads), smem, a.stream,
-                             map, qmap, P);
+  e = launch_pdl(kern, dim3((unsigned)(units * G)), dim3(C::kThreads), smem, a.stream, map, qmap,
+                 P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
   return launch_pdl(tc_combine_kernel<T, VG, G, CombineShape<VG, G>::kCPT>,
                     dim3((unsigned)nq, (unsigned)((g.H + CombineShape<VG, G>::kHPB - 1) /
@@ -757,10 +737,10 @@ size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t
   return tc::decode_ws_bytes(s, tc::decode_units(g, s, num_seqs), num_seqs);
 }
 
-size_t tc_call_workspace(const Geometry& g, Phase ph, const ReadArgs& a) {
+size_t tc_call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end) {
   tc::Shape s;
   if (ph == Phase::kPrefill || !tc::pick(g, ph, &s)) return 0;
-  const int64_t nq = (int64_t)(a.seq_end - a.seq_begin);
+  const int64_t nq = (int64_t)(seq_end - seq_begin);
   return tc::decode_ws_bytes(s, tc::decode_units(g, s, nq), nq);
 }
 
@@ -799,13 +779,6 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.num_blocks = g.num_blocks;
   P.max_blocks = g.max_blocks;
   P.scale_log2 = g.scale * tc::kLog2e;
-  {
-    int e = 0;
-    if (P.scale_log2 > 0.f && std::isfinite(P.scale_log2)) e = std::ilogb(P.scale_log2);
-    e = e < -60 ? -60 : e > 60 ? 60 : e;
-    P.xscale = std::ldexp(1.f, e);
-    P.xunscale = std::ldexp(1.f, -e);
-  }
   P.softcap_on = g.softcap > 0.f ? 1 : 0;
   P.cap_in = g.softcap > 0.f ? g.scale / g.softcap : 0.f;
   P.cap_out = g.softcap * tc::kLog2e;
@@ -874,24 +847,3 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
 
 }  // namespace pa
 
-#ifdef PA_TC_TRACE
-extern "C" int pa_trace_dump(void* host, size_t bytes) {
-  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, bytes < sizeof(pa::tc::g_trace)
-                                                              ? bytes : sizeof(pa::tc::g_trace));
-}
-extern "C" int pa_trace_clear(void) {
-  static unsigned long long zero[8192][16];  // >= sizeof either trace array
-  cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
-  return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
-}
-extern "C" int pa_trace_combine(void* host, int reset) {
-  if (reset) {
-    const unsigned long long init[3] = {~0ull, ~0ull, 0ull};
-    return (int)cudaMemcpyToSymbol(pa::tc::g_ctrace, init, sizeof(init));
-  }
-  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_ctrace, sizeof(pa::tc::g_ctrace));
-}
-extern "C" int pa_trace_tile_dump(void* host) {
-  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
-}
-#endif

@@ -194,30 +194,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, int M, int N, bool b
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// Optional timeline trace (compiled only with -DPA_TC_TRACE): %globaltimer
-// stamps at phase boundaries per CTA, read back by a debug entry point.
-#ifdef PA_TC_TRACE
-static __device__ unsigned long long g_trace[8192][16];
-__device__ __forceinline__ void trace(int slot) {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  if (blockIdx.x < 8192) g_trace[blockIdx.x][slot] = t;
-}
-static __device__ unsigned long long g_trace_tile[2][256][16];
-__device__ __forceinline__ void trace_tile(int k, int slot) {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  if (blockIdx.x < 2 && k < 256) g_trace_tile[blockIdx.x][k][slot] = t;
-}
-// combine kernel: first start, first return from the grid wait, last end
-static __device__ unsigned long long g_ctrace[3];
-#define PA_TRACE(slot) trace(slot)
-#define PA_TRACE_TILE(k, slot) trace_tile(k, slot)
-#else
-#define PA_TRACE(slot) ((void)0)
-#define PA_TRACE_TILE(k, slot) ((void)0)
-#endif
-
 // ---------------------------------------------------------------------------
 // Parameters
 // ---------------------------------------------------------------------------
@@ -238,9 +214,6 @@ struct Params {
   int num_seqs, seq_begin, seq_end;
   int H, vhs, ro, rd, interleaved, cos_rows, bs, num_blocks, max_blocks;
   float scale_log2;  // scale * log2(e)
-  float xscale, xunscale;  // a power of two near scale_log2, and its inverse (CTA-pair
-                           // score exchange in 16 bits: partial scores travel as
-                           // fp16(S_c * xscale))
   float cap_in;      // scale / softcap   (softcap > 0)
   float cap_out;     // softcap * log2(e)
   int softcap_on;
@@ -529,7 +502,6 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
   const int lane = threadIdx.x & 31;
   const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin, units = P.units;
   const int own = lane < nseq ? (int)decode_tiles(P, seq_begin + lane, N) : 0;
-  if (lane == 0) PA_TRACE(13);
   // Smallest T with sum_b ceil(n_b / T) <= units. Since n_b / T <=
   // ceil(n_b / T) <= n_b / T + 1, it lies in [ceil(total / units),
   // ceil(total / (units - nseq))] (total = sum_b n_b; units >= nseq), and
@@ -556,7 +528,6 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
     if (warp_splits<N>(P, own, mid, nseq, seq_begin, more, cap) <= units) hi = mid; else lo = mid + 1;
   }
   const int T = lo;
-  if (lane == 0) PA_TRACE(14);
   // this lane's units, then an exclusive scan over the lanes
   int mine = 0;
   for (int i = lane; i < nseq; i += 32)
@@ -586,7 +557,6 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
     }
     run += c;
   }
-  if (lane == 0) PA_TRACE(15);
   const unsigned who = __ballot_sync(0xffffffffu, hit);
   if (who == 0) return w;  // idle unit
   const int src = __ffs(who) - 1;
@@ -675,13 +645,7 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
 // round trip per round of splits.
 template <typename T, int VG, int G, int CPT>
 __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ Params P) {
-#ifdef PA_TC_TRACE
-  if (threadIdx.x == 0) atomicMin(&g_ctrace[0], globaltimer());
-#endif
   grid_dep_wait();  // the attention kernel's partials are complete and visible
-#ifdef PA_TC_TRACE
-  if (threadIdx.x == 0) atomicMin(&g_ctrace[1], globaltimer());
-#endif
   constexpr int kTPH = G * VG / CPT;         // threads per head
   constexpr int kHPB = 256 / kTPH;           // heads per CTA
   constexpr int kRound = CPT >= 16 ? 4 : 8;  // splits whose loads are in flight together
@@ -749,10 +713,6 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
                                                       pk[4 * q + 3]);
     }
   }
-#ifdef PA_TC_TRACE
-  __syncthreads();
-  if (threadIdx.x == 0) atomicMax(&g_ctrace[2], globaltimer());
-#endif
 }
 
 // Combine launch shape: CPT channels per thread, heads per CTA.
@@ -770,16 +730,18 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+// The driver's tensor-map encoder, looked up once (a function-local static:
+// its initialisation is thread-safe).
 inline EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
+      return reinterpret_cast<EncodeTiledFn>(p);
+    return nullptr;
+  }();
   return fn;
 }
 

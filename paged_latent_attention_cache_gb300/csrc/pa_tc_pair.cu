@@ -16,12 +16,11 @@
 // The partial scores are exchanged by four dedicated warps (6-9, one per
 // TMEM lane quadrant): per tile they read S_c from TMEM, send it to the peer
 // through distributed shared memory (st.async, completing on the peer's
-// mbarrier), add the peer's rows (S_0 + S_1 in that order in both CTAs, so
-// both hold bit-identical S, P, m and l) and write the sum back for the
-// softmax warps; the exchange of tile k+1 overlaps the softmax of tile k.
-// With bf16 inputs the partials travel as fp16 in units of a power of two
-// near scale*log2e (16 KB per tile, two tiles in flight); fp16 inputs send
-// f32 partials (32 KB, one tile in flight).
+// mbarrier), add the peer's rows (the f32 sum S_0 + S_1 is the same in both
+// CTAs, so both hold bit-identical S, P, m and l) and write the sum back for
+// the softmax warps; the exchange of tile k+1 overlaps the softmax of tile
+// k. The partials travel as f32 (32 KB per tile, one tile in flight), so the
+// exchange adds no rounding and no range limit to the scores.
 // Three S buffers: O 256 + 3 x 64 + P 2 x 32 = 512 TMEM columns.
 //
 // Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
@@ -61,9 +60,9 @@ struct PairBarriers {
   uint64_t s_free[3];  // the softmax warps are done with the S buffer (128 arrivals)
   uint64_t p_full[2], pv_done[2];
   uint64_t q_tma, q_full;
-  uint64_t x_in[2];   // x_s buffer b holds the peer's partial rows (local expect_tx +
-                       // the peer's st.async complete_tx bytes)
-  uint64_t x_out[2];  // the peer has read the rows this CTA sent into its buffer b
+  uint64_t x_in[1];   // x_s holds the peer's partial rows (local expect_tx + the
+                       // peer's st.async complete_tx bytes)
+  uint64_t x_out[1];  // the peer has read the rows this CTA sent into its x_s
   uint64_t drain;
   uint32_t tmem_base;
   int bad;
@@ -77,17 +76,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
   using C = PairCfg<N, STAGES>;
   constexpr int G = 2, VG = C::kVG, NS = C::kSBufs;
-  // Score exchange format. bf16 inputs: partial scores travel as fp16 in
-  // units of xscale (a power of two near scale*log2e), 16 KB per tile, and
-  // x_s holds two tiles, so a tile is sent without waiting for the peer to
-  // have read the previous one. The 16-bit rounding of a partial logit L is
-  // at most |L| * 2^-11, below the rounding P itself gets as bf16 (2^-9
-  // relative) for |L| < 4 and of that order beyond. fp16 inputs (P kept to
-  // 2^-11): f32 partials, 32 KB per tile, one buffer.
-  constexpr bool kHalfX = std::is_same<T, __nv_bfloat16>::value;
-  constexpr int kXBufs = kHalfX ? 2 : 1;
-  constexpr int kXTile = kHalfX ? kRows * N * 2 : kRows * N * 4;  // bytes per tile
-  static_assert(kXBufs * kXTile <= C::kXBytes, "exchange buffers");
+  // Score exchange: f32 partials, one 32 KB tile in x_s at a time. (A 16-bit
+  // format would hold two tiles, but it rounds a partial logit L by |L| *
+  // 2^-11, several times P's own rounding once |L| reaches tens, and it
+  // overflows beyond 65504.)
+  constexpr int kXTile = kRows * N * 4;  // bytes per tile
+  static_assert(kXTile <= C::kXBytes, "exchange buffer");
   extern __shared__ uint8_t smem_raw[];
   __shared__ Work work;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -102,7 +96,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t peer = g ^ 1u;
   const int unit = blockIdx.x / G;
   const int vhs = P.vhs;
-  if (tid == 0) PA_TRACE(0);
 
   // ---- prologue (same plan in both CTAs of the pair) ----
   // As in the single-CTA kernel: inputs are read only after griddepcontrol.wait,
@@ -182,13 +175,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     }
     mbar_init(smem_u32(&bars->q_tma), 1);
     mbar_init(smem_u32(&bars->q_full), kRows);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bars->x_in[i]), 1);
-      mbar_init(smem_u32(&bars->x_out[i]), 1);
-    }
-    // armed for tiles 0 (and 1 with two exchange buffers)
+    mbar_init(smem_u32(&bars->x_in[0]), 1);
+    mbar_init(smem_u32(&bars->x_out[0]), 1);
+    // armed for tile 0
     mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
-    if (kXBufs == 2) mbar_expect_tx(smem_u32(&bars->x_in[1]), kXTile);
     mbar_init(smem_u32(&bars->drain), 1);
     bars->bad = 0;
     bars->abort = 0;
@@ -209,7 +199,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const uint32_t tmem = bars->tmem_base;
   volatile int* abort = &bars->abort;
   const Work W = work;
-  if (tid == 0) PA_TRACE(1);
 
   if (W.status == 0) {
     const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
@@ -282,7 +271,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
           fence_proxy_async();
           mbar_arrive(smem_u32(&bars->q_full));
-          if (tid == 0) PA_TRACE(3);
           if (!ok) break;
         }
         const int sb = dry ? 0 : k % NS;   // S buffer
@@ -293,8 +281,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_sum[sb]), (k / NS) & 1, abort,
                                                 P.err_flags));
           if (!ok) break;
-          if (tid == 0) PA_TRACE_TILE(k, 0);
-          if (tid == 0 && k == 0) PA_TRACE(4);
         }
         // The tile is handled in 32-column chunks read from TMEM twice (row
         // maximum, then exponentials), which keeps the loop body short.
@@ -397,11 +383,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         if (dry) continue;
         mbar_arrive(smem_u32(&bars->s_free[sb]));
         mbar_arrive(smem_u32(&bars->p_full[pb]));
-        if (tid == 0) PA_TRACE_TILE(k, 1);
       }
 
       // ---- epilogue ----
-      if (tid == 0) PA_TRACE(5);
       grid_dep_launch();
       named_sync(2, 160);
       ok = __all_sync(0xffffffffu, ok && !*abort);
@@ -454,35 +438,26 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // Warp w handles TMEM lanes 32*(w%4)..+31 (the quadrant its SM
       // sub-partition may access). Per tile: read this CTA's partial S rows,
       // send them to the peer's x_s with st.async (the bytes complete on the
-      // peer's x_in), wait for the peer's rows, form S_0 + S_1 (that order in
-      // both CTAs) and write the sum back into the S buffer for the softmax
-      // warps. x_s is chunk-major: 16-byte chunk q of row r at [q][r], so a
-      // warp's store of one chunk for its 32 rows is 512 contiguous bytes;
-      // with the 16-bit format it holds two such tiles (buffers 0 and 1).
-      // The sum is exact up to one rounding and the same in both CTAs.
-      constexpr int kChunks = kHalfX ? N / 8 : N / 4;  // 16-byte chunks per row and tile
+      // peer's x_in), wait for the peer's rows, form S_0 + S_1 (f32 addition
+      // is commutative, so both CTAs get the same bits) and write the sum
+      // back into the S buffer for the softmax warps. x_s is chunk-major:
+      // 16-byte chunk q of row r at [q][r], so a warp's store of one chunk
+      // for its 32 rows is 512 contiguous bytes.
+      constexpr int kChunks = N / 4;  // 16-byte chunks per row and tile
       const int xq = warp & 3, xrow = xq * 32 + lane, xt = tid - 192;  // xt: 0..127
       const uint32_t lane_addr = tmem + ((uint32_t)(xq * 32) << 16);
-      const uint32_t x_row = smem_u32(x_s) + xrow * 16;  // chunk 0 of this row, buffer 0
+      const uint32_t x_row = smem_u32(x_s) + xrow * 16;  // chunk 0 of this row
       const uint32_t x_peer = map_peer(x_row, peer);
-      const uint32_t x_in_peer0 = map_peer(smem_u32(&bars->x_in[0]), peer);
-      const uint32_t x_in_peer1 = map_peer(smem_u32(&bars->x_in[1]), peer);
-      const uint32_t x_out_peer0 = map_peer(smem_u32(&bars->x_out[0]), peer);
-      const uint32_t x_out_peer1 = map_peer(smem_u32(&bars->x_out[1]), peer);
-      const float xs = P.xscale, xu = P.xunscale;
+      const uint32_t x_in_peer = map_peer(smem_u32(&bars->x_in[0]), peer);
+      const uint32_t x_out_peer = map_peer(smem_u32(&bars->x_out[0]), peer);
       volatile int* xfail = &bars->xfail;
       bool ok = true;
       for (int k = 0; k < n; ++k) {
         const int sb = k % NS;
-        const int xb = kXBufs == 2 ? (k & 1) : 0;  // exchange buffer of tile k
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
                                               P.err_flags));
         uint32_t r[N / 32][32];
-        // 16-bit format: this CTA's partial rounded the way the peer will see
-        // it (the rounded values, in xscale units, are kept in r for the sum)
-        uint32_t hx[kHalfX ? N / 2 : 1];
         if (ok) {
-          if (xt == 0) PA_TRACE_TILE(k, 8);
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < N / 32; ++c)
@@ -490,105 +465,50 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           tmem_wait_ld();
 #pragma unroll
           for (int c = 0; c < N / 32; ++c) reg_fence(r[c]);
-          if (kHalfX) {
-#pragma unroll
-            for (int j = 0; j < N / 2; ++j) {
-              const int c0 = 2 * j;
-              uint32_t* d = &r[c0 / 32][c0 & 31];
-              __half2 h =
-                  __floats2half2_rn(__uint_as_float(d[0]) * xs, __uint_as_float(d[1]) * xs);
-              hx[j] = *reinterpret_cast<uint32_t*>(&h);
-              const float2 f = __half22float2(h);
-              d[0] = __float_as_uint(f.x);
-              d[1] = __float_as_uint(f.y);
-            }
-          }
-          if (k >= kXBufs)  // the peer has read tile k - kXBufs from buffer xb
-            ok = __all_sync(0xffffffffu,
-                            wait_bar_cluster(smem_u32(&bars->x_out[xb]),
-                                             ((k - kXBufs) / kXBufs) & 1, abort, P.err_flags));
+          if (k >= 1)  // the peer has read tile k - 1 from x_s
+            ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_out[0]),
+                                                          (k - 1) & 1, abort, P.err_flags));
         }
         if (ok) {
-          const uint32_t dst = x_peer + xb * kXTile;
-          const uint32_t x_in_p = xb ? x_in_peer1 : x_in_peer0;
 #pragma unroll
-          for (int q = 0; q < kChunks; ++q) {
-            if (kHalfX)
-              st_async_b32x4(dst + q * kRows * 16, hx[4 * q], hx[4 * q + 1], hx[4 * q + 2],
-                             hx[4 * q + 3], x_in_p);
-            else
-              st_async_b32x4(dst + q * kRows * 16, r[q / 8][(4 * q) & 31],
-                             r[q / 8][(4 * q + 1) & 31], r[q / 8][(4 * q + 2) & 31],
-                             r[q / 8][(4 * q + 3) & 31], x_in_p);
-          }
-          if (xt == 0) PA_TRACE_TILE(k, 9);
-          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in[xb]),
-                                                        (k / kXBufs) & 1, abort, P.err_flags));
+          for (int q = 0; q < kChunks; ++q)
+            st_async_b32x4(x_peer + q * kRows * 16, r[q / 8][(4 * q) & 31],
+                           r[q / 8][(4 * q + 1) & 31], r[q / 8][(4 * q + 2) & 31],
+                           r[q / 8][(4 * q + 3) & 31], x_in_peer);
+          ok = __all_sync(0xffffffffu, wait_bar_cluster(smem_u32(&bars->x_in[0]), k & 1, abort,
+                                                        P.err_flags));
         }
         if (ok) {
-          if (xt == 0) PA_TRACE_TILE(k, 12);
-          const uint8_t* src = reinterpret_cast<const uint8_t*>(x_s) + xrow * 16 + xb * kXTile;
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(x_s) + xrow * 16;
 #pragma unroll
           for (int q = 0; q < kChunks; ++q) {
             const uint4 v = *reinterpret_cast<const uint4*>(src + q * kRows * 16);
-            if (kHalfX) {
-              // S = (own + peer) / xscale: the same two rounded values in both
-              // CTAs, so both hold bit-identical S (the scaling is exact)
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int c0 = 8 * q + 2 * e;
-                uint32_t* d = &r[c0 / 32][c0 & 31];
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w4[e]));
-                d[0] = __float_as_uint((__uint_as_float(d[0]) + f.x) * xu);
-                d[1] = __float_as_uint((__uint_as_float(d[1]) + f.y) * xu);
-              }
-            } else {
-              uint32_t* d = &r[q / 8][(4 * q) & 31];
-              const float pv[4] = {__uint_as_float(v.x), __uint_as_float(v.y),
-                                   __uint_as_float(v.z), __uint_as_float(v.w)};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float mine = __uint_as_float(d[e]);
-                d[e] = __float_as_uint(g == 0 ? mine + pv[e] : pv[e] + mine);
-              }
-            }
+            uint32_t* d = &r[q / 8][(4 * q) & 31];
+            d[0] = __float_as_uint(__uint_as_float(d[0]) + __uint_as_float(v.x));
+            d[1] = __float_as_uint(__uint_as_float(d[1]) + __uint_as_float(v.y));
+            d[2] = __float_as_uint(__uint_as_float(d[2]) + __uint_as_float(v.z));
+            d[3] = __float_as_uint(__uint_as_float(d[3]) + __uint_as_float(v.w));
           }
         } else if (lane == 0) {
           *xfail = 1;
         }
-        // Buffer xb is released to the peer once every row of it has been
-        // read (the named barrier). With one buffer the peer's next tile
-        // waits for that, so it goes first; with two the peer sends into the
-        // other buffer meanwhile, and the sum goes to the softmax warps
-        // first. All four exchange warps pass every tile's barrier, a failed
-        // tile's included, and leave the loop together after it.
-        bool leave = false;
-        auto release = [&]() {
-          named_sync(3, 128);
-          leave = *xfail != 0;
-          if (!leave && xt == 0) {
-            if (k + kXBufs < n) mbar_expect_tx(smem_u32(&bars->x_in[xb]), kXTile);
-            arrive_peer_relaxed(xb ? x_out_peer1 : x_out_peer0);
-          }
-        };
-        if (kXBufs == 1) {
-          release();
-          if (leave) break;
+        // x_s is released to the peer once every row of it has been read (the
+        // named barrier); the peer's next tile waits for that, so the release
+        // comes before the sum goes back to TMEM. All four exchange warps pass
+        // every tile's barrier, a failed tile's included, and leave the loop
+        // together after it.
+        named_sync(3, 128);
+        if (*xfail != 0) break;
+        if (xt == 0) {
+          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
+          arrive_peer_relaxed(x_out_peer);
         }
-        if (ok) {
 #pragma unroll
-          for (int c = 0; c < N / 32; ++c)
-            tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive(smem_u32(&bars->s_sum[sb]));
-          if (xt == 0) PA_TRACE_TILE(k, 11);
-        }
-        if (kXBufs == 2) {
-          release();
-          if (leave) break;
-        }
+        for (int c = 0; c < N / 32; ++c)
+          tmem_st32(lane_addr + C::kColS + sb * N + c * 32, r[c]);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(smem_u32(&bars->s_sum[sb]));
       }
     } else if (warp == 4) {
       // =================== TMA producer ===================
@@ -636,7 +556,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
         if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
-        if (lane == 0) PA_TRACE_TILE(k, 5);
         __syncwarp();
         if (lane < nsub) {
           const uint32_t full = smem_u32(&bars->full[stage]);
@@ -687,7 +606,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                          b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
                 tc_commit(smem_u32(&bars->pv_done[pb]));
                 tc_commit(smem_u32(&bars->empty[stage]));
-                PA_TRACE_TILE(kp, 3);
                 ++kp;
                 progressed = true;
               }
@@ -700,7 +618,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
                   (kq < NS ||
                    mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NS) / NS) & 1))) {
-                PA_TRACE_TILE(kq, 4);
                 tc_fence_after();
                 const uint32_t kb = k_base + stage * C::kStageBytes;
                 // Descriptors built once; per step only the address field
@@ -728,7 +645,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                          i > 0 ? 1u : 0u);
                 }
                 tc_commit(smem_u32(&bars->s_part[sb]));
-                PA_TRACE_TILE(kq, 2);
                 ++kq;
                 progressed = true;
               }
@@ -756,14 +672,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   }
 
   if (W.status != 0) grid_dep_launch();
-  if (tid == 0) PA_TRACE(6);
   tc_fence_before();
   cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (tid == 0) PA_TRACE(7);
 }
 
 template <typename T>
@@ -771,14 +685,12 @@ cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& 
   constexpr int N = 64, STAGES = 3;
   using C = PairCfg<N, STAGES>;
   const size_t smem = C::kSmemData + sizeof(PairBarriers) + 1024;
-  static bool configured[64] = {false};
+  static std::atomic<bool> configured[64];
   auto kern = tc_pair_kernel<T, N, STAGES>;
-  if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    configured[g.device] = true;
-  }
+  cudaError_t e = once_per_device(configured, g.device, [&] {
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (e != cudaSuccess) return e;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
@@ -807,8 +719,8 @@ cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& 
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
-  cudaError_t e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem,
-                             a.stream, map, qmap, qmap64, P);
+  e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem, a.stream, map, qmap,
+                 qmap64, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
   return launch_pdl(tc_combine_kernel<T, 256, 2, CombineShape<256, 2>::kCPT>,
                     dim3((unsigned)nq, (unsigned)((g.H + CombineShape<256, 2>::kHPB - 1) /
@@ -825,14 +737,3 @@ template cudaError_t launch_pair<__half>(const Geometry&, Phase, const ReadArgs&
 }  // namespace pa
 
 
-#ifdef PA_TC_TRACE
-extern "C" int pa_trace_pair_dump(void* host, void* tile_host) {
-  cudaMemcpyFromSymbol(tile_host, pa::tc::g_trace_tile, sizeof(pa::tc::g_trace_tile));
-  return (int)cudaMemcpyFromSymbol(host, pa::tc::g_trace, sizeof(pa::tc::g_trace));
-}
-extern "C" int pa_trace_pair_clear(void) {
-  static unsigned long long zero[8192][16];
-  cudaMemcpyToSymbol(pa::tc::g_trace_tile, zero, sizeof(pa::tc::g_trace_tile));
-  return (int)cudaMemcpyToSymbol(pa::tc::g_trace, zero, sizeof(zero));
-}
-#endif

@@ -16,7 +16,7 @@ def _check(w, portable=False, tokens=None, default_scale=False):
     ref = Hn.run_oracle(w, tokens)
     assert got["flags"] == 0, hex(got["flags"])
     Hn.check_cache(w, got["cache"], ref["cache"])
-    Hn.check_out(w, got["out"], ref["out"], tokens)
+    Hn.check_out(w, got["out"], ref["out"], tokens, ref["scales"])
     return got
 
 
@@ -59,14 +59,29 @@ def test_geometries(hs, vhs, ro, rd, H):
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
 @pytest.mark.parametrize("bs", [16, 64])
-def test_pair_kernel_exchange_formats(dtype, bs):
-    """The CTA-pair kernel (576/512 latent) with both partial-score exchange
-    formats (fp16 partials for bf16 inputs, f32 for fp16 inputs), one box
-    per key tile (64-row blocks) and four (16-row blocks), over decode and
-    prefill tokens with several key tiles and ragged tails."""
+def test_pair_kernel_dtypes_and_boxes(dtype, bs):
+    """The CTA-pair kernel (576/512 latent) with bf16 and fp16 inputs, one
+    box per key tile (64-row blocks) and four (16-row blocks), over decode
+    and prefill tokens with several key tiles and ragged tails."""
     w = W.make_workload("pair", q_lens=[1, 1, 70, 1], past_lens=[300, 1, 200, 129],
                         num_heads=128, **W.DSV3, block_size=bs, seed=31, dtype=dtype,
                         drop_slots=1)
+    _check(w)
+
+
+@pytest.mark.parametrize("dtype,gain", [(torch.bfloat16, 128), (torch.bfloat16, 2 ** 17),
+                                        (torch.float16, 128), (torch.float16, 2 ** 13)],
+                         ids=["bf16-x128", "bf16-x2^17", "fp16-x128", "fp16-x2^13"])
+def test_pair_kernel_large_logits(dtype, gain):
+    """The CTA pair splits each score into two partial dot products that it
+    exchanges between its SMs. With the query scaled by 128 the partial
+    logits reach hundreds of log2 units, with 2^17 (bf16) or 2^13 (fp16)
+    they pass 6e4, beyond the fp16 range: the outputs stay finite and
+    within the bounds (the softmax is one-hot at the largest gains)."""
+    w = W.make_workload("pair_peaked", q_lens=[1, 1, 40], past_lens=[300, 77, 150],
+                        num_heads=128, **W.DSV3, block_size=64, seed=33, dtype=dtype,
+                        query_gain=gain, scale=W.DSV3_SCALE)
+    assert Hn.run_gpu(w)["op"].kernel_family(0) == 1
     _check(w)
 
 
@@ -179,12 +194,13 @@ def test_after_write_flag_bit_equal(name, own_slots):
 
 @pytest.mark.parametrize("name", ["glm_decode", "dsv3_decode"])
 def test_workspace_reuse_across_batch_sizes(name):
-    """Decode splits publish partials and count finished splits in the
-    workspace; the last split of a sequence merges. One workspace serves
+    """Decode splits publish their partials and the per-sequence plan in
+    the workspace, and the combine kernel merges them. One workspace serves
     calls over different sequence ranges in a row: a repeated full call is
     bit-equal to the first, and a call over a sub-range (a different split
     plan, so different rounding) agrees with it within the output tolerance.
-    A counter left non-zero would drop or duplicate partials."""
+    A plan or partial left behind by an earlier call and read by a later
+    one would show up as a mismatch."""
     w = Hn.workload(name)
     d = w.to("cuda")
     from paged_latent_attention_cache_gb300.api import PagedLatentAttention
