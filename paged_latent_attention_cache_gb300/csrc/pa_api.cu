@@ -14,6 +14,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <string>
 
 #include "pa_common.cuh"
@@ -37,14 +38,18 @@ pa_status fail(pa_status s, const char* fmt, ...) {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Per-device SM count, looked up once per device.
+// Per-device SM count, looked up once per device (atomic: several host
+// threads may make their first call at once).
 int sm_count(int device) {
-  static int cache[64] = {0};
-  if (device >= 0 && device < 64 && cache[device] > 0) return cache[device];
+  static std::atomic<int> cache[64];
+  if (device >= 0 && device < 64) {
+    const int c = cache[device].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || n <= 0)
     n = 148;
-  if (device >= 0 && device < 64) cache[device] = n;
+  if (device >= 0 && device < 64) cache[device].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -146,6 +151,15 @@ bool use_tc(const Geometry& g, Phase ph) {
   return !(g.flags & PA_FLAG_PORTABLE) && tc_supported(g, ph);
 }
 
+// Workspace one read call needs: decode over sequences [seq_begin, seq_end),
+// prefill over num_tokens tokens.
+size_t call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end,
+                      int64_t num_tokens) {
+  if (use_tc(g, ph)) return tc_call_workspace(g, ph, seq_begin, seq_end);
+  const int64_t nq = ph == Phase::kDecode ? (int64_t)(seq_end - seq_begin) : num_tokens;
+  return portable_call_workspace(g, ph, nq);
+}
+
 pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int64_t num_tokens,
                      const void* key_cache, const void* cos_cache, const void* sin_cache,
                      const int32_t* cumseq, const int32_t* past, const int32_t* block_table,
@@ -180,8 +194,7 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
              past,    block_table, num_seqs,  seq_begin, seq_end,   workspace,
              workspace_bytes, out, err_flags, reinterpret_cast<cudaStream_t>(stream)};
   const bool tc = use_tc(g, ph);
-  const int64_t nq = ph == Phase::kDecode ? (int64_t)(seq_end - seq_begin) : num_tokens;
-  const size_t need = tc ? tc_call_workspace(g, ph, a) : portable_call_workspace(g, ph, nq);
+  const size_t need = call_workspace(g, ph, seq_begin, seq_end, num_tokens);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace ? workspace_bytes : (size_t)0, need);
@@ -192,6 +205,17 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
 }  // namespace
 
 pa_status record_error(pa_status s, const char* msg) { return fail(s, "%s", msg); }
+
+pa_status decode_call_workspace(const pa_latent_params* p, int32_t seq_begin, int32_t seq_end,
+                                size_t* need) {
+  Geometry g;
+  const pa_status s = resolve(p, &g);
+  if (s != PA_OK) return s;
+  *need = seq_end > seq_begin && seq_begin >= 0
+              ? call_workspace(g, Phase::kDecode, seq_begin, seq_end, seq_end - seq_begin)
+              : 0;
+  return PA_OK;
+}
 
 }  // namespace pa
 

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "pa_latent.h"
 
 namespace pa {
@@ -31,6 +33,19 @@ struct Geometry {
 };
 
 enum class Phase { kDecode = 0, kPrefill = 1 };
+
+// Runs an idempotent per-device set-up action (a kernel attribute) once per
+// device ordinal < 64. Safe when several host threads make their first call
+// at the same time: the flags are atomic, and two threads that both see a
+// flag unset both run the action, which is harmless.
+template <typename F>
+cudaError_t once_per_device(std::atomic<bool> (&done)[64], int device, F&& action) {
+  if (device < 0 || device >= 64) return action();
+  if (done[device].load(std::memory_order_acquire)) return cudaSuccess;
+  const cudaError_t e = action();
+  if (e == cudaSuccess) done[device].store(true, std::memory_order_release);
+  return e;
+}
 
 // Records msg as the calling thread's pa_latent_last_error() text and
 // returns s.
@@ -71,7 +86,15 @@ cudaError_t launch_portable(const Geometry& g, Phase ph, const ReadArgs& a);
 // ---- tcgen05 / TMA attention (pa_tc.cu)
 bool tc_supported(const Geometry& g, Phase ph);
 size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t num_tokens);
-size_t tc_call_workspace(const Geometry& g, Phase ph, const ReadArgs& a);
+// Workspace one read call over sequences [seq_begin, seq_end) needs.
+size_t tc_call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end);
 cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a);
+
+// ---- shared by the entry points (pa_api.cu)
+// Workspace bytes a decode call over sequences [seq_begin, seq_end) of these
+// parameters needs on the current device, or an error status for invalid
+// parameters. Host-only.
+pa_status decode_call_workspace(const pa_latent_params* p, int32_t seq_begin, int32_t seq_end,
+                                size_t* need);
 
 }  // namespace pa

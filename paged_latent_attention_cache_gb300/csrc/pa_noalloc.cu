@@ -17,9 +17,11 @@
 namespace {
 
 // Scratch for the split-KV partials and the per-sequence plan of one decode
-// call. 32 MiB covers the decode calls of every geometry with a tensor-core
-// kernel up to a few hundred sequences (a 576/512 batch of 64 sequences uses
-// about 20 MiB); larger calls are rejected.
+// call: 32 MiB. A tensor-core decode call needs about 264 KB per sequence
+// with the 576/512 geometry (two SMs x 128 rows x (256 + 2) f32) and 67 KB
+// with 192/128, for at least as many sequences as the grid's work units (one
+// per SM, or per SM pair), so calls of up to 127 sequences (576/512) or 504
+// sequences (192/128) fit; larger calls are rejected.
 constexpr size_t kScratchBytes = 32ull << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
@@ -56,9 +58,9 @@ pa_status pa_latent_decode_noalloc(const pa_latent_params* p, const void* query,
                                    const int32_t* block_table, int32_t num_seqs,
                                    int32_t seq_begin, int32_t seq_end, void* out,
                                    int32_t* err_flags, void* stream) {
-  pa_status s = pa_latent_validate(p);
+  size_t need = 0;
+  const pa_status s = pa::decode_call_workspace(p, seq_begin, seq_end, &need);
   if (s != PA_OK) return s;
-  const size_t need = pa_latent_workspace_size(p, num_seqs, num_tokens);
   if (need > kScratchBytes) {
     char msg[192];
     snprintf(msg, sizeof msg,

@@ -331,18 +331,17 @@ template <typename T, int NV>
 cudaError_t launch_typed(const Geometry& g, Phase ph, const ReadArgs& a, PortableParams& P,
                          int64_t nq) {
   const size_t smem = smem_bytes(g);
-  static int configured[64] = {0};
-  if (g.device >= 0 && g.device < 64 && !configured[g.device]) {
-    cudaError_t e = cudaFuncSetAttribute(portable_attn_kernel<T, NV>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kWarps * pa::kMaxHeadSize * 4 +
-                                               kTile * (pa::kMaxHeadSize + 8) * 2 + kTile * 8));
-    if (e != cudaSuccess) return e;
-    configured[g.device] = 1;
-  }
+  static std::atomic<bool> configured[64];
+  cudaError_t e = once_per_device(configured, g.device, [] {
+    return cudaFuncSetAttribute(portable_attn_kernel<T, NV>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)(kWarps * pa::kMaxHeadSize * 4 +
+                                      kTile * (pa::kMaxHeadSize + 8) * 2 + kTile * 8));
+  });
+  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)nq, (unsigned)((g.H + kWarps - 1) / kWarps), (unsigned)P.splits);
   portable_attn_kernel<T, NV><<<grid, kWarps * 32, smem, a.stream>>>(P);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess || P.splits == 1) return e;
   portable_combine_kernel<T><<<dim3((unsigned)nq, (unsigned)g.H), 128, 0, a.stream>>>(P);
   return cudaGetLastError();

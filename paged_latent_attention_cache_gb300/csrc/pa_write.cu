@@ -13,11 +13,6 @@
 
 namespace pa {
 
-#ifdef PA_TC_TRACE
-// trace builds only: first start and last end of the write kernel
-static __device__ unsigned long long g_wtrace[2];
-#endif
-
 // Largest batch whose cumulative offsets are staged in shared memory (the
 // token -> sequence search then runs on chip instead of as a chain of
 // dependent global loads).
@@ -35,13 +30,6 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
   // start its prologue now; it waits (griddepcontrol.wait) for this grid to
   // complete before it reads the cache.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-#ifdef PA_TC_TRACE
-  if (threadIdx.x == 0) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    atomicMin(&g_wtrace[0], t);
-  }
-#endif
   extern __shared__ int32_t s_cum[];  // cumseq[0..num_seqs] when staged
   const bool staged = num_seqs <= kStagedSeqs;
   if (staged) {
@@ -94,14 +82,6 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
     }
     *reinterpret_cast<uint4*>(key_cache + (int64_t)slot * hs + d0) = v;
   }
-#ifdef PA_TC_TRACE
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    atomicMax(&g_wtrace[1], t);
-  }
-#endif
 }
 
 cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
@@ -134,12 +114,3 @@ cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
 
 }  // namespace pa
 
-#ifdef PA_TC_TRACE
-extern "C" int pa_trace_write(void* host, int reset) {
-  if (reset) {
-    const unsigned long long init[2] = {~0ull, 0ull};
-    return (int)cudaMemcpyToSymbol(pa::g_wtrace, init, sizeof(init));
-  }
-  return (int)cudaMemcpyFromSymbol(host, pa::g_wtrace, sizeof(pa::g_wtrace));
-}
-#endif
