@@ -3,24 +3,28 @@
 One step = one pass of the whole operator over one synthetic batch: the
 write phase (RoPE + paged scatter of the new latent rows), the decode phase
 (split-KV attention + log-sum-exp combine) and, for mixed batches, the
-prefill phase. The default workload is GLM-style dense MLA decode (bf16,
-H=64, latent 192 / value 128 / rotary 64 at offset 128, batch 32, one new
-token per sequence, contexts uniform in [1024, 8192], bs=64).
+prefill phase. The headline workload is DeepSeek-V3-style absorbed MLA
+decode (bf16, H=128, latent 576 / value 512 / rotary 64 at offset 512,
+batch 64, one new token per sequence, context 4096, bs=64), the largest
+decode configuration; the same JSON line carries DeepSeek-V3-style chunked
+prefill (4 x 4096 new tokens, tensor-bound), GLM-style decode and the mixed
+fp16 serving batch under "extras", each timed the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl reference] [--portable]
+                    [--extras A,B,...|none] [--impl reference] [--portable]
 
 Timing: W untimed eager steps, then the step is captured in a CUDA graph
 and K graph replays are timed, bracketed by a barrier and a device
 synchronise; each replay is timed with CUDA events on the launching stream
 and L2 is flushed (a write of 2x the L2 size) before every replay, outside
-the events. A second loop replays one graph per phase for the breakdown. Under torchrun each rank runs its own seeded batch
-(weak scaling, no collective on the data path) and the max over ranks is
-reported. `value` is algorithmic latent-cache bytes per second (TB/s);
-`e2e` is the same metric through the operator object with the step's inputs
-copied host->device from pinned memory and the output copied back inside
-the timed region. `--impl reference` times the CPU oracle on the same
-workload instead (rank 0 only).
+the events. A second loop replays one graph per (non-empty) phase for the
+breakdown and the dominant call's duration. Under torchrun each rank runs
+its own seeded batch (weak scaling, no collective on the data path) and the
+max over ranks is reported. `value` is algorithmic latent-cache bytes per
+second (TB/s) of the headline workload; `e2e` is the same metric through the
+operator object with the step's inputs copied host->device from pinned
+memory and the output copied back inside the timed region. `--impl
+reference` times the CPU oracle on the same workload instead (rank 0 only).
 """
 from __future__ import annotations
 
@@ -47,11 +51,11 @@ UNIT = "TB/s"
 # ---------------------------------------------------------------------------
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# attention kernel, from the `ncu --set full` captures summarised under
-# profiles/ (tc_attn_kernel_glm_decode.md, tc_pair_kernel_dsv3_decode.md),
-# with the SHA-256 of the tensor-core kernel sources they were taken on.
-# Once those sources change the figure no longer describes the kernel and
-# the roofline reports null traffic until a new capture replaces it.
+# attention kernel, from `ncu --set full` captures of that kernel on the
+# named workload, with the SHA-256 of the tensor-core kernel sources they
+# were taken on. Once those sources change the figure no longer describes
+# the kernel and the roofline reports null traffic until a new capture
+# replaces it.
 KERNEL_SOURCES = ("pa_tc.cu", "pa_tc_common.cuh", "pa_tc_pair.cu")
 NCU_TRAFFIC = {
     "glm_decode": ("tc_attn_kernel", 54255872, "e0f1913c268e7a95"),
@@ -297,59 +301,59 @@ def graph_kernel_nodes(g):
         return None
 
 
-def run_gpu_arm(args, rank, world, device):
+def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=True):
+    """Times one workload: K graph replays of the whole step (write, decode,
+    prefill; empty phases are not launched), then K replays of the per-phase
+    graphs, optionally the end-to-end path. Returns a dict of results."""
     import torch
-    from paged_latent_attention_cache_gb300 import build as _build
-    _build.build()
     from paged_latent_attention_cache_gb300.api import PagedLatentAttention
 
-    w = build_workload(args.workload, rank_seed(0, rank) if world > 1 else 0)
+    w = build_workload(name, rank_seed(0, rank) if world > 1 else 0)
     d = w.to(device)
     op = PagedLatentAttention.from_workload(w, device=device, portable=args.portable)
     out = torch.empty(w.num_tokens, w.num_heads * w.v_head_size, dtype=w.dtype, device=device)
     cache = d.key_cache
     nd = w.num_decode_seqs
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
     def write():
         op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
 
     def decode():
-        if nd > 0:
-            op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                      d.block_table, out, 0, nd, after_write=True)
+        op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                  d.block_table, out, 0, nd, after_write=True)
 
     def prefill():
-        if nd < w.num_seqs:
-            op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                       d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
+        op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                   d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
+
+    phases = [("write", write), ("decode", decode if nd > 0 else None),
+              ("prefill", prefill if nd < w.num_seqs else None)]
 
     def step():
-        write()
-        decode()
-        prefill()
+        for _, f in phases:
+            if f is not None:
+                f()
 
-    for _ in range(max(args.warmup, 3)):   # eager warm-up (also configures kernels)
+    for _ in range(max(warmup, 3)):   # eager warm-up (also configures kernels)
         flush.zero_()
         step()
     torch.cuda.synchronize(device)
     if op.error_flags() != 0:
-        raise RuntimeError(f"device error flags {op.error_flags():#x}")
-    # One graph for the whole step (the timed unit) and one per phase (the
-    # breakdown and the dominant call's duration).
+        raise RuntimeError(f"{name}: device error flags {op.error_flags():#x}")
+    # One graph for the whole step (the timed unit) and one per non-empty
+    # phase (the breakdown and the dominant call's duration).
     g_step, kept = make_graph(step, keep=True)
     launches_per_step = graph_kernel_nodes(g_step) if kept else None
-    g_phase = [make_graph(f)[0] for f in (write, decode, prefill)]
+    g_phase = [(n, make_graph(f)[0]) for n, f in phases if f is not None]
     for _ in range(3):
         flush.zero_()
         g_step.replay()
-        for gp in g_phase:
+        for _, gp in g_phase:
             gp.replay()
     torch.cuda.synchronize(device)
 
-    K = args.steps
+    K = steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
     gpu_index = device.index
     vis = os.environ.get("CUDA_VISIBLE_DEVICES")
@@ -361,7 +365,7 @@ def run_gpu_arm(args, rank, world, device):
     # the raw clock samples of the timed region (the JSON line carries their summary)
     clock_dir = os.environ.get("PA_BENCH_CLOCK_DIR", os.path.join(ROOT, "bench_out"))
     os.makedirs(clock_dir, exist_ok=True)
-    sampler = ClockSampler(gpu_index, os.path.join(clock_dir, f"clocks_r{rank}.csv"))
+    sampler = ClockSampler(gpu_index, os.path.join(clock_dir, f"clocks_{name}_r{rank}.csv"))
     time.sleep(0.3)
     barrier(device)
     torch.cuda.synchronize(device)
@@ -376,66 +380,69 @@ def run_gpu_arm(args, rank, world, device):
     wall = time.perf_counter() - wall0
     clocks = sampler.stop()
     # per-phase breakdown (separate loop, same flushing)
-    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    pev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(g_phase) + 1)]
+           for _ in range(K)]
     for i in range(K):
         flush.zero_()
         pev[i][0].record(stream)
-        for j, gp in enumerate(g_phase):
+        for j, (_, gp) in enumerate(g_phase):
             gp.replay()
             pev[i][j + 1].record(stream)
     torch.cuda.synchronize(device)
 
     step_ms = [e[0].elapsed_time(e[1]) for e in evs]
-    write_ms = [e[0].elapsed_time(e[1]) for e in pev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in pev]
-    pre_ms = [e[2].elapsed_time(e[3]) for e in pev]
+    phase_ms = {n: 0.0 for n, _ in phases}
+    for j, (n, _) in enumerate(g_phase):
+        phase_ms[n] = statistics.mean(e[j].elapsed_time(e[j + 1]) for e in pev)
     ms_per_step = reduce_max(sum(step_ms) / K, device)
+    q = statistics.quantiles(step_ms, n=10) if K >= 2 else [step_ms[0]] * 9
+    dist = {"median": round(statistics.median(step_ms), 5), "p10": round(q[0], 5),
+            "p90": round(q[-1], 5)}
 
-    # End to end through the operator object: H2D of the step's inputs from
-    # pinned memory, the three phases, D2H of the output.
-    host = {k: getattr(w, k).pin_memory() for k in
-            ("query", "key", "cumseq", "past", "block_table", "slot_mapping")}
-    dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out_host.numel() * out_host.element_size()
+    e2e_ms = h2d = d2h = None
+    if e2e:
+        # End to end through the operator object: H2D of the step's inputs
+        # from pinned memory, the three phases, D2H of the output.
+        host = {k: getattr(w, k).pin_memory() for k in
+                ("query", "key", "cumseq", "past", "block_table", "slot_mapping")}
+        dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in host.values())
+        d2h = out_host.numel() * out_host.element_size()
 
-    def e2e_step():
-        for k, v in host.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        op.forward(dev_in["query"], dev_in["key"], cache, d.cos_cache, d.sin_cache,
-                   dev_in["cumseq"], dev_in["past"], dev_in["block_table"],
-                   dev_in["slot_mapping"], nd, out=out)
-        out_host.copy_(out, non_blocking=True)
+        def e2e_step():
+            for k, v in host.items():
+                dev_in[k].copy_(v, non_blocking=True)
+            op.forward(dev_in["query"], dev_in["key"], cache, d.cos_cache, d.sin_cache,
+                       dev_in["cumseq"], dev_in["past"], dev_in["block_table"],
+                       dev_in["slot_mapping"], nd, out=out)
+            out_host.copy_(out, non_blocking=True)
 
-    for _ in range(3):
-        flush.zero_()
-        e2e_step()
-    torch.cuda.synchronize(device)
-    e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
-    barrier(device)
-    for i in range(K):
-        flush.zero_()
-        e2e_evs[i][0].record(stream)
-        e2e_step()
-        e2e_evs[i][1].record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_evs) / K, device)
+        for _ in range(3):
+            flush.zero_()
+            e2e_step()
+        torch.cuda.synchronize(device)
+        e2e_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+        barrier(device)
+        for i in range(K):
+            flush.zero_()
+            e2e_evs[i][0].record(stream)
+            e2e_step()
+            e2e_evs[i][1].record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_evs) / K, device)
     if op.error_flags() != 0:
-        raise RuntimeError(f"device error flags {op.error_flags():#x}")
+        raise RuntimeError(f"{name}: device error flags {op.error_flags():#x}")
 
     work = algorithmic_work(w)
     dec_work = algorithmic_work(w, seqs=range(nd), include_write=False)
     pre_work = algorithmic_work(w, seqs=range(nd, w.num_seqs), include_write=False)
-    total_bytes = work["bytes"] * world
-    value = total_bytes / (ms_per_step * 1e-3) / 1e12
-    tflops = work["flops"] * world / (ms_per_step * 1e-3) / 1e12
-    res = dict(w=w, work=work, dec_work=dec_work, pre_work=pre_work, value=value,
-               tflops=tflops, ms_per_step=ms_per_step, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
-               clocks=clocks, wall=wall, launches=launches_per_step,
-               write_ms=statistics.mean(write_ms), dec_ms=statistics.mean(dec_ms),
-               pre_ms=statistics.mean(pre_ms), step_ms_med=statistics.median(step_ms),
-               family=(op.kernel_family(0), op.kernel_family(1)))
+    res = dict(w=w, work=work, dec_work=dec_work, pre_work=pre_work,
+               value=work["bytes"] * world / (ms_per_step * 1e-3) / 1e12,
+               tflops=work["flops"] * world / (ms_per_step * 1e-3) / 1e12,
+               ms_per_step=ms_per_step, dist=dist, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
+               clocks=clocks, wall=wall, launches=launches_per_step, phase_ms=phase_ms,
+               family=(op.kernel_family(0), op.kernel_family(1)), steps=K)
     return res
 
 
@@ -450,12 +457,85 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def roofline(res, peaks):
+    """Roofline of the dominant call (decode when the batch has decode
+    sequences, else prefill): the bound is whichever of its algorithmic
+    bytes at the measured HBM copy bandwidth and its FLOPs at the measured
+    dense bf16 burst peak takes longer; `achieved` is the algorithmic work
+    over the call's mean duration, timed live with CUDA events."""
+    w = res["w"]
+    hbm, bf16, bf16_sus, peak_src = peaks
+    if w.num_decode_seqs:
+        dom, dom_ms = res["dec_work"], res["phase_ms"]["decode"]
+        dom_name = "decode call (split-KV attention + combine)"
+    else:
+        dom, dom_ms = res["pre_work"], res["phase_ms"]["prefill"]
+        dom_name = "prefill call"
+    t_bytes = dom["bytes"] / (hbm * 1e9)
+    t_flops = dom["flops"] / (bf16 * 1e12)
+    traffic, traffic_kernel = ncu_traffic(w.name)
+    if t_flops > t_bytes:
+        achieved = dom["flops"] / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
+                "unit": "TFLOP/s", "frac": round(achieved / bf16, 4),
+                "peak_kind": "bf16 dense burst (of measured)",
+                "frac_of_sustained": round(achieved / bf16_sus, 4),
+                "sustained_peak": bf16_sus}
+    else:
+        achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "peak_kind": "HBM copy (of measured)"}
+    roof.update({"traffic": traffic, "traffic_kernel": traffic_kernel,
+                 "alg_bytes": dom["bytes"], "alg_flops": dom["flops"],
+                 "kernel": dom_name, "kernel_ms": round(dom_ms, 5),
+                 "peak_source": peak_src})
+    return roof
+
+
+def config_of(w, world):
+    """The workload description both arms print."""
+    return {"workload": w.name, "dtype": {"torch.bfloat16": "bf16",
+                                           "torch.float16": "f16"}[str(w.dtype)],
+            "num_heads": w.num_heads, "head_size": w.head_size, "v_head_size": w.v_head_size,
+            "rotary": [w.rotary_offset, w.rotary_dim], "block_size": w.block_size,
+            "num_seqs": w.num_seqs, "num_decode_seqs": w.num_decode_seqs,
+            "num_tokens": w.num_tokens, "softcap": w.softcap,
+            "local_window_size": w.local_window_size,
+            "l2": "flushed before every step (write of 2x L2)",
+            "timing": "CUDA graph of the step, CUDA events per replay",
+            "parallelism": f"replicas x{world} (independent batches per rank)"}
+
+
+def summary(res, peaks, world, args):
+    w = res["w"]
+    return {
+        "value": round(res["value"], 4), "unit": UNIT,
+        "ms_per_step": round(res["ms_per_step"], 5), "step_ms": res["dist"],
+        "steps": res["steps"],
+        "tflops": round(res["tflops"], 3),
+        "tokens_per_s": round(w.num_tokens * world / (res["ms_per_step"] * 1e-3), 1),
+        "phase_ms": {k: round(v, 5) for k, v in res["phase_ms"].items()},
+        "alg_bytes_per_step": res["work"]["bytes"], "alg_flops_per_step": res["work"]["flops"],
+        "roofline": roofline(res, peaks),
+        "kernels": "portable" if args.portable or res["family"][0] != 1 else "tcgen05",
+        "clocks": res["clocks"],
+        "config": config_of(w, world),
+    }
+
+
+EXTRA_STEPS = {"dsv3_prefill": 20}
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="glm_decode")
+    ap.add_argument("--workload", default="dsv3_decode")
+    ap.add_argument("--extras", default="dsv3_prefill,glm_decode,mixed_serving",
+                    help="comma-separated workloads timed after the headline one "
+                         "('none' to skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--portable", action="store_true",
                     help="force the portable CUDA-core attention kernels")
@@ -476,73 +556,54 @@ def main(argv=None):
     torch.cuda.set_device(device)
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
-    res = run_gpu_arm(args, rank, world, device)
+    from paged_latent_attention_cache_gb300 import build as _build
+    _build.build()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
+    peaks = load_peaks()
+    res = measure_workload(args, args.workload, rank, world, device, args.steps, args.warmup,
+                           flush)
+    extras = [] if args.extras in ("", "none") else \
+        [x for x in args.extras.split(",") if x and x != args.workload]
+    extra_res = {}
+    for name in extras:
+        k = min(args.steps, EXTRA_STEPS.get(name, args.steps))
+        r = measure_workload(args, name, rank, world, device, k, args.warmup, flush, e2e=False)
+        extra_res[name] = summary(r, peaks, world, args)
+        del r
+        torch.cuda.empty_cache()
     if rank == 0:
         w = res["w"]
-        hbm, bf16, bf16_sus, peak_src = load_peaks()
-        if w.num_decode_seqs:
-            dom, dom_ms = res["dec_work"], res["dec_ms"]
-            dom_name = "decode call (split-KV attention + combine)"
-        else:
-            dom, dom_ms = res["pre_work"], res["pre_ms"]
-            dom_name = "prefill call"
-        # The bound is whichever of HBM bytes and bf16 FLOPs takes longer at
-        # the measured peaks; a kernel that runs for more than ~100 ms of
-        # the timed loop is measured against the sustained tensor peak.
-        t_bytes = dom["bytes"] / (hbm * 1e9)
-        long_run = dom_ms * args.steps > 100.0
-        tpeak = bf16_sus if long_run else bf16
-        t_flops = dom["flops"] / (tpeak * 1e12)
-        traffic, traffic_kernel = ncu_traffic(w.name)
-        if t_flops > t_bytes:
-            achieved = dom["flops"] / (dom_ms * 1e-3) / 1e12
-            roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tpeak,
-                    "unit": "TFLOP/s", "frac": round(achieved / tpeak, 4),
-                    "peak_kind": "bf16 dense, " + ("sustained" if long_run else "burst")}
-        else:
-            achieved = dom["bytes"] / (dom_ms * 1e-3) / 1e9
-            roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm,
-                    "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                    "peak_kind": "HBM copy"}
-        roof.update({"traffic": traffic, "traffic_kernel": traffic_kernel,
-                     "alg_bytes": dom["bytes"], "alg_flops": dom["flops"],
-                     "kernel": dom_name, "kernel_ms": round(dom_ms, 5),
-                     "peak_source": peak_src})
+        head = summary(res, peaks, world, args)
         line = {
             "metric": METRIC,
-            "value": round(res["value"], 4),
+            "value": head["value"],
             "unit": UNIT,
             "n_gpus": world,
             "steps": args.steps,
             "warmup": max(args.warmup, 3),
-            "ms_per_step": round(res["ms_per_step"], 5),
+            "ms_per_step": head["ms_per_step"],
+            "step_ms": head["step_ms"],
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": {"torch.bfloat16": "bf16", "torch.float16": "f16"}[str(w.dtype)],
+            "dtype": head["config"]["dtype"],
             "data": "synthetic (seeded N(0,0.5^2) latent rows, shuffled block pool)",
-            "config": {"workload": w.name, "num_heads": w.num_heads,
-                       "head_size": w.head_size, "v_head_size": w.v_head_size,
-                       "rotary": [w.rotary_offset, w.rotary_dim], "block_size": w.block_size,
-                       "num_seqs": w.num_seqs, "num_tokens": w.num_tokens,
-                       "l2": "flushed before every step (write of 2x L2)",
-                       "timing": "CUDA graph of the step, CUDA events per replay",
-                       "parallelism": f"replicas x{world} (independent batches per rank)",
-                       "kernels": "portable" if args.portable else
-                       ("tcgen05" if res["family"][0] == 1 else "portable")},
-            "tflops": round(res["tflops"], 3),
-            "tokens_per_s": round(w.num_tokens * world / (res["ms_per_step"] * 1e-3), 1),
-            "phase_ms": {"write": round(res["write_ms"], 5), "decode": round(res["dec_ms"], 5),
-                         "prefill": round(res["pre_ms"], 5)},
-            "alg_bytes_per_step": res["work"]["bytes"],
-            "alg_flops_per_step": res["work"]["flops"],
-            "roofline": roof,
+            "config": head["config"],
+            "kernels": head["kernels"],
+            "tflops": head["tflops"],
+            "tokens_per_s": head["tokens_per_s"],
+            "phase_ms": head["phase_ms"],
+            "alg_bytes_per_step": head["alg_bytes_per_step"],
+            "alg_flops_per_step": head["alg_flops_per_step"],
+            "roofline": head["roofline"],
             "e2e": {"value": round(res["work"]["bytes"] * world / (res["e2e_ms"] * 1e-3) / 1e12,
                                4),
                     "unit": UNIT, "ms_per_step": round(res["e2e_ms"], 5),
                     "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": None if res["launches"] is None else res["launches"] * args.steps,
-            "clocks": res["clocks"],
+            "clocks": head["clocks"],
+            "extras": extra_res,
         }
         if world == 1:
             sec, work, n = time_oracle(w, args.cpu_budget)
@@ -565,7 +626,6 @@ def run_reference(args, rank, world):
     through the batch) after its write phase."""
     if rank != 0:
         return 0
-    import numpy as np
     w = build_workload(args.workload, 0)
     from oracle import pa_oracle as O
     from paged_latent_attention_cache_gb300 import workloads as W
@@ -581,10 +641,12 @@ def run_reference(args, rank, world):
     T = w.num_tokens
     # keep the whole run within a few minutes
     per_step_budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
+
     def one(t):
         out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
                                     past, bt, p)
         O.round_f64_to_bits(out, dt)
+
     for i in range(max(args.warmup, 3)):
         one(i % T)
     total_s, total_bytes, done = 0.0, 0, 0
@@ -592,8 +654,7 @@ def run_reference(args, rank, world):
         t = i % T
         t0 = time.perf_counter()
         one(t)
-        dt_s = time.perf_counter() - t0
-        total_s += dt_s
+        total_s += time.perf_counter() - t0
         total_bytes += algorithmic_work(w, tokens=[t], include_write=False)["bytes"]
         done += 1
         if total_s > per_step_budget * args.steps:
@@ -603,7 +664,7 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": done, "warmup": max(args.warmup, 3),
             "ms_per_step": 1e3 * total_s / done, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": W.dtype_tag(w.dtype), "data": "synthetic",
-            "config": {"workload": w.name},
+            "config": config_of(w, world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
                              "kind": "oracle",
                              "sample": "one token's read phase per step, cycling through the "
