@@ -308,12 +308,23 @@ def peaked(w: Workload, gain: float) -> Workload:
     return out
 
 
+def dsv3_prefill_small(seed: int = 6, dtype=torch.bfloat16) -> Workload:
+    """A quarter-size DeepSeek-V3-style chunked prefill (4 x 1024 new tokens
+    on pasts {0,0,512,512}, bs=128): the same kernel as dsv3_prefill with
+    about 1.2 GB on the device, small enough for a many-pass profiler
+    capture."""
+    w = dsv3_prefill(seed=seed, new_tokens=1024, pasts=(0, 0, 512, 512), dtype=dtype)
+    w.name = "dsv3_prefill_small"
+    return w
+
+
 WORKLOADS = {
     "tiny": tiny,
     "glm_decode": glm_decode,
     "dsv3_decode": dsv3_decode,
     "dsv3_prefill": dsv3_prefill,
     "mixed_serving": mixed_serving,
+    "dsv3_prefill_small": dsv3_prefill_small,
 }
 
 

@@ -5,7 +5,11 @@ Tolerances: cache rows written through RoPE within 1 ulp of the dtype
 (non-rotary channels and untouched rows bit-exact). Attention outputs meet
 two bounds against the oracle's float64 result:
 
-* the fixed bound max |err| <= 2e-3 (fp16) / 1.5e-2 (bf16);
+* the fixed bound max |err| <= 2e-3 (fp16) / 1.5e-2 (bf16), stated for
+  inputs with the configurations' spread (N(0, 0.5^2) queries); on the
+  peaked variants (queries scaled by 8 up to 2^17, logits of tens to
+  10^5) the 16-bit query operand alone moves scores by more than that bound
+  allows for O(1) outputs, and only the scale-aware bound applies;
 * per element, |err| <= K_REL * u * (|ref| + n_p + n_q + n_d), u the unit
   roundoff of the dtype (2^-8 bf16, 2^-11 fp16) and n_* the oracle's
   ``error_scales``: the output's sensitivity to rounding the probabilities
@@ -102,17 +106,23 @@ def output_bound(dtype, ref_f64: np.ndarray, scales: np.ndarray) -> np.ndarray:
 
 
 def check_out(w: W.Workload, got_bits: np.ndarray, ref_f64: np.ndarray, tokens=None,
-              scales=None):
+              scales=None, fixed_bound=None):
     """Both bounds of the module docstring (the scale-aware one when the
-    oracle's ``scales`` are given). Returns (max abs error, largest ratio of
-    an element's error to its scale-aware bound, or None)."""
+    oracle's ``scales`` are given; the fixed one unless the workload's query
+    was scaled, or ``fixed_bound`` says otherwise). Returns (max abs error,
+    largest ratio of an element's error to its scale-aware bound, or None)."""
     dt = W.dtype_tag(w.dtype)
     g = got_bits if tokens is None else got_bits[np.asarray(tokens)]
     gf = O.bits_to_f64(g, dt)
     assert np.isfinite(gf).all(), "non-finite output"
     err = np.abs(gf - ref_f64.reshape(gf.shape))
     tol = TOL[w.dtype]
-    assert err.max() <= tol, f"max abs error {err.max():.3e} > {tol}"
+    if fixed_bound is None:
+        fixed_bound = w.meta.get("query_gain", 1.0) == 1.0
+    if fixed_bound:
+        assert err.max() <= tol, f"max abs error {err.max():.3e} > {tol}"
+    else:
+        assert scales is not None, "a peaked workload needs the scale-aware bound"
     ratio = None
     if scales is not None:
         bound = output_bound(w.dtype, ref_f64, scales).reshape(err.shape)
