@@ -56,26 +56,35 @@ UNIT = "TB/s"
 # were taken on. Once those sources change the figure no longer describes
 # the kernel and the roofline reports null traffic until a new capture
 # replaces it.
-KERNEL_SOURCES = ("pa_tc.cu", "pa_tc_common.cuh", "pa_tc_pair.cu")
+KERNEL_SOURCES = {
+    "tc_attn_kernel": ("pa_tc.cu", "pa_tc_common.cuh"),
+    "tc_pair_kernel": ("pa_tc_pair.cu", "pa_tc_cluster.cuh", "pa_tc_common.cuh"),
+}
+# workload -> (kernel, bytes per launch, source digest, how the figure was taken)
 NCU_TRAFFIC = {
-    "glm_decode": ("tc_attn_kernel", 54255872, "e0f1913c268e7a95"),
-    "dsv3_decode": ("tc_pair_kernel", 314825216, "e0f1913c268e7a95"),
+    "dsv3_decode": ("tc_pair_kernel", 315302912, "6bfdcaeb45ee9672", "measured on this workload"),
+    # traffic grows with the tokens (query in, output out, each sequence's
+    # cache rows): the quarter-size capture times four
+    "dsv3_prefill": ("tc_pair_kernel", 4 * 1100012288, "6bfdcaeb45ee9672",
+                     "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
 }
 
 
-def kernel_source_digest() -> str:
+def kernel_source_digest(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, "paged_latent_attention_cache_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
+    """(bytes, kernel, note) of the dominant kernel's DRAM traffic per
+    launch, or Nones once its sources have changed since the capture."""
     entry = NCU_TRAFFIC.get(workload)
-    if entry is None or entry[2] != kernel_source_digest():
-        return None, None
-    return entry[1], entry[0]
+    if entry is None or entry[2] != kernel_source_digest(entry[0]):
+        return None, None, None
+    return entry[1], entry[0], entry[3]
 
 
 # ---------------------------------------------------------------------------
@@ -473,7 +482,7 @@ def roofline(res, peaks):
         dom_name = "prefill call"
     t_bytes = dom["bytes"] / (hbm * 1e9)
     t_flops = dom["flops"] / (bf16 * 1e12)
-    traffic, traffic_kernel = ncu_traffic(w.name)
+    traffic, traffic_kernel, traffic_note = ncu_traffic(w.name)
     if t_flops > t_bytes:
         achieved = dom["flops"] / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16,
@@ -487,6 +496,7 @@ def roofline(res, peaks):
                 "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "peak_kind": "HBM copy (of measured)"}
     roof.update({"traffic": traffic, "traffic_kernel": traffic_kernel,
+                 "traffic_source": traffic_note,
                  "alg_bytes": dom["bytes"], "alg_flops": dom["flops"],
                  "kernel": dom_name, "kernel_ms": round(dom_ms, 5),
                  "peak_source": peak_src})
