@@ -232,30 +232,31 @@ struct Params {
                      // the cache may be read before griddepcontrol.wait
   int tpc;           // prefill: consecutive tokens per work unit (rows = tpc * H <= 128)
   int own_slots;     // with early: the write touches no row below a sequence's past
+  // Accumulator layout: `groups` CTAs (or CTAs of a pair) each hold `vg`
+  // value channels of a head (vg a multiple of 64, groups * vg >= vhs).
+  int vg, groups;
+  // Single-CTA kernel geometry (pa_tc.cu), fixed per launch on the host:
+  int hs;            // latent width (channels hs..slabs*64 of the last slab read as zeros)
+  int slabs;         // 64-channel slabs per row: ceil(hs / 64)
+  int stages;        // key stages in the shared-memory ring (<= 8)
+  int stage_bytes;   // N * slabs * 128
+  int q_bytes;       // query rows * slabs * 128
+  int col_s, col_p;  // TMEM columns of the S and P buffers (O starts at column 0)
+  int tmem_cols;     // TMEM columns allocated (a power of two >= 32)
 };
 
-// QR = query rows kept in shared memory (128, or 64 when H <= 64: the M=128
-// MMA then reads rows 64-127 from the next slab, rows that are never stored).
-template <int HS, int VG, int G, int N, int STAGES, int QR, int NB>
-struct Cfg {
-  static constexpr int kBoxes = HS / 64;                  // 64-channel slabs
-  static constexpr int kQBytes = QR * HS * 2;
-  static constexpr int kQBox = QR * 128;                   // bytes per Q slab
-  static constexpr int kKBox = N * 128;                    // bytes per K slab
-  static constexpr int kStageBytes = N * HS * 2;
-  static constexpr int kSmemData = kQBytes + STAGES * kStageBytes;
-  // TMEM columns: O | S x NB | P x NB   (P is 16-bit: N/2 columns each);
-  // NB = 2 double-buffers S and P, NB = 1 leaves room for two CTAs per SM
-  static constexpr int kColO = 0;
-  static constexpr int kColS = VG;
-  static constexpr int kColP = VG + NB * N;
-  static constexpr int kCols = VG + NB * N + NB * N / 2;
-  static constexpr int kTmemCols = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
-                                   : kCols <= 256 ? 256 : 512;
-  static_assert(kCols <= 512, "TMEM budget");
-  static_assert(HS % 64 == 0 && VG % 64 == 0 && VG <= 256 && N % 32 == 0 && N <= 128, "shape");
-  static_assert(STAGES <= 8, "stages");
+// Compile-time part of a single-CTA kernel configuration: N keys per tile,
+// QR query rows kept in shared memory (128, or 64 when H <= 64: the M=128
+// MMA then reads rows 64-127 from the next slab, rows that are never
+// stored), NB S/P buffers in TMEM. The latent width, value channels and
+// stage count are per-launch values in Params.
+template <int N, int QR, int NB>
+struct Tile {
+  static constexpr int kQBox = QR * 128;  // bytes per query slab
+  static constexpr int kKBox = N * 128;   // bytes per key slab of a stage
+  static_assert(N % 32 == 0 && N <= 128, "key tile");
   static_assert(QR == 64 || QR == 128, "query rows");
+  static_assert(NB == 1 || NB == 2, "S/P buffers");
   // Warp roles: 0-3 softmax; producer and MMA issuer on warps 4 and 5, or,
   // with 64 query rows (only softmax warps 0 and 1 hold rows), on warps 6
   // and 7, which share no scheduler partition (warp % 4) with a live
@@ -263,7 +264,6 @@ struct Cfg {
   static constexpr int kProdWarp = QR == 64 ? 6 : 4;
   static constexpr int kMmaWarp = kProdWarp + 1;
   static constexpr int kThreads = 32 * (kMmaWarp + 1);
-  static_assert(NB == 1 || NB == 2, "S/P buffers");
 };
 
 struct Barriers {
@@ -639,25 +639,30 @@ __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, in
 //   O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  M = max_s m_s
 // (log2-domain maxima, unnormalised partial outputs). A NaN partial maximum
 // marks a split that read an invalid block: the row becomes zeros, as does a
-// row that saw no key (sum = 0). Thread = CPT consecutive channels of one
-// head; each thread issues the loads of a round of splits together and folds
-// them with a running maximum, so the merge costs the plan load plus one
-// round trip per round of splits.
-template <typename T, int VG, int G, int CPT>
+// row that saw no key (sum = 0). Thread = CPT consecutive accumulator
+// channels of one head (groups * vg channels, of which the first vhs are
+// stored); each thread issues the loads of a round of splits together and
+// folds them with a running maximum, so the merge costs the plan load plus
+// one round trip per round of splits. VGF, GF > 0 fix vg and groups at
+// compile time (the 192/128 and 576/512 shapes), 0 takes them from Params.
+template <typename T, int CPT, int VGF, int GF>
 __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__ Params P) {
   grid_dep_wait();  // the attention kernel's partials are complete and visible
-  constexpr int kTPH = G * VG / CPT;         // threads per head
-  constexpr int kHPB = 256 / kTPH;           // heads per CTA
   constexpr int kRound = CPT >= 16 ? 4 : 8;  // splits whose loads are in flight together
-  static_assert(CPT % 4 == 0 && 256 % kTPH == 0, "combine shape");
+  static_assert(CPT % 4 == 0, "combine shape");
+  const int vg = VGF ? VGF : P.vg, groups = GF ? GF : P.groups;
+  const int tph = groups * vg / CPT;         // threads per head
+  const int hpb = 256 / tph;                 // heads per CTA
+  const int hl = (int)threadIdx.x / tph;
+  if (hl >= hpb) return;
   const int x = blockIdx.x;
-  const int h = blockIdx.y * kHPB + (int)threadIdx.x / kTPH;
-  const int c0 = ((int)threadIdx.x % kTPH) * CPT;  // channel in [0, G*VG)
-  const int g = c0 / VG, cc = c0 - g * VG;
+  const int h = blockIdx.y * hpb + hl;
+  const int c0 = ((int)threadIdx.x % tph) * CPT;  // channel in [0, groups*vg)
+  const int g = c0 / vg, cc = c0 - g * vg;
   const int2 plan = P.ws_plan[x];
   const int32_t q0 = P.cumseq[P.seq_begin + x];
   const int S = plan.y;
-  if (S > 1 && h < P.H) {  // (one split: the attention kernel wrote the output)
+  if (S > 1 && h < P.H && c0 < P.vhs) {  // (one split: the attention kernel wrote the output)
     float M = -INFINITY, L = 0.f, o[CPT];
 #pragma unroll
     for (int e = 0; e < CPT; ++e) o[e] = 0.f;
@@ -668,9 +673,9 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
 #pragma unroll
       for (int i = 0; i < kRound; ++i) {
         if (s0 + i < S) {
-          const int64_t slot = ((int64_t)(plan.x + s0 + i) * G + g) * kRows + h;
+          const int64_t slot = ((int64_t)(plan.x + s0 + i) * groups + g) * kRows + h;
           ml[i] = reinterpret_cast<const float2*>(P.ws_ml)[slot];
-          const float4* src = reinterpret_cast<const float4*>(P.ws_o + slot * VG + cc);
+          const float4* src = reinterpret_cast<const float4*>(P.ws_o + slot * vg + cc);
 #pragma unroll
           for (int q = 0; q < CPT / 4; ++q) ov[i][q] = src[q];
         }
@@ -700,27 +705,26 @@ __global__ void __launch_bounds__(256) tc_combine_kernel(const __grid_constant__
       }
     }
     const float inv = (L > 0.f && !bad) ? 1.f / L : 0.f;
-    uint32_t pk[CPT / 2];
+    T* dst = reinterpret_cast<T*>(P.out) + ((int64_t)q0 * P.H + h) * P.vhs + c0;
+    if (c0 + CPT <= P.vhs && P.vhs % 8 == 0) {  // whole, aligned vectors
+      uint32_t pk[CPT / 2];
 #pragma unroll
-    for (int e = 0; e < CPT / 2; ++e) pk[e] = pack2<T>(o[2 * e] * inv, o[2 * e + 1] * inv);
-    T* dst = reinterpret_cast<T*>(P.out) + ((int64_t)q0 * P.H + h) * P.vhs + g * VG + cc;
-    if (CPT == 4) {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+      for (int e = 0; e < CPT / 2; ++e) pk[e] = pack2<T>(o[2 * e] * inv, o[2 * e + 1] * inv);
+      if (CPT == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < CPT / 8; ++q)
+          reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                                                        pk[4 * q + 3]);
+      }
     } else {
 #pragma unroll
-      for (int q = 0; q < CPT / 8; ++q)
-        reinterpret_cast<uint4*>(dst)[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
-                                                      pk[4 * q + 3]);
+      for (int e = 0; e < CPT; ++e)
+        if (c0 + e < P.vhs) dst[e] = Half<T>::from_f32(o[e] * inv);
     }
   }
 }
-
-// Combine launch shape: CPT channels per thread, heads per CTA.
-template <int VG, int G>
-struct CombineShape {
-  static constexpr int kCPT = G * VG >= 512 ? 16 : 4;
-  static constexpr int kHPB = 256 / (G * VG / kCPT);
-};
 
 // ---------------------------------------------------------------------------
 // Host-side helpers
@@ -745,8 +749,12 @@ inline EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// A read-phase configuration chosen on the host: value channels per CTA
+// (vg) and CTAs per head group (groups), the key tile (n), stage count,
+// query rows kept (qr), S/P buffers (nb); pair = the 576/512 CTA-pair kernel.
 struct Shape {
   int hs, vg, groups, n, stages, qr, nb;
+  bool pair;
 };
 
 // Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
@@ -776,6 +784,21 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Split combine of a decode call over nq sequences, launched after the
+// attention kernel with programmatic dependent launch.
+template <typename T>
+cudaError_t launch_combine(const Params& P, int H, int64_t nq, cudaStream_t st) {
+  const int cpt = P.groups * P.vg >= 512 ? 16 : 4;
+  const int hpb = 256 / (P.groups * P.vg / cpt);
+  const dim3 grid((unsigned)nq, (unsigned)((H + hpb - 1) / hpb));
+  if (P.vg == 128 && P.groups == 1)
+    return launch_pdl(tc_combine_kernel<T, 4, 128, 1>, grid, dim3(256), 0, st, P);
+  if (P.vg == 256 && P.groups == 2)
+    return launch_pdl(tc_combine_kernel<T, 16, 256, 2>, grid, dim3(256), 0, st, P);
+  return cpt == 16 ? launch_pdl(tc_combine_kernel<T, 16, 0, 0>, grid, dim3(256), 0, st, P)
+                   : launch_pdl(tc_combine_kernel<T, 4, 0, 0>, grid, dim3(256), 0, st, P);
 }
 
 // CTA-pair kernel for the 576/512 geometry (pa_tc_pair.cu).

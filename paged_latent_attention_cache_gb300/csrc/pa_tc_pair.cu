@@ -722,10 +722,7 @@ cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& 
   e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem, a.stream, map, qmap,
                  qmap64, P);
   if (e != cudaSuccess || ph != Phase::kDecode) return e;
-  return launch_pdl(tc_combine_kernel<T, 256, 2, CombineShape<256, 2>::kCPT>,
-                    dim3((unsigned)nq, (unsigned)((g.H + CombineShape<256, 2>::kHPB - 1) /
-                                                  CombineShape<256, 2>::kHPB)),
-                    dim3(256), 0, a.stream, P);
+  return launch_combine<T>(P, g.H, nq, a.stream);
 }
 
 template cudaError_t launch_pair<__nv_bfloat16>(const Geometry&, Phase, const ReadArgs&, Params&,

@@ -11,8 +11,13 @@ from tests import harness as Hn
 pytestmark = pytest.mark.gpu
 
 
-def _check(w, portable=False, tokens=None, default_scale=False):
+def _check(w, portable=False, tokens=None, default_scale=False, family=None):
+    """Runs w through the C ABI and checks it against the oracle; ``family``
+    (when given) is the kernel family both read phases must use (1 =
+    tcgen05 tensor cores, 0 = portable CUDA cores)."""
     got = Hn.run_gpu(w, portable=portable, scale=0.0 if default_scale else None)
+    if family is not None:
+        assert (got["op"].kernel_family(0), got["op"].kernel_family(1)) == (family, family)
     ref = Hn.run_oracle(w, tokens)
     assert got["flags"] == 0, hex(got["flags"])
     Hn.check_cache(w, got["cache"], ref["cache"])
@@ -35,6 +40,7 @@ VARIANTS = {
     "softcap_3": dict(softcap=3.0),
     "softcap_tight": dict(softcap=0.5, scale=0.3),
     "fp16": dict(dtype=torch.float16),
+    "fp16_no_rotary": dict(dtype=torch.float16, rotary_dim=0, rotary_offset=0),
     "rotary_at_0": dict(rotary_offset=0, rotary_dim=32),
 }
 
@@ -46,16 +52,35 @@ def test_variant(name, portable):
     kw.update(VARIANTS[name])
     default_scale = kw.pop("scale", None) == 0.0
     w = W.make_workload(name, q_lens=[1, 1, 9, 0, 33], past_lens=[70, 0, 40, 5, 3], **kw)
-    _check(w, portable, default_scale=default_scale)
+    _check(w, portable, default_scale=default_scale, family=0 if portable else 1)
 
 
-@pytest.mark.parametrize("hs,vhs,ro,rd,H", [(64, 64, 0, 0, 2), (576, 512, 512, 64, 16),
-                                            (256, 200, 128, 128, 3), (1024, 512, 960, 64, 2)])
-def test_geometries(hs, vhs, ro, rd, H):
+@pytest.mark.parametrize("hs,vhs,ro,rd,H,family", [
+    (64, 64, 0, 0, 2, 1), (576, 512, 512, 64, 16, 1), (256, 200, 128, 128, 3, 1),
+    (1024, 512, 960, 64, 2, 0), (128, 128, 64, 64, 100, 1), (80, 48, 16, 64, 5, 1),
+    (256, 256, 0, 64, 128, 1), (160, 1, 96, 64, 7, 1), (208, 136, 0, 0, 64, 1)])
+def test_geometries(hs, vhs, ro, rd, H, family):
+    """Latent widths up to 256 (multiples of 16; a last 64-channel slab may be
+    partial) and any value width up to the latent width run on the
+    tensor-core kernels, as does 576/512; wider latents use the portable
+    kernels. Decode and prefill tokens, heads up to 128."""
     w = W.make_workload("geo", q_lens=[1, 17], past_lens=[100, 30], num_heads=H, head_size=hs,
                         v_head_size=vhs, rotary_offset=ro, rotary_dim=rd, block_size=16,
                         seed=22, scale=0.08)
-    _check(w)
+    _check(w, family=family)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+@pytest.mark.parametrize("hs", [64, 128, 192, 256])
+def test_vhs_equal_hs_default_scale(hs, dtype):
+    """v_head_size == head_size with the default scale 1/sqrt(head_size)
+    (the rule of paged_attention.rs execute: an explicit scale is required
+    only when v_head_size != head_size), on the tensor-core kernels, over a
+    long decode (several key splits) and a prefill chunk."""
+    w = W.make_workload("vhs_eq_hs", q_lens=[1, 1, 40], past_lens=[3000, 64, 100], num_heads=16,
+                        head_size=hs, v_head_size=hs, rotary_offset=hs - 64, rotary_dim=64,
+                        block_size=64, seed=27, dtype=dtype)
+    _check(w, default_scale=True, family=1)
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
