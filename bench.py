@@ -57,7 +57,7 @@ UNIT = "TB/s"
 # the kernel and the roofline reports null traffic until a new capture
 # replaces it.
 KERNEL_SOURCES = {
-    "tc_attn_kernel": ("pa_tc.cu", "pa_tc_common.cuh"),
+    "tc_attn_kernel": ("pa_tc_attn.cuh", "pa_tc_common.cuh"),
     "tc_pair_kernel": ("pa_tc_pair.cu", "pa_tc_cluster.cuh", "pa_tc_common.cuh"),
 }
 # workload -> (kernel, bytes per launch, source digest, how the figure was taken)

@@ -101,6 +101,57 @@ def round_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     return bits_to_f64(round_f64_to_bits(x, dtype), dtype)
 
 
+# FP8 cache format: OCP FP8 E4M3 ("e4m3fn"): sign, 4 exponent bits with bias
+# 7, 3 mantissa bits; exponent field 0 holds the subnormals m * 2^-9; codes
+# 0x7F and 0xFF are NaN (there are no infinities), so the largest finite
+# value is 1.75 * 2^8 = 448.
+E4M3 = "e4m3"
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact values of E4M3 codes (uint8)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.ldexp(1.0, e - 7))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return sign * mag
+
+
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes of float64 values: round to nearest, ties to even,
+    saturating to +-448 (values of magnitude 448 or more give the largest
+    finite code); a value that rounds to zero keeps its sign (0x80 for a
+    negative one)."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.minimum(np.abs(x), E4M3_MAX)
+    with np.errstate(divide="ignore"):
+        _, ex = np.frexp(ax)                       # ax = f * 2^ex, f in [0.5, 1)
+    e = np.maximum(ex.astype(np.int64) - 1, -6)    # unbiased exponent, subnormals at -6
+    spacing = np.ldexp(1.0, e - 3)
+    r = np.minimum(np.rint(ax / spacing) * spacing, E4M3_MAX)
+    # code of the rounded magnitude r
+    with np.errstate(divide="ignore"):
+        _, er = np.frexp(r)
+    er = er.astype(np.int64) - 1
+    normal = r >= 2.0 ** -6
+    ef = np.where(normal, er + 7, 0)
+    mf = np.where(normal, np.rint((r / np.ldexp(1.0, er) - 1.0) * 8.0), np.rint(r / 2.0 ** -9))
+    code = (ef << 3) | mf.astype(np.int64)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    return code.astype(np.uint8)
+
+
+def quantize_e4m3(row: np.ndarray, k_scale: float) -> np.ndarray:
+    """E4M3 codes of a cache row: each channel's value rounded to float32,
+    divided by k_scale in float32 (IEEE division), then rounded to E4M3."""
+    v32 = np.asarray(row, dtype=np.float64).astype(np.float32)
+    q32 = v32 / np.float32(k_scale)
+    return round_to_e4m3(q32.astype(np.float64))
+
+
 # ---------------------------------------------------------------------------
 # Token location and RoPE
 # ---------------------------------------------------------------------------
@@ -173,6 +224,26 @@ class F64Cache:
 
     def put(self, slot: int, row: np.ndarray):
         self.rows[slot] = row
+
+
+class E4M3Cache:
+    """Cache rows held as E4M3 codes with one scale for the whole cache: a
+    store quantizes the float64 row (``quantize_e4m3``), a load returns the
+    code's value times k_scale (exact in float64)."""
+
+    def __init__(self, codes: np.ndarray, k_scale: float):
+        self.codes = np.array(codes, dtype=np.uint8, copy=True)
+        self.k_scale = float(k_scale)
+
+    @property
+    def num_rows(self) -> int:
+        return self.codes.shape[0]
+
+    def get(self, idx) -> np.ndarray:
+        return e4m3_to_f64(self.codes[idx]) * self.k_scale
+
+    def put(self, slot: int, row: np.ndarray):
+        self.codes[slot] = quantize_e4m3(row, self.k_scale)
 
 
 class BitsCache:
@@ -347,14 +418,19 @@ def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cums
 
     Shapes: query ``[T, H*hs]``, key ``[T, hs]``, cache
     ``[num_blocks, bs, 1, hs]`` (any shape with hs last), cos/sin
-    ``[rows, rd/2]``. The read phase sees the cache after the write.
+    ``[rows, rd/2]``. The read phase sees the cache after the write. With
+    ``p["cache_dtype"] == "e4m3"`` the cache holds uint8 E4M3 codes scaled
+    by ``p["k_scale"]`` (returned as codes).
     Returns (new cache bits in the input's shape, output bits
     ``[len(tokens), H*vhs]``, output float64 before rounding); with
     ``stats`` a fourth item, the ``error_scales`` ``[len(tokens), 3, H*vhs]``."""
     dt = p["dtype"]
     hs, _ = _check_geometry(p)
     shape = cache_bits.shape
-    cache = BitsCache(np.asarray(cache_bits).reshape(-1, hs), dt)
+    if p.get("cache_dtype") == E4M3:
+        cache = E4M3Cache(np.asarray(cache_bits).reshape(-1, hs), p["k_scale"])
+    else:
+        cache = BitsCache(np.asarray(cache_bits).reshape(-1, hs), dt)
     cos_tab = bits_to_f64(cos_bits, dt)
     sin_tab = bits_to_f64(sin_bits, dt)
     latent_write(lambda t: bits_to_f64(key_bits[t], dt), cos_tab, sin_tab,
@@ -363,7 +439,8 @@ def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cums
                         cumseq, past, block_table, p, tokens, stats)
     out = res[0] if stats else res
     out = out.reshape(out.shape[0], -1)
+    stored = cache.codes if isinstance(cache, E4M3Cache) else cache.bits
     if not stats:
-        return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out
+        return stored.reshape(shape), round_f64_to_bits(out, dt), out
     sc = res[1].reshape(out.shape[0], 3, -1)
-    return cache.bits.reshape(shape), round_f64_to_bits(out, dt), out, sc
+    return stored.reshape(shape), round_f64_to_bits(out, dt), out, sc

@@ -13,7 +13,8 @@ states it (schema input list in the PR #1978 review, "ORT v1.29 schema"):
 
 * ``query``        ``[T, H*hs]``            f16/bf16
 * ``key``          ``[T, hs]``              latent rows, same dtype
-* ``key_cache``    ``[num_blocks, bs, 1, hs]`` paged latent cache
+* ``key_cache``    ``[num_blocks, bs, 1, hs]`` paged latent cache, in the
+  query dtype, or uint8 E4M3 codes with one ``k_scale`` for an FP8 cache
 * ``cumseq``       int32 ``[B+1]``           ``cumulative_sequence_length``
 * ``past``         int32 ``[B]``             ``past_seqlens`` (context - q_len)
 * ``block_table``  int32 ``[B, max_blocks]`` physical block per logical block,
@@ -66,6 +67,8 @@ class Workload:
     block_table: torch.Tensor
     slot_mapping: torch.Tensor
     meta: Dict[str, object] = field(default_factory=dict)
+    cache_dtype: Optional[str] = None   # None: the query dtype; "e4m3": FP8 codes
+    k_scale: float = 1.0                # FP8 cache: value = code * k_scale
 
     @property
     def num_tokens(self) -> int:
@@ -83,7 +86,8 @@ class Workload:
             cos_rows=self.cos_rows, block_size=self.block_size,
             num_blocks=self.num_blocks, max_blocks_per_seq=self.max_blocks_per_seq,
             scale=self.scale, softcap=self.softcap,
-            local_window_size=self.local_window_size)
+            local_window_size=self.local_window_size, cache_dtype=self.cache_dtype,
+            k_scale=self.k_scale)
 
     def to(self, device) -> "Workload":
         out = Workload(**{k: getattr(self, k) for k in self.__dataclass_fields__})
@@ -106,6 +110,20 @@ def _normal(shape, gen: torch.Generator, std: float, dtype: torch.dtype,
         hi = min(n, lo + chunk)
         out[lo:hi] = (torch.randn(hi - lo, generator=gen) * std).to(dtype)
     return out.view(*shape)
+
+
+def _e4m3_codes(shape, gen: torch.Generator) -> torch.Tensor:
+    """Seeded E4M3 cache contents (uint8 codes, drawn directly as bit
+    fields): random sign, exponent field uniform in 8..13 (magnitudes 2 to
+    120, about what N(0, 0.5^2) rows divided by k_scale = 1/64 span) and a
+    random 3-bit mantissa. No code is NaN."""
+    n = 1
+    for s in shape:
+        n *= int(s)
+    sign = torch.randint(0, 2, (n,), generator=gen, dtype=torch.int32) << 7
+    exp = torch.randint(8, 14, (n,), generator=gen, dtype=torch.int32) << 3
+    man = torch.randint(0, 8, (n,), generator=gen, dtype=torch.int32)
+    return (sign | exp | man).to(torch.uint8).view(*shape)
 
 
 def rope_tables(cos_rows: int, rotary_dim: int, dtype: torch.dtype,
@@ -133,15 +151,20 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
                   seed: int = 0, std: float = 0.5, query_gain: float = 1.0,
                   drop_slots: int = 0, drop_frac: float = 0.0,
                   num_decode_seqs: Optional[int] = None,
-                  block_table_shape: Optional[Sequence[int]] = None) -> Workload:
+                  block_table_shape: Optional[Sequence[int]] = None,
+                  cache_dtype: Optional[str] = None, k_scale: float = 1.0 / 64) -> Workload:
     """Draw one seeded batch.
 
     ``drop_slots`` / ``drop_frac`` set that many (or that fraction of) seeded
     slot_mapping entries to -1. ``query_gain`` multiplies the drawn query
     (a power of two keeps the scaling exact) so that the logits spread over
-    tens or hundreds and the softmax is peaked instead of near-uniform. ``block_table_shape`` lets a caller ask for a
-    block table that is literally a permutation of the whole pool reshaped
-    (the tiny configuration's wording)."""
+    tens or hundreds and the softmax is peaked instead of near-uniform.
+    ``block_table_shape`` lets a caller ask for a block table that is
+    literally a permutation of the whole pool reshaped (the tiny
+    configuration's wording). ``cache_dtype="e4m3"`` makes the cache an FP8
+    one: the pool holds seeded E4M3 codes (``_e4m3_codes``) with one
+    ``k_scale``; the keys stay in the query dtype (the write phase quantizes
+    them)."""
     assert len(q_lens) == len(past_lens)
     gen = torch.Generator().manual_seed(seed)
     B = len(q_lens)
@@ -195,7 +218,11 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
     if query_gain != 1.0:
         query = (query.float() * query_gain).to(dtype)
     key = _normal((T, head_size), gen, std, dtype)
-    key_cache = _normal((num_blocks, block_size, 1, head_size), gen, std, dtype)
+    if cache_dtype == "e4m3":
+        key_cache = _e4m3_codes((num_blocks, block_size, 1, head_size), gen)
+    else:
+        assert cache_dtype is None, cache_dtype
+        key_cache = _normal((num_blocks, block_size, 1, head_size), gen, std, dtype)
     cos, sin = rope_tables(cos_rows, rotary_dim, dtype)
     if num_decode_seqs is None:
         num_decode_seqs = 0
@@ -214,7 +241,9 @@ def make_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
                     num_decode_seqs=int(num_decode_seqs), query=query, key=key,
                     key_cache=key_cache, cos_cache=cos, sin_cache=sin, cumseq=cumseq,
                     past=past, block_table=block_table, slot_mapping=slot,
-                    meta=dict(seed=seed, std=std, query_gain=query_gain))
+                    meta=dict(seed=seed, std=std, query_gain=query_gain),
+                    cache_dtype=cache_dtype,
+                    k_scale=float(k_scale) if cache_dtype is not None else 1.0)
 
 
 # ---------------------------------------------------------------------------
@@ -318,6 +347,26 @@ def dsv3_prefill_small(seed: int = 6, dtype=torch.bfloat16) -> Workload:
     return w
 
 
+def glm_decode_fp8(seed: int = 7, batch: int = 32) -> Workload:
+    """glm_decode's shape (contexts uniform in [1024, 8192]) with an FP8
+    (E4M3) latent cache, k_scale = 1/64."""
+    g = torch.Generator().manual_seed(seed * 7919 + 1)
+    ctx = torch.randint(1024, 8193, (batch,), generator=g).tolist()
+    return make_workload("glm_decode_fp8", q_lens=[1] * batch, past_lens=[c - 1 for c in ctx],
+                         num_heads=64, **GLM, block_size=64, num_blocks=8192,
+                         max_blocks_per_seq=128, cos_rows=8192, scale=1.0 / math.sqrt(192.0),
+                         seed=seed, cache_dtype="e4m3")
+
+
+def dsv3_decode_fp8(seed: int = 8, batch: int = 64, context: int = 4096) -> Workload:
+    """dsv3_decode's shape with an FP8 (E4M3) latent cache, k_scale = 1/64."""
+    nb = batch * ((context + 63) // 64)
+    return make_workload("dsv3_decode_fp8", q_lens=[1] * batch,
+                         past_lens=[context - 1] * batch, num_heads=128, **DSV3,
+                         block_size=64, num_blocks=nb, max_blocks_per_seq=(context + 63) // 64,
+                         cos_rows=context, scale=DSV3_SCALE, seed=seed, cache_dtype="e4m3")
+
+
 WORKLOADS = {
     "tiny": tiny,
     "glm_decode": glm_decode,
@@ -325,13 +374,18 @@ WORKLOADS = {
     "dsv3_prefill": dsv3_prefill,
     "mixed_serving": mixed_serving,
     "dsv3_prefill_small": dsv3_prefill_small,
+    "glm_decode_fp8": glm_decode_fp8,
+    "dsv3_decode_fp8": dsv3_decode_fp8,
 }
 
 
 def to_bits(t: torch.Tensor):
-    """uint16 numpy view of a bf16/f16 tensor's bit patterns (a copy on the
-    host when the tensor lives on a device)."""
+    """uint16 numpy view of a bf16/f16 tensor's bit patterns, or the uint8
+    codes of an FP8 cache (a copy on the host when the tensor lives on a
+    device)."""
     import numpy as np
+    if t.dtype == torch.uint8:
+        return t.detach().contiguous().cpu().numpy()
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
@@ -343,4 +397,6 @@ def oracle_params(w: "Workload") -> Dict[str, object]:
     """The workload's operator parameters with the dtype as a tag string."""
     p = w.params()
     p["dtype"] = dtype_tag(w.dtype)
+    if w.cache_dtype is None:
+        p.pop("k_scale")
     return p

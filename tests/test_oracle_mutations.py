@@ -35,6 +35,14 @@ MUTANTS = {
     "scales_score_centre_dropped": ("var_a = (a @ V2) - 2.0 * out * (a @ V)",
                                     "var_a = (a @ V2) - 0.0 * out * (a @ V)"),
     "scales_diag_wrong_channel": ("np.abs(q[:, :vhs])", "np.abs(q[:, -vhs:])"),
+    "e4m3_bias_8": ("np.ldexp(1.0, e - 7)", "np.ldexp(1.0, e - 8)"),
+    "e4m3_subnormal_scale": ("np.where(e == 0, m * 2.0 ** -9,", "np.where(e == 0, m * 2.0 ** -10,"),
+    "e4m3_truncates": ("r = np.minimum(np.rint(ax / spacing) * spacing, E4M3_MAX)",
+                       "r = np.minimum(np.floor(ax / spacing) * spacing, E4M3_MAX)"),
+    "e4m3_saturates_too_high": ("E4M3_MAX = 448.0", "E4M3_MAX = 480.0"),
+    "fp8_read_unscaled": ("return e4m3_to_f64(self.codes[idx]) * self.k_scale",
+                          "return e4m3_to_f64(self.codes[idx])"),
+    "fp8_multiplies": ("q32 = v32 / np.float32(k_scale)", "q32 = v32 * np.float32(k_scale)"),
 }
 
 PINS = [
@@ -54,6 +62,12 @@ PINS = [
     lambda: pins.test_error_scales_probability_term_monte_carlo(),
     lambda: pins.test_error_scales_score_term_monte_carlo(),
     lambda: pins.test_error_scales_diagonal_term_is_a_derivative(),
+    lambda: pins.test_e4m3_decode_matches_torch(),
+    lambda: pins.test_e4m3_rounding_matches_torch_cast_in_range(),
+    lambda: pins.test_e4m3_saturates_to_448(),
+    lambda: pins.test_fp8_write_is_exact_for_representable_rows(),
+    lambda: pins.test_fp8_read_equals_plain_read_of_dequantized_cache(),
+    lambda: pins.test_fp8_quantization_divides_by_k_scale_in_float32(),
 ]
 
 

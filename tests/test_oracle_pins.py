@@ -580,3 +580,114 @@ def test_stats_leave_the_result_unchanged():
     out, sc = O.latent_attend(q, *args, stats=True)
     assert np.array_equal(plain, out)
     assert sc.shape == (w.num_tokens, 3, w.num_heads, w.v_head_size) and (sc >= 0).all()
+
+
+# ---------------------------------------------------------------------------
+# FP8 (E4M3) latent cache
+# ---------------------------------------------------------------------------
+
+def test_e4m3_decode_matches_torch():
+    """All 256 codes decode to torch's float8_e4m3fn values (NaN codes too)."""
+    codes = np.arange(256, dtype=np.uint8)
+    ours = O.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+
+
+def test_e4m3_rounding_matches_torch_cast_in_range():
+    """float32 inputs up to the saturation point: the codes equal torch's
+    float32 -> float8_e4m3fn cast (round to nearest, ties to even),
+    including exact ties and subnormals."""
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(20000) * 20, rng.standard_normal(5000) * 1e-2,
+                        rng.uniform(-464, 464, 5000)])
+    vals = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    vals = np.sort(vals[np.isfinite(vals)])
+    mids = (vals[1:] + vals[:-1]) / 2                     # exact ties
+    x = np.concatenate([x, mids, -mids, [0.0, -0.0, 464.0, -464.0]]).astype(np.float32)
+    ours = O.round_to_e4m3(x.astype(np.float64))
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_rounding_is_nearest_by_brute_force():
+    """Each code is the finite E4M3 value nearest to x (ties: even mantissa),
+    found by comparing against all 254 finite values."""
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.standard_normal(3000) * 30, rng.standard_normal(1000) * 0.01])
+    codes = np.arange(256, dtype=np.uint8)
+    vals = O.e4m3_to_f64(codes)
+    fin = np.isfinite(vals)
+    got = O.round_to_e4m3(x)
+    for xi, ci in zip(x, got):
+        d = np.abs(vals[fin] - xi)
+        best = codes[fin][d == d.min()]
+        if len(best) > 1:   # a tie: the even mantissa wins; the sign follows x
+            best = best[(best & 1) == 0]
+        best = best[np.signbit(O.e4m3_to_f64(best)) == np.signbit(xi)] if len(best) > 1 else best
+        assert O.e4m3_to_f64(np.array([ci]))[0] == O.e4m3_to_f64(best[:1])[0], (xi, ci, best)
+
+
+def test_e4m3_saturates_to_448():
+    """Magnitudes at or beyond 448 give the largest finite code, 0x7E (448)
+    or 0xFE (-448); nothing becomes NaN."""
+    x = np.array([448.0, 460.0, 464.0, 465.0, 1e6, 3e38, -465.0, -1e30])
+    codes = O.round_to_e4m3(x)
+    assert codes.tolist() == [0x7E] * 6 + [0xFE] * 2
+
+
+def test_fp8_write_is_exact_for_representable_rows():
+    """Without rotation, a key row whose values are k_scale times E4M3
+    values is stored as exactly those codes."""
+    rng = np.random.default_rng(13)
+    k_scale = 2.0 ** -6
+    codes = rng.integers(0, 256, size=(3, 32)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x11                      # no NaN codes
+    rows = O.e4m3_to_f64(codes) * k_scale
+    p = _params(rotary_dim=0, rotary_offset=0, cache_dtype=O.E4M3, k_scale=k_scale)
+    cache = O.E4M3Cache(np.zeros((8 * 16, 32), np.uint8), k_scale)
+    cumseq, past = np.array([0, 3]), np.array([0])
+    O.latent_write(rows, None, None, np.array([5, 17, 40]), cumseq, past, cache, p)
+    assert np.array_equal(cache.codes[[5, 17, 40]], codes)
+
+
+def test_fp8_read_equals_plain_read_of_dequantized_cache():
+    """The FP8 operator equals the plain operator run on a cache holding the
+    dequantized values (exact in bf16 for k_scale = 2^-6): dequantization is
+    code * k_scale and nothing else changes in the read phase."""
+    rng = np.random.default_rng(14)
+    k_scale = 2.0 ** -6
+    codes = (rng.integers(0, 2, (8 * 16, 32)) << 7 | rng.integers(8, 14, (8 * 16, 32)) << 3 |
+             rng.integers(0, 8, (8 * 16, 32))).astype(np.uint8)
+    T, H = 5, 2
+    q = rng.standard_normal((T, H * 32)) * 0.5
+    cumseq, past = np.array([0, 2, 5]), np.array([17, 30])
+    bt = rng.permutation(8).reshape(2, 4)
+    cos_t, sin_t, _ = _exact_tables(64, 16)
+    p8 = _params(cache_dtype=O.E4M3, k_scale=k_scale)
+    pb = _params()
+    fp8 = O.latent_attend(q, O.E4M3Cache(codes, k_scale), cos_t, sin_t, cumseq, past, bt, p8)
+    plain = O.latent_attend(q, O.F64Cache(O.e4m3_to_f64(codes) * k_scale), cos_t, sin_t, cumseq,
+                            past, bt, pb)
+    assert np.array_equal(fp8, plain)
+    # and the dequantized values are bf16 values (a bf16 cache would hold them exactly)
+    vals = O.e4m3_to_f64(codes) * k_scale
+    assert np.array_equal(O.round_f64(vals, "bf16"), vals)
+
+
+def test_fp8_quantization_divides_by_k_scale_in_float32():
+    """The stored code of value v is round_to_e4m3(f32(f32(v) / f32(k_scale)))."""
+    rng = np.random.default_rng(15)
+    v = rng.standard_normal(4000) * 0.5
+    k = 0.0123
+    got = O.quantize_e4m3(v, k)
+    q = (v.astype(np.float32) / np.float32(k)).astype(np.float64)
+    vals = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    # the decoded code is within half a spacing of f32(v)/k (nearest value)
+    dec = O.e4m3_to_f64(got)
+    spacing = np.ldexp(1.0, (np.maximum(np.floor(np.log2(np.abs(q) + 1e-300)), -6) - 3)
+                       .astype(np.int64))
+    assert np.all(np.abs(dec - q) <= spacing / 2 + 1e-12)
+    assert np.isfinite(vals[got]).all()
