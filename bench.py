@@ -96,8 +96,10 @@ def algorithmic_work(w, seqs=None, tokens=None, include_write=True):
     row a sequence's queries can see once, plus Q, O, the cos/sin rows, the
     block-table entries, the key rows read and the cache rows written.
     FLOPs = (2*hs + 2*vhs) per (visible key, head). ``seqs`` restricts the
-    read phase to those sequences, ``tokens`` to those tokens."""
+    read phase to those sequences, ``tokens`` to those tokens. A cache row is
+    hs bytes in an FP8 cache, 2*hs otherwise."""
     el = 2
+    el_c = 1 if getattr(w, "cache_dtype", None) == "e4m3" else 2
     H, hs, vhs, bs = w.num_heads, w.head_size, w.v_head_size, w.block_size
     win = w.local_window_size
     cs = w.cumseq.tolist()
@@ -122,12 +124,12 @@ def algorithmic_work(w, seqs=None, tokens=None, include_write=True):
         cache_rows += span
         bt_entries += last_pos // bs - first_lo // bs + 1
         q_rows += len(toks)
-    read_bytes = (cache_rows * hs * el + q_rows * H * hs * el + q_rows * H * vhs * el +
+    read_bytes = (cache_rows * hs * el_c + q_rows * H * hs * el + q_rows * H * vhs * el +
                   q_rows * w.rotary_dim * el + bt_entries * 4)
     write_bytes = 0
     if include_write:
         n_written = int((w.slot_mapping >= 0).sum())
-        write_bytes = (w.num_tokens * hs * el + n_written * hs * el +
+        write_bytes = (w.num_tokens * hs * el + n_written * hs * el_c +
                        w.num_tokens * (w.rotary_dim * el + 4))
     return dict(bytes=read_bytes + write_bytes, read_bytes=read_bytes, flops=flops,
                 cache_rows=cache_rows, tokens=q_rows)

@@ -63,6 +63,13 @@ typedef enum pa_dtype {
   PA_DTYPE_BF16 = 1
 } pa_dtype;
 
+/* Element format of key_cache (pa_latent_params.cache_dtype). */
+typedef enum pa_cache_dtype {
+  PA_CACHE_DEFAULT = 0,  /* the query dtype (pa_latent_params.dtype)           */
+  PA_CACHE_FP8_E4M3 = 1  /* OCP FP8 E4M3 ("e4m3fn") codes, one byte per channel,
+                            with one dequantization scale k_scale for the cache */
+} pa_cache_dtype;
+
 /* Bits OR-ed into *err_flags by the device (see "Conventions"). */
 #define PA_DEVERR_SLOT        0x01 /* slot_mapping[t] >= num_blocks*bs or < -1     */
 #define PA_DEVERR_BLOCK       0x02 /* block_table entry read is not in [0, num_blocks) */
@@ -72,6 +79,9 @@ typedef enum pa_dtype {
 #define PA_DEVERR_CONTEXT     0x20 /* past < 0 or context > max_blocks_per_seq*bs  */
 #define PA_DEVERR_TIMEOUT     0x40 /* an internal pipeline wait exceeded its bound;
                                       the affected rows were not written          */
+#define PA_DEVERR_RANGE       0x80 /* FP8 cache, bf16 query: a rotated query value
+                                      exceeded 65504 (the fp16 operands of that
+                                      read path) and was saturated to +-65504     */
 
 /* pa_latent_params.flags */
 #define PA_FLAG_PORTABLE 0x1 /* run the portable CUDA-core attention kernels even
@@ -118,6 +128,10 @@ typedef struct pa_latent_params {
   float softcap;              /* <= 0: off; else s = softcap*tanh(s/softcap)         */
   int32_t local_window_size;  /* < 0: off; else keys with pos - j > window skipped   */
   int32_t flags;              /* PA_FLAG_*                                           */
+  int32_t cache_dtype;        /* pa_cache_dtype of key_cache                         */
+  float k_scale;              /* FP8 cache: a channel's value is code * k_scale; the
+                                 write stores e4m3(v / k_scale) (f32 division,
+                                 round to nearest even, saturated to +-448)          */
 } pa_latent_params;
 
 /* Checks the parameters alone (the first group of checks of every entry

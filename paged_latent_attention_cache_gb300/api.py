@@ -22,7 +22,7 @@ class PagedLatentAttention:
                  num_blocks: int, max_blocks_per_seq: int, scale: float = 0.0,
                  softcap: float = 0.0, local_window_size: int = -1, max_seqs: int,
                  max_tokens: int, device="cuda", portable: bool = False,
-                 own_slots: bool = False):
+                 own_slots: bool = False, cache_dtype=None, k_scale: float = 1.0):
         self.dtype = dtype
         self.num_heads = num_heads
         self.head_size = head_size
@@ -33,7 +33,8 @@ class PagedLatentAttention:
             rotary_interleaved=rotary_interleaved, cos_rows=cos_rows, block_size=block_size,
             num_blocks=num_blocks, max_blocks_per_seq=max_blocks_per_seq, scale=scale,
             softcap=softcap, local_window_size=local_window_size,
-            flags=B.PA_FLAG_PORTABLE if portable else 0)
+            flags=B.PA_FLAG_PORTABLE if portable else 0, cache_dtype=cache_dtype,
+            k_scale=k_scale)
         s = B.pa_latent_validate(self.params)
         if s != B.PA_OK:
             raise B.PaError(s, B.last_error())
@@ -60,7 +61,7 @@ class PagedLatentAttention:
                    max_blocks_per_seq=w.max_blocks_per_seq, scale=w.scale, softcap=w.softcap,
                    local_window_size=w.local_window_size, max_seqs=w.num_seqs,
                    max_tokens=max(w.num_tokens, 1), device=device, portable=portable,
-                   own_slots=own_slots)
+                   own_slots=own_slots, cache_dtype=w.cache_dtype, k_scale=w.k_scale)
 
     def kernel_family(self, phase: int) -> int:
         return B.pa_latent_kernel_family(self.params, phase)

@@ -28,6 +28,9 @@ PA_ERR_WORKSPACE = 4
 PA_DTYPE_F16 = 0
 PA_DTYPE_BF16 = 1
 
+PA_CACHE_DEFAULT = 0
+PA_CACHE_FP8_E4M3 = 1
+
 PA_DEVERR_SLOT = 0x01
 PA_DEVERR_BLOCK = 0x02
 PA_DEVERR_POSITION = 0x04
@@ -35,6 +38,7 @@ PA_DEVERR_CUMSEQ = 0x08
 PA_DEVERR_DECODE_QLEN = 0x10
 PA_DEVERR_CONTEXT = 0x20
 PA_DEVERR_TIMEOUT = 0x40
+PA_DEVERR_RANGE = 0x80
 
 PA_FLAG_PORTABLE = 0x1
 PA_FLAG_AFTER_WRITE = 0x2
@@ -68,6 +72,8 @@ class pa_latent_params(ctypes.Structure):
         ("softcap", ctypes.c_float),
         ("local_window_size", ctypes.c_int32),
         ("flags", ctypes.c_int32),
+        ("cache_dtype", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
     ]
 
 
@@ -119,14 +125,22 @@ def _check(s: int):
 
 def make_params(*, dtype, num_heads, head_size, v_head_size=0, rotary_offset=0, rotary_dim=0,
                 rotary_interleaved=0, cos_rows=1, block_size, num_blocks, max_blocks_per_seq,
-                scale=0.0, softcap=0.0, local_window_size=-1, flags=0) -> pa_latent_params:
+                scale=0.0, softcap=0.0, local_window_size=-1, flags=0, cache_dtype=None,
+                k_scale=1.0) -> pa_latent_params:
+    """``cache_dtype``: None / PA_CACHE_DEFAULT (the dtype), or "e4m3" /
+    PA_CACHE_FP8_E4M3 with the FP8 cache's ``k_scale``."""
     if isinstance(dtype, torch.dtype):
         dtype = {torch.float16: PA_DTYPE_F16, torch.bfloat16: PA_DTYPE_BF16}.get(dtype, -1)
+    if cache_dtype is None:
+        cache_dtype = PA_CACHE_DEFAULT
+    elif isinstance(cache_dtype, str):
+        cache_dtype = {"e4m3": PA_CACHE_FP8_E4M3}.get(cache_dtype, -1)
     return pa_latent_params(int(dtype), int(num_heads), int(head_size), int(v_head_size),
                             int(rotary_offset), int(rotary_dim), int(rotary_interleaved),
                             int(cos_rows), int(block_size), int(num_blocks),
                             int(max_blocks_per_seq), float(scale), float(softcap),
-                            int(local_window_size), int(flags))
+                            int(local_window_size), int(flags), int(cache_dtype),
+                            float(k_scale))
 
 
 def _ptr(t: Optional[torch.Tensor]):

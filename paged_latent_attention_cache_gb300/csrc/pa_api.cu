@@ -24,6 +24,7 @@ namespace pa {
 namespace {
 
 thread_local std::string g_last_error;
+thread_local const char* g_launch_step = nullptr;
 
 pa_status fail(pa_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
 pa_status fail(pa_status s, const char* fmt, ...) {
@@ -109,6 +110,11 @@ pa_status resolve(const pa_latent_params* p, Geometry* g) {
   if (!isfinite(p->softcap)) return fail(PA_ERR_INVALID_ARGUMENT, "softcap must be finite");
   if (p->flags & ~(PA_FLAG_PORTABLE | PA_FLAG_AFTER_WRITE | PA_FLAG_OWN_SLOTS))
     return fail(PA_ERR_INVALID_ARGUMENT, "unknown flag bits 0x%x", p->flags);
+  if (p->cache_dtype != PA_CACHE_DEFAULT && p->cache_dtype != PA_CACHE_FP8_E4M3)
+    return fail(PA_ERR_INVALID_ARGUMENT, "cache_dtype %d is not a pa_cache_dtype", p->cache_dtype);
+  const bool fp8 = p->cache_dtype == PA_CACHE_FP8_E4M3;
+  if (fp8 && !(isfinite(p->k_scale) && p->k_scale > 0.f))
+    return fail(PA_ERR_INVALID_ARGUMENT, "an FP8 cache needs a finite k_scale > 0");
 
   g->dtype = p->dtype;
   g->H = p->num_heads;
@@ -124,6 +130,8 @@ pa_status resolve(const pa_latent_params* p, Geometry* g) {
   g->scale = scale;
   g->softcap = p->softcap > 0.f ? p->softcap : 0.f;
   g->window = p->local_window_size < 0 ? -1 : p->local_window_size;
+  g->fp8 = fp8 ? 1 : 0;
+  g->k_scale = fp8 ? p->k_scale : 1.f;
   g->flags = p->flags;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -143,7 +151,10 @@ pa_status check_tokens(int64_t num_tokens, int32_t num_seqs, const Geometry& g) 
 }
 
 pa_status cuda_status(cudaError_t e, const char* what) {
+  const char* step = g_launch_step;
+  g_launch_step = nullptr;
   if (e == cudaSuccess) return PA_OK;
+  if (step) return fail(PA_ERR_CUDA, "%s (%s): %s", what, step, cudaGetErrorString(e));
   return fail(PA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
@@ -194,6 +205,10 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
              past,    block_table, num_seqs,  seq_begin, seq_end,   workspace,
              workspace_bytes, out, err_flags, reinterpret_cast<cudaStream_t>(stream)};
   const bool tc = use_tc(g, ph);
+  if (g.fp8 && !tc)
+    return fail(PA_ERR_NOT_IMPLEMENTED,
+                "an FP8 cache is read by the tensor-core kernels only (latent widths 64..256 "
+                "on one SM; not with PA_FLAG_PORTABLE)");
   const size_t need = call_workspace(g, ph, seq_begin, seq_end, num_tokens);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
@@ -205,6 +220,8 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
 }  // namespace
 
 pa_status record_error(pa_status s, const char* msg) { return fail(s, "%s", msg); }
+
+void set_launch_step(const char* step) { g_launch_step = step; }
 
 pa_status decode_call_workspace(const pa_latent_params* p, int32_t seq_begin, int32_t seq_end,
                                 size_t* need) {

@@ -27,6 +27,8 @@ struct Geometry {
   float scale;      // resolved (never 0)
   float softcap;    // <= 0: off
   int window;       // < 0: off
+  int fp8;          // key_cache holds E4M3 codes (PA_CACHE_FP8_E4M3)
+  float k_scale;    // FP8 cache: value = code * k_scale (1 otherwise)
   int flags;
   int num_sms;      // SM count of the current device
   int device;       // current device ordinal
@@ -50,6 +52,10 @@ cudaError_t once_per_device(std::atomic<bool> (&done)[64], int device, F&& actio
 // Records msg as the calling thread's pa_latent_last_error() text and
 // returns s.
 pa_status record_error(pa_status s, const char* msg);
+
+// Names the step of a launch that failed (a static string); the entry
+// point adds it to the error text of a failed launch. Cleared per call.
+void set_launch_step(const char* step);
 
 // ---- write phase (pa_write.cu)
 cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,

@@ -12,7 +12,9 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.H > kRows) return false;
   if (g.hs == 576 && g.vhs == 512) {
     // CTA-pair kernel (pa_tc_pair.cu): each CTA rotates the query channels it
-    // holds, so the rotary channels must lie in one CTA's range.
+    // holds, so the rotary channels must lie in one CTA's range. It reads a
+    // cache in the query dtype only.
+    if (g.fp8) return false;
     if (!(g.rd == 0 || g.ro >= 320 || g.ro + g.rd <= 256)) return false;
     *s = Shape{576, 256, 2, 64, 3, 128, 2, true};
     return true;
@@ -20,6 +22,18 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
   // (a latent narrower than one 64-channel TMA box runs on the portable kernels)
   if (g.hs > 256 || g.hs < 64) return false;
   const int vg = 64 * ((g.vhs + 63) / 64);
+  if (g.fp8) {
+    // FP8 cache: two fp16 key stages (the converted tiles the MMAs read) and
+    // as many E4M3 stages as the rest of shared memory holds (they carry
+    // the copies in flight from HBM).
+    Shape t{g.hs, vg, 1, vg > 128 ? 64 : 128, 2, (ph == Phase::kDecode && g.H <= 64) ? 64 : 128,
+            2, false};
+    t.stages8 = (kSmemBudget - 1024 - q_bytes(t) - 2 * stage_bytes(t)) / stage8_bytes(t);
+    if (t.stages8 > 8) t.stages8 = 8;
+    if (t.stages8 < 2 || tmem_cols_used(t) > 512) return false;
+    *s = t;
+    return true;
+  }
   // Prefill with H <= 64 (units of 128 / H tokens, each a short chain of a
   // few key tiles) runs two CTAs per SM where they fit in half an SM: 64-key
   // tiles, two stages and a single S/P buffer (97 KB of shared memory and
@@ -48,6 +62,7 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
 template <typename T>
 cudaError_t launch_single(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
                           const Shape& s) {
+  if (s.stages8) return launch_fp8<T>(g, ph, a, P, nq, s);
   if (fixed_shape(s)) return launch_fixed<T>(g, ph, a, P, nq, s);
   if (s.n == 128 && s.qr == 64) return launch_shape<T, 128, 64, 2, 0, 0, 0>(g, ph, a, P, nq, s);
   if (s.n == 128) return launch_shape<T, 128, 128, 2, 0, 0, 0>(g, ph, a, P, nq, s);
@@ -111,9 +126,14 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.bs = g.bs;
   P.num_blocks = g.num_blocks;
   P.max_blocks = g.max_blocks;
-  P.scale_log2 = g.scale * tc::kLog2e;
+  // An FP8 cache's keys are code * k_scale: the kernels multiply the codes,
+  // so k_scale joins the score scale (and the softcap factors) and the
+  // output scale.
+  const float eff = g.scale * g.k_scale;
+  P.out_scale = g.k_scale;
+  P.scale_log2 = eff * tc::kLog2e;
   P.softcap_on = g.softcap > 0.f ? 1 : 0;
-  P.cap_in = g.softcap > 0.f ? g.scale / g.softcap : 0.f;
+  P.cap_in = g.softcap > 0.f ? eff / g.softcap : 0.f;
   P.cap_out = g.softcap * tc::kLog2e;
   // Series coefficients a_(2i+1) = softcap * log2(e) * t_(2i+1) * (scale /
   // softcap)^(2i+1), t = 1, -1/3, 2/15, -17/315, 62/2835 (the Maclaurin
@@ -122,7 +142,7 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.cap_vlim = 0.f;
   for (int i = 0; i < 5; ++i) P.cap_a[i] = 0.f;
   if (g.softcap > 0.f) {
-    const double ci = (double)g.scale / (double)g.softcap;
+    const double ci = (double)eff / (double)g.softcap;
     const double co = (double)g.softcap * 1.4426950408889634;
     const double t[5] = {1.0, -1.0 / 3.0, 2.0 / 15.0, -17.0 / 315.0, 62.0 / 2835.0};
     bool normal = true;
@@ -154,8 +174,10 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
     const size_t per = (size_t)units * s.groups * tc::kRows;
     const size_t o = ((per * s.vg * sizeof(float)) + 255) & ~(size_t)255;
     const size_t ml = ((per * 2 * sizeof(float)) + 255) & ~(size_t)255;
-    if (a.workspace == nullptr || a.workspace_bytes < tc::decode_ws_bytes(s, units, nq))
+    if (a.workspace == nullptr || a.workspace_bytes < tc::decode_ws_bytes(s, units, nq)) {
+      set_launch_step("decode workspace");
       return cudaErrorInvalidValue;
+    }
     char* w = reinterpret_cast<char*>(a.workspace);
     P.ws_o = reinterpret_cast<float*>(w);
     P.ws_ml = reinterpret_cast<float*>(w + o);

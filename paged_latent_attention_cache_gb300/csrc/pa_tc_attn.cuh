@@ -40,8 +40,11 @@
 // exits without trapping.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include <cfloat>
 #include <cmath>
+#include <type_traits>
 
 #include "pa_tc_common.cuh"
 
@@ -51,6 +54,67 @@ namespace tc {
 // TMEM columns allocated for `used` columns: a power of two >= 32.
 constexpr int fixed_tmem_cols(int used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
+}
+
+// Two E4M3 codes (low byte first) as an fp16x2 word (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Eight f32 values as fp16, saturated to +-65504; records in *big whether one
+// was beyond that range (NaN stays NaN).
+__device__ __forceinline__ uint4 pack8_f16_sat(const float (&f)[8], bool* big) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a = f[2 * i], b = f[2 * i + 1];
+    *big |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;
+    a = fminf(fmaxf(a, -65504.f), 65504.f);
+    b = fminf(fmaxf(b, -65504.f), 65504.f);
+    w[i] = pack2<__half>(a, b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// FP8 cache with a bf16 query: one query row, in place in its swizzled
+// slabs (16-byte chunk c of row r at c ^ (r & 7)), from bf16 to fp16 (the
+// MMA operands of that path), its rotary channels rotated in f32 first. A
+// value beyond the fp16 range is saturated and flags PA_DEVERR_RANGE.
+template <typename T, int QBOX>
+__device__ __noinline__ void q_row_to_f16(uint8_t* q_s, int row, int hs, const Params& P,
+                                          int64_t pos) {
+  auto at = [&](int d0) -> uint4* {
+    const int slab = d0 >> 6, ch = (d0 >> 3) & 7;
+    return reinterpret_cast<uint4*>(q_s + slab * QBOX + row * 128 + ((ch ^ (row & 7)) << 4));
+  };
+  const int ro = P.rd > 0 ? P.ro : hs, rd = P.rd, half = rd >> 1;
+  const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * half;
+  const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * half;
+  bool big = false;
+  for (int d0 = 0; d0 < hs; d0 += 8) {
+    const bool rot = d0 >= ro && d0 < ro + rd;
+    float a[8];
+    unpack8<T>(*at(d0), a);
+    if (rot && !P.interleaved) {
+      if (d0 >= ro + half) continue;  // rotated with its partner below
+      float bb[8], na[8], nb[8];
+      unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+      rope8<T>(na, bb, d0, ro, rd, 0, crow, srow);
+      rope8<T>(nb, a, d0 + half, ro, rd, 0, crow, srow);
+      *at(d0) = pack8_f16_sat(na, &big);
+      *at(d0 + half) = pack8_f16_sat(nb, &big);
+      continue;
+    }
+    if (rot) {
+      float dummy[8];
+      rope8<T>(a, dummy, d0, ro, rd, 1, crow, srow);
+    }
+    *at(d0) = pack8_f16_sat(a, &big);
+  }
+  if (big) raise_flag(P.err_flags, PA_DEVERR_RANGE);
 }
 
 
@@ -92,11 +156,14 @@ __device__ __noinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t b0, uint3
 // 192/128 geometry); 0 takes them from the launch's Params (any other
 // width). Fixed values keep every CTA's one-time code short: its
 // instructions are fetched cold on every launch.
-template <typename T, int N, int QR, int NB, bool CAP, int HSF, int VGF, int STF>
-__global__ void __launch_bounds__(Tile<N, QR, NB>::kThreads, 1)
+// FP8: the cache holds E4M3 codes; the MMAs then take fp16 operands (the
+// query rounded to fp16 once, the key tiles converted exactly, P in fp16).
+template <typename T, int N, int QR, int NB, bool CAP, int HSF, int VGF, int STF, bool FP8>
+__global__ void __launch_bounds__(Tile<N, QR, NB, FP8>::kThreads, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ Params P) {
-  using C = Tile<N, QR, NB>;
+  using C = Tile<N, QR, NB, FP8>;
+  using TM = typename std::conditional<FP8, __half, T>::type;  // MMA operand type
   constexpr int kSlabsF = (HSF + 63) / 64;
   constexpr int kTmemColsF = fixed_tmem_cols(VGF + NB * N + NB * N / 2);
   const int hs = HSF ? HSF : P.hs;
@@ -115,6 +182,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                                              ~(uintptr_t)1023);
   uint8_t* q_s = smem;             // slabs query slabs of QR rows
   uint8_t* k_s = smem + q_bytes;   // stages key stages of N rows x slabs slabs
+  uint8_t* k8_s = k_s + stages * stage_bytes;  // FP8: stages8 E4M3 tiles of N rows x hs bytes
   Barriers* bars = &bars_s;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -199,8 +267,16 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     fence_proxy_async();  // scratch stores before the query load reuses the region
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(smem_u32(&bars->full[s]), 1);
+      // (FP8: the key tile is complete when every converter thread has
+      // written its part; otherwise when the TMA bytes have landed)
+      mbar_init(smem_u32(&bars->full[s]), FP8 ? 128 : 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    if (FP8) {
+      for (int s = 0; s < P.stages8; ++s) {
+        mbar_init(smem_u32(&bars->full8[s]), 1);
+        mbar_init(smem_u32(&bars->empty8[s]), 128);
+      }
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bars->s_full[i]), 1);
@@ -269,7 +345,11 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // channels [64s, 64s+64); row r's 16-byte chunk c sits at c ^ (r&7));
           // each thread then rotates its own row's rotary channels in place.
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
-          if (ok && P.rd > 0 && row < rows) {
+          if (FP8 && !std::is_same<T, __half>::value) {
+            // bf16 query, fp16 MMA operands: the whole row is rounded to fp16
+            // in place (its rotary channels rotated first, in f32)
+            if (ok && row < rows) q_row_to_f16<T, C::kQBox>(q_s, row, hs, P, pos_r);
+          } else if (ok && P.rd > 0 && row < rows) {
             const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos_r * (P.rd >> 1);
             const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos_r * (P.rd >> 1);
             auto at = [&](int d0) -> uint4* {
@@ -426,9 +506,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               for (int e = 0; e < 32; ++e)
                 if (c + e < clo || c + e > chi) r[e] = __float_as_uint(-INFINITY);
             }
-            if (!CAP) lsum += exp_chunk<T, 0>(r, pk, A);
-            else if (mode == 1) lsum += exp_chunk<T, 1>(r, pk, A);
-            else lsum += exp_chunk<T, 2>(r, pk, A);
+            if (!CAP) lsum += exp_chunk<TM, 0>(r, pk, A);
+            else if (mode == 1) lsum += exp_chunk<TM, 1>(r, pk, A);
+            else lsum += exp_chunk<TM, 2>(r, pk, A);
             tmem_st16(lane_addr + col_p + sb * (N / 2) + c / 2, pk);
           }
           if (!dry) l += lsum;
@@ -469,7 +549,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         tc_fence_after();
         const bool bad = bars->bad != 0;
         if (splits == 1) {
-          const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
+          const float inv = (l > 0.f && !bad) ? P.out_scale / l : 0.f;
           const bool vec = vhs % 8 == 0;  // 16-byte aligned output rows
 #pragma unroll 1
           for (int c = 0; c < vg && c < vhs; c += 16) {
@@ -501,10 +581,13 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             tmem_ld16(lane_addr + c, r);
             if (row < rows) {
               float4* dst = reinterpret_cast<float4*>(wo + c);
+              const float os = P.out_scale;
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                     __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+                dst[e] = make_float4(__uint_as_float(r[4 * e]) * os,
+                                     __uint_as_float(r[4 * e + 1]) * os,
+                                     __uint_as_float(r[4 * e + 2]) * os,
+                                     __uint_as_float(r[4 * e + 3]) * os);
             }
           }
           if (row < rows) {
@@ -533,18 +616,24 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // the CTA-pair kernel does, issues the first stages of every CTA at
       // once, and the first tiles then arrive later behind that burst.)
       const int32_t* bt = P.block_table + (int64_t)b * P.max_blocks;
+      // the ring the copies land in: key tiles, or (FP8) the E4M3 tiles the
+      // converter warps read
+      const int pst = FP8 ? P.stages8 : stages;
+      uint64_t* pfull = FP8 ? bars->full8 : bars->full;
+      uint64_t* pempty = FP8 ? bars->empty8 : bars->empty;
+      const int pbytes = FP8 ? P.stage8_bytes : stage_bytes;
+      uint8_t* pbase = FP8 ? k8_s : k_s;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
-        const int stage = k % stages;
+        const int stage = k % pst;
         if (!waited && k >= dirty_from) {
           grid_dep_wait();  // the write phase's cache rows are complete and visible
           waited = true;
         }
-        if (k >= stages) {
+        if (k >= pst) {
           bool okw = true;
           if (lane == 0)
-            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / stages) & 1) ^ 1, abort,
-                           P.err_flags);
+            okw = wait_bar(smem_u32(&pempty[stage]), ((k / pst) & 1) ^ 1, abort, P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         } else if (P.decode && k == 2 && nsub <= 2) {
           // Decode: every CTA starts at once, and with few copies per tile
@@ -553,7 +642,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           // tiles go out now, the later stages once tile 0 has landed (GLM
           // decode: 35.6 -> 33.7 us per step).
           bool okw = true;
-          if (lane == 0) okw = wait_bar(smem_u32(&bars->full[0]), 0, abort, P.err_flags);
+          if (lane == 0) okw = wait_bar(smem_u32(&pfull[0]), 0, abort, P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
         // coordinates of the nsub boxes of rows (one cache block each)
@@ -570,14 +659,19 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             }
           }
         }
-        if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), (uint32_t)stage_bytes);
+        if (lane == 0) mbar_expect_tx(smem_u32(&pfull[stage]), (uint32_t)pbytes);
         __syncwarp();
         if (lane < nsub) {  // lane sb issues the boxes of rows sb (every slab)
-          const uint32_t full = smem_u32(&bars->full[stage]);
-          const uint32_t dst0 = smem_u32(k_s + stage * stage_bytes) + lane * P.box_rows * 128;
+          const uint32_t full = smem_u32(&pfull[stage]);
+          if (FP8) {  // one box of box_rows whole E4M3 rows (hs bytes each)
+            tma_load_2d(smem_u32(pbase + stage * pbytes) + lane * P.box_rows * hs, &kmap, 0, y,
+                        full);
+          } else {
+            const uint32_t dst0 = smem_u32(pbase + stage * pbytes) + lane * P.box_rows * 128;
 #pragma unroll 1
-          for (int slab = 0; slab < slabs; ++slab)
-            tma_load_2d(dst0 + slab * C::kKBox, &kmap, slab * 64, y, full);
+            for (int slab = 0; slab < slabs; ++slab)
+              tma_load_2d(dst0 + slab * C::kKBox, &kmap, slab * 64, y, full);
+          }
         }
         issued = k + 1;
         __syncwarp();
@@ -586,9 +680,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (*abort && lane == 0) {
         // copies still in flight must land before the CTA exits
         drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
-        for (int st = 0; st < stages && st < issued; ++st) {
-          const int kl = issued - 1 - ((issued - 1 - st) % stages);
-          drain_wait(smem_u32(&bars->full[st]), (kl / stages) & 1, P.err_flags);
+        for (int st = 0; st < pst && st < issued; ++st) {
+          const int kl = issued - 1 - ((issued - 1 - st) % pst);
+          drain_wait(smem_u32(&pfull[st]), (kl / pst) & 1, P.err_flags);
         }
       }
       __syncwarp();
@@ -596,7 +690,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     } else if (warp == C::kMmaWarp) {
       // =================== MMA issuer ===================
       if (lane == 0) {
-        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr bool kBf16 = std::is_same<TM, __nv_bfloat16>::value;
         constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
         const uint32_t id_pv = idesc_f16(kBf16, kRows, vg, true);
         const int nk = hs / 16;  // QK^T K-steps
@@ -673,6 +767,44 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
       }
       __syncwarp();
+    } else if (FP8 && warp >= C::kConvWarp) {
+      // =============== E4M3 -> fp16 key tiles (FP8 cache) ===============
+      // Per tile: wait for its E4M3 rows (full8) and a free fp16 stage
+      // (empty, committed after PV of the tile that used it before), convert
+      // (every E4M3 value is an fp16 normal, so exactly) into the 128-byte-
+      // swizzled K-major layout the MMAs read (16-byte chunk c of row r at
+      // c ^ (r & 7) in its 64-channel slab), then release both. Thread ct
+      // handles row ct / (128 / N) of the tile.
+      constexpr int kTpr = 128 / N;  // converter threads per key row
+      const int ct = tid - C::kConvWarp * 32;
+      const int r = ct / kTpr, j0 = ct % kTpr;
+      const int hs16 = hs / 16;
+      const int st8 = P.stages8;
+      for (int k = 0; k < n; ++k) {
+        const int s8 = k % st8, s16 = k % stages;
+        bool okc = wait_bar(smem_u32(&bars->full8[s8]), (k / st8) & 1, abort, P.err_flags);
+        if (okc && k >= stages)
+          okc = wait_bar(smem_u32(&bars->empty[s16]), ((k / stages) & 1) ^ 1, abort,
+                         P.err_flags);
+        if (!__all_sync(0xffffffffu, okc)) break;
+        const uint8_t* src = k8_s + s8 * P.stage8_bytes + r * hs;
+        uint8_t* dst = k_s + s16 * stage_bytes + r * 128;
+#pragma unroll 2
+        for (int j = j0; j < hs16; j += kTpr) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + j * 16);
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
+                                      e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),
+                                      e4m3x2_to_f16x2(v.w & 0xffffu), e4m3x2_to_f16x2(v.w >> 16));
+          const int c0 = j * 16, ch = (c0 >> 3) & 7;
+          uint8_t* d = dst + (c0 >> 6) * C::kKBox;
+          *reinterpret_cast<uint4*>(d + ((ch ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(d + (((ch + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async();  // the generic-proxy stores, before the MMAs read them
+        mbar_arrive(smem_u32(&bars->full[s16]));
+        mbar_arrive(smem_u32(&bars->empty8[s8]));
+      }
     }
   }
 
@@ -696,7 +828,10 @@ constexpr int kHalfSmemBudget = 113 * 1024 - 1024;
 
 inline int q_bytes(const Shape& s) { return s.qr * ((s.hs + 63) / 64) * 128; }
 inline int stage_bytes(const Shape& s) { return s.n * ((s.hs + 63) / 64) * 128; }
-inline int smem_bytes(const Shape& s) { return q_bytes(s) + s.stages * stage_bytes(s) + 1024; }
+inline int stage8_bytes(const Shape& s) { return s.n * s.hs; }
+inline int smem_bytes(const Shape& s) {
+  return q_bytes(s) + s.stages * stage_bytes(s) + s.stages8 * stage8_bytes(s) + 1024;
+}
 inline int tmem_cols_used(const Shape& s) { return s.vg + s.nb * s.n + s.nb * s.n / 2; }
 inline int tmem_alloc_cols(int used) {
   int c = 32;
@@ -704,10 +839,10 @@ inline int tmem_alloc_cols(int used) {
   return c;
 }
 
-template <typename T, int N, int QR, int NB, int HSF, int VGF, int STF>
+template <typename T, int N, int QR, int NB, int HSF, int VGF, int STF, bool FP8 = false>
 cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
                          const Shape& s) {
-  using C = Tile<N, QR, NB>;
+  using C = Tile<N, QR, NB, FP8>;
   P.hs = g.hs;
   P.slabs = (g.hs + 63) / 64;
   P.stages = s.stages;
@@ -716,14 +851,16 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   P.col_s = s.vg;
   P.col_p = s.vg + NB * N;
   P.tmem_cols = tmem_alloc_cols(tmem_cols_used(s));
+  P.stages8 = s.stages8;
+  P.stage8_bytes = stage8_bytes(s);
   const size_t smem = (size_t)smem_bytes(s);
   // the softcap code is compiled only into the kernels that use it; the
   // dynamic shared-memory limit is raised once per device to the opt-in
   // maximum less the kernel's static shared memory
   static std::atomic<bool> configured[2][64];
   const int cap = P.softcap_on ? 1 : 0;
-  auto kern = cap ? tc_attn_kernel<T, N, QR, NB, true, HSF, VGF, STF>
-                  : tc_attn_kernel<T, N, QR, NB, false, HSF, VGF, STF>;
+  auto kern = cap ? tc_attn_kernel<T, N, QR, NB, true, HSF, VGF, STF, FP8>
+                  : tc_attn_kernel<T, N, QR, NB, false, HSF, VGF, STF, FP8>;
   cudaError_t e = once_per_device(configured[cap], g.device, [&] {
     int optin = 0;
     cudaFuncAttributes fa;
@@ -734,23 +871,42 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 optin - (int)fa.sharedSizeBytes);
   });
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    set_launch_step("kernel shared-memory attribute");
+    return e;
+  }
   EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
+  if (!enc) {
+    set_launch_step("driver tensor-map encoder lookup");
+    return cudaErrorNotSupported;
+  }
   const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
                                      ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   // Cache rows [num_blocks*bs, hs]: boxes of 64 channels x box_rows rows (a
-  // box that reaches past channel hs reads zeros there).
+  // box that reaches past channel hs reads zeros there); FP8: boxes of whole
+  // E4M3 rows (hs bytes) x box_rows rows, unswizzled.
   CUtensorMap map;
   const cuuint64_t dims[2] = {(cuuint64_t)g.hs, (cuuint64_t)g.num_blocks * g.bs};
   const cuuint64_t strides[1] = {(cuuint64_t)g.hs * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  CUresult r;
+  if (FP8) {
+    const cuuint64_t strides8[1] = {(cuuint64_t)g.hs};
+    const cuuint32_t box8[2] = {(cuuint32_t)g.hs, (cuuint32_t)P.box_rows};
+    r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.key_cache), dims,
+            strides8, box8, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
+    r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  if (r != CUDA_SUCCESS) {
+    set_launch_step("cache tensor map");
+    return cudaErrorInvalidValue;
+  }
   // Query rows [T*H, hs]: one QR-row box per 64-channel slab loads a token's heads.
   CUtensorMap qmap;
   const cuuint64_t qdims[2] = {(cuuint64_t)g.hs, (cuuint64_t)a.num_tokens * g.H};
@@ -758,16 +914,25 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   r = enc(&qmap, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (r != CUDA_SUCCESS) {
+    set_launch_step("query tensor map");
+    return cudaErrorInvalidValue;
+  }
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
   e = launch_pdl(kern, dim3((unsigned)units), dim3(C::kThreads), smem, a.stream, map, qmap, P);
-  if (e != cudaSuccess || ph != Phase::kDecode) return e;
-  return launch_combine<T>(P, g.H, nq, a.stream);
+  if (e != cudaSuccess) {
+    set_launch_step("attention kernel launch");
+    return e;
+  }
+  if (ph != Phase::kDecode) return e;
+  e = launch_combine<T>(P, g.H, nq, a.stream);
+  if (e != cudaSuccess) set_launch_step("combine kernel launch");
+  return e;
 }
 
 // The 192/128 shapes compiled with their geometry fixed (pa_tc_glm.cu).
 inline bool fixed_shape(const Shape& s) {
-  if (s.hs != 192 || s.vg != 128 || s.pair) return false;
+  if (s.hs != 192 || s.vg != 128 || s.pair || s.stages8) return false;
   return (s.n == 128 && s.qr == 64 && s.nb == 2 && s.stages == 4) ||
          (s.n == 64 && s.qr == 128 && s.nb == 1 && s.stages == 2) ||
          (s.n == 128 && s.qr == 128 && s.nb == 2 && s.stages == 3);
@@ -775,6 +940,10 @@ inline bool fixed_shape(const Shape& s) {
 template <typename T>
 cudaError_t launch_fixed(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
                          const Shape& s);
+// FP8-cache shapes (pa_tc_fp8.cu).
+template <typename T>
+cudaError_t launch_fp8(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
+                       const Shape& s);
 
 }  // namespace tc
 }  // namespace pa

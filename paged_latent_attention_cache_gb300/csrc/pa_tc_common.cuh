@@ -243,6 +243,12 @@ struct Params {
   int q_bytes;       // query rows * slabs * 128
   int col_s, col_p;  // TMEM columns of the S and P buffers (O starts at column 0)
   int tmem_cols;     // TMEM columns allocated (a power of two >= 32)
+  // FP8 cache (E4M3 codes, value = code * k_scale): the E4M3 tiles land in a
+  // ring of their own (stages8 stages of N rows x hs bytes) and are
+  // converted to fp16 tiles; k_scale is folded into scale_log2 / the softcap
+  // factors and into out_scale, which multiplies the output (1 otherwise).
+  int stages8, stage8_bytes;
+  float out_scale;
 };
 
 // Compile-time part of a single-CTA kernel configuration: N keys per tile,
@@ -250,7 +256,7 @@ struct Params {
 // MMA then reads rows 64-127 from the next slab, rows that are never
 // stored), NB S/P buffers in TMEM. The latent width, value channels and
 // stage count are per-launch values in Params.
-template <int N, int QR, int NB>
+template <int N, int QR, int NB, bool FP8 = false>
 struct Tile {
   static constexpr int kQBox = QR * 128;  // bytes per query slab
   static constexpr int kKBox = N * 128;   // bytes per key slab of a stage
@@ -263,11 +269,15 @@ struct Tile {
   // softmax warp; warps 4 and 5 then have no role.
   static constexpr int kProdWarp = QR == 64 ? 6 : 4;
   static constexpr int kMmaWarp = kProdWarp + 1;
-  static constexpr int kThreads = 32 * (kMmaWarp + 1);
+  // FP8 cache: four converter warps (one per scheduler partition) after the
+  // MMA warp turn E4M3 key tiles into fp16 tiles.
+  static constexpr int kConvWarp = kMmaWarp + 1;
+  static constexpr int kThreads = 32 * (kMmaWarp + 1 + (FP8 ? 4 : 0));
 };
 
 struct Barriers {
   uint64_t full[8], empty[8];
+  uint64_t full8[8], empty8[8];  // FP8 cache: E4M3 tile ring (TMA -> converters)
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2];
   uint64_t q_tma, q_full;
   uint64_t drain;
@@ -755,6 +765,7 @@ inline EncodeTiledFn encode_fn() {
 struct Shape {
   int hs, vg, groups, n, stages, qr, nb;
   bool pair;
+  int stages8 = 0;  // FP8 cache: E4M3 stages (0: the cache is in the query dtype)
 };
 
 // Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
@@ -783,7 +794,9 @@ cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e != cudaSuccess) (void)cudaGetLastError();  // not left behind for a later call
+  return e;
 }
 
 // Split combine of a decode call over nq sequences, launched after the

@@ -8,6 +8,10 @@
 // i.e. whole rows, so loads and stores are coalesced. HBM traffic is the
 // algorithmic minimum: each key row read once (plus its 128-byte rotary
 // partner slice, which hits L1), each written row stored once.
+#include <cuda_fp8.h>
+
+#include <type_traits>
+
 #include "pa_common.cuh"
 #include "pa_internal.h"
 
@@ -18,14 +22,17 @@ namespace pa {
 // dependent global loads).
 constexpr int kStagedSeqs = 8191;
 
-template <typename T>
+// FP8 = the cache holds E4M3 codes: each channel's (rotated) value v is
+// stored as e4m3(v / k_scale), the division an IEEE f32 one, the conversion
+// rounding to nearest even and saturating at +-448.
+template <typename T, bool FP8>
 __global__ void __launch_bounds__(256)
 latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
                     const T* __restrict__ sin_cache, const int32_t* __restrict__ slot_mapping,
                     const int32_t* __restrict__ cumseq, const int32_t* __restrict__ past,
-                    int32_t num_seqs, T* __restrict__ key_cache, int64_t num_tokens, int hs,
+                    int32_t num_seqs, void* __restrict__ key_cache, int64_t num_tokens, int hs,
                     int ro, int rd, int interleaved, int cos_rows, int64_t num_slots,
-                    int32_t* err_flags) {
+                    float k_scale, int32_t* err_flags) {
   // A kernel launched after this one with programmatic dependent launch may
   // start its prologue now; it waits (griddepcontrol.wait) for this grid to
   // complete before it reads the cache.
@@ -71,6 +78,30 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
       if (g == 0) raise_flag(err_flags, pos < 0 ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
       continue;
     }
+    if (FP8) {
+      float x[8];
+      unpack8<T>(v, x);
+      if (rot) {
+        float xp[8];
+        unpack8<T>(vp, xp);
+        rope8<T>(x, xp, d0, ro, rd, interleaved, cos_cache + pos * (rd >> 1),
+                 sin_cache + pos * (rd >> 1));
+      }
+      uint32_t w[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * k], k_scale), __fdiv_rn(x[4 * k + 1], k_scale)),
+            __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(x[4 * k + 2], k_scale), __fdiv_rn(x[4 * k + 3], k_scale)),
+            __NV_SATFINITE, __NV_E4M3);
+        w[k] = (uint32_t)lo | ((uint32_t)hi << 16);
+      }
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint8_t*>(key_cache) + (int64_t)slot * hs + d0) =
+          make_uint2(w[0], w[1]);
+      continue;
+    }
     if (rot) {
       float x[8], xp[8];
       unpack8<T>(v, x);
@@ -80,7 +111,7 @@ latent_write_kernel(const T* __restrict__ key, const T* __restrict__ cos_cache,
       rope8<T>(x, xp, d0, ro, rd, interleaved, crow, srow);
       v = pack8<T>(x);
     }
-    *reinterpret_cast<uint4*>(key_cache + (int64_t)slot * hs + d0) = v;
+    *reinterpret_cast<uint4*>(reinterpret_cast<T*>(key_cache) + (int64_t)slot * hs + d0) = v;
   }
 }
 
@@ -97,17 +128,19 @@ cudaError_t launch_write(const Geometry& g, const void* key, int64_t num_tokens,
   if (blocks > cap) blocks = cap;
   const int64_t num_slots = (int64_t)g.num_blocks * g.bs;
   const size_t smem = num_seqs <= kStagedSeqs ? (size_t)(num_seqs + 1) * sizeof(int32_t) : 0;
+  auto go = [&](auto kern, auto* typed) {
+    using TP = std::remove_pointer_t<decltype(typed)>;
+    kern<<<(unsigned)blocks, threads, smem, stream>>>(
+        (const TP*)key, (const TP*)cos_cache, (const TP*)sin_cache, slot_mapping, cumseq, past,
+        num_seqs, key_cache, num_tokens, g.hs, g.ro, g.rd, g.interleaved, g.cos_rows, num_slots,
+        g.k_scale, err_flags);
+  };
   if (g.dtype == PA_DTYPE_BF16) {
-    latent_write_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, smem, stream>>>(
-        (const __nv_bfloat16*)key, (const __nv_bfloat16*)cos_cache,
-        (const __nv_bfloat16*)sin_cache, slot_mapping, cumseq, past, num_seqs,
-        (__nv_bfloat16*)key_cache, num_tokens, g.hs, g.ro, g.rd, g.interleaved, g.cos_rows,
-        num_slots, err_flags);
+    if (g.fp8) go(latent_write_kernel<__nv_bfloat16, true>, (__nv_bfloat16*)nullptr);
+    else go(latent_write_kernel<__nv_bfloat16, false>, (__nv_bfloat16*)nullptr);
   } else {
-    latent_write_kernel<__half><<<(unsigned)blocks, threads, smem, stream>>>(
-        (const __half*)key, (const __half*)cos_cache, (const __half*)sin_cache, slot_mapping,
-        cumseq, past, num_seqs, (__half*)key_cache, num_tokens, g.hs, g.ro, g.rd,
-        g.interleaved, g.cos_rows, num_slots, err_flags);
+    if (g.fp8) go(latent_write_kernel<__half, true>, (__half*)nullptr);
+    else go(latent_write_kernel<__half, false>, (__half*)nullptr);
   }
   return cudaGetLastError();
 }

@@ -73,10 +73,16 @@ def _ordered(bits: np.ndarray) -> np.ndarray:
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
+def _ordered8(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes (sign-magnitude) mapped to integers in value order."""
+    c = codes.astype(np.int64)
+    return np.where(c & 0x80, -(c & 0x7F), c)
+
+
 def check_cache(w: W.Workload, got: np.ndarray, ref: np.ndarray):
     """Rows no token wrote are bit-exact; written rows are bit-exact outside
-    the rotary channels and within 1 ulp inside them. Returns the number of
-    rotary values that differ by that ulp."""
+    the rotary channels and within 1 ulp (FP8 cache: 1 code) inside them.
+    Returns the number of rotary values that differ by that ulp."""
     hs = w.head_size
     g = got.reshape(-1, hs)
     r = ref.reshape(-1, hs)
@@ -93,7 +99,8 @@ def check_cache(w: W.Workload, got: np.ndarray, ref: np.ndarray):
     assert exact.all(), f"{(~exact).sum()} non-rotary cache values differ"
     if not rd:
         return 0
-    d = np.abs(_ordered(gw[:, rot]) - _ordered(rw[:, rot]))
+    order = _ordered8 if w.cache_dtype == "e4m3" else _ordered
+    d = np.abs(order(gw[:, rot]) - order(rw[:, rot]))
     assert d.max(initial=0) <= 1, f"rotary cache channels differ by {d.max()} ulp"
     return int((d > 0).sum())
 

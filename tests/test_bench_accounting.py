@@ -30,7 +30,8 @@ def _check(w):
     assert got["flops"] == flops
     assert got["tokens"] == q_rows
     el = 2
-    want = (rows * w.head_size * el + q_rows * w.num_heads * (w.head_size + w.v_head_size) * el +
+    el_c = 1 if w.cache_dtype == "e4m3" else 2   # an E4M3 cache row is hs bytes
+    want = (rows * w.head_size * el_c + q_rows * w.num_heads * (w.head_size + w.v_head_size) * el +
             q_rows * w.rotary_dim * el + bt * 4)
     assert got["read_bytes"] == want
 
@@ -43,6 +44,11 @@ def test_accounting_causal():
 def test_accounting_window():
     _check(W.make_workload("accw", q_lens=[1, 30, 2], past_lens=[100, 50, 7], num_heads=2,
                            **W.GLM, block_size=16, seed=4, local_window_size=11))
+
+
+def test_accounting_fp8_cache():
+    _check(W.make_workload("acc8", q_lens=[1, 5, 0, 17], past_lens=[40, 0, 3, 9], num_heads=4,
+                           **W.GLM, block_size=16, seed=6, cache_dtype="e4m3"))
 
 
 def test_accounting_write_bytes():

@@ -55,6 +55,60 @@ def test_variant(name, portable):
     _check(w, portable, default_scale=default_scale, family=0 if portable else 1)
 
 
+FP8_VARIANTS = {
+    "plain": {},
+    "bs_16": dict(block_size=16),
+    "bs_128": dict(block_size=128),
+    "softcap": dict(softcap=3.0),
+    "window_5": dict(local_window_size=5),
+    "fp16_query": dict(dtype=torch.float16),
+    "interleaved": dict(rotary_interleaved=1),
+    "no_rotary": dict(rotary_dim=0, rotary_offset=0),
+    "heads_128": dict(num_heads=128),
+    "hs_256_vhs_256": dict(head_size=256, v_head_size=256, rotary_offset=192),
+    "hs_80_vhs_48": dict(head_size=80, v_head_size=48, rotary_offset=16),
+    "k_scale_odd": dict(k_scale=0.0123),
+    "saturating_keys": dict(k_scale=2.0 ** -10),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FP8_VARIANTS))
+def test_fp8_cache_variants(name):
+    """FP8 (E4M3) latent cache on the tensor-core kernels: decode and
+    prefill tokens (split decode over a long context, prefill chunks with
+    ragged tails), option variants and geometries. saturating_keys uses a
+    k_scale small enough that many written values exceed 448 and saturate."""
+    kw = dict(num_heads=4, **W.GLM, block_size=64, seed=29, drop_slots=2, cache_dtype="e4m3")
+    kw.update(FP8_VARIANTS[name])
+    w = W.make_workload(f"fp8_{name}", q_lens=[1, 1, 9, 0, 33], past_lens=[3000, 0, 40, 5, 3],
+                        **kw)
+    _check(w, family=1)
+
+
+def test_fp8_query_beyond_fp16_range_is_flagged():
+    """A bf16 query value beyond 65504 cannot enter the fp16 operands of the
+    FP8-cache read: it is saturated and PA_DEVERR_RANGE is raised."""
+    w = W.make_workload("fp8_range", q_lens=[1, 3], past_lens=[50, 7], num_heads=4, **W.GLM,
+                        block_size=16, seed=30, cache_dtype="e4m3")
+    w.query[0, 5] = 3.0e5
+    got = Hn.run_gpu(w)
+    assert got["flags"] & B.PA_DEVERR_RANGE
+    from oracle import pa_oracle as O
+    assert np.isfinite(O.bits_to_f64(got["out"], "bf16")).all()
+
+
+def test_fp8_cache_not_built_paths_say_so():
+    """FP8 on the CTA-pair geometry (576/512) and on the portable kernels is
+    not built: the read calls return PA_ERR_NOT_IMPLEMENTED before any
+    launch."""
+    for kw, portable in ((dict(num_heads=16, **W.DSV3), False), (dict(num_heads=4, **W.GLM), True)):
+        w = W.make_workload("fp8_nyi", q_lens=[1], past_lens=[10], block_size=16, seed=31,
+                            cache_dtype="e4m3", **kw)
+        with pytest.raises(B.PaError) as e:
+            Hn.run_gpu(w, portable=portable)
+        assert e.value.status == B.PA_ERR_NOT_IMPLEMENTED
+
+
 @pytest.mark.parametrize("hs,vhs,ro,rd,H,family", [
     (64, 64, 0, 0, 2, 1), (576, 512, 512, 64, 16, 1), (256, 200, 128, 128, 3, 1),
     (1024, 512, 960, 64, 2, 0), (128, 128, 64, 64, 100, 1), (80, 48, 16, 64, 5, 1),

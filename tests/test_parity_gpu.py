@@ -78,6 +78,22 @@ def test_peaked_decode_parity(name, gain):
     print(f"RATIO {w.name}: max abs err {err:.3e}, {ratio:.3f} of the scale-aware bound")
 
 
+def test_fp8_cache_glm_decode_parity(oracle_results):
+    """GLM-style decode (H=64, 192/128, 32 sequences, contexts U[1024, 8192])
+    over an FP8 (E4M3) latent cache with k_scale = 1/64: the written codes
+    are bit-exact outside the rotary channels and within one code inside;
+    the outputs meet the bounds against the oracle of the FP8 operator."""
+    name = "glm_decode_fp8"
+    w = Hn.workload(name)
+    got = Hn.run_gpu(w)
+    ref = _oracle(oracle_results, name)
+    assert got["flags"] == 0
+    assert got["op"].kernel_family(0) == 1
+    Hn.check_cache(w, got["cache"], ref["cache"])
+    err, ratio = Hn.check_out(w, got["out"], ref["out"], scales=ref["scales"])
+    print(f"RATIO {name}: max abs err {err:.3e}, {ratio:.3f} of the scale-aware bound")
+
+
 def test_single_key_rows_are_exact():
     """A token at position 0 sees only its own row: its output equals the
     written cache row's value channels exactly (the pages' "first token
