@@ -28,8 +28,10 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
     // the copies in flight from HBM).
     Shape t{g.hs, vg, 1, vg > 128 ? 64 : 128, 2, (ph == Phase::kDecode && g.H <= 64) ? 64 : 128,
             2, false};
-    t.stages8 = (kSmemBudget - 1024 - q_bytes(t) - 2 * stage_bytes(t)) / stage8_bytes(t);
+    if (g.hs == 192 && vg == 128 && t.qr == 64) t.stages = kFp8Stages16;
+    t.stages8 = (kSmemBudget - 1024 - q_bytes(t) - t.stages * stage_bytes(t)) / stage8_bytes(t);
     if (t.stages8 > 8) t.stages8 = 8;
+    if (g.hs == 192 && vg == 128 && t.qr == 64 && t.stages8 > kFp8Stages8) t.stages8 = kFp8Stages8;
     if (t.stages8 < 2 || tmem_cols_used(t) > 512) return false;
     *s = t;
     return true;
@@ -62,8 +64,8 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
 template <typename T>
 cudaError_t launch_single(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
                           const Shape& s) {
-  if (s.stages8) return launch_fp8<T>(g, ph, a, P, nq, s);
   if (fixed_shape(s)) return launch_fixed<T>(g, ph, a, P, nq, s);
+  if (s.stages8) return launch_fp8<T>(g, ph, a, P, nq, s);
   if (s.n == 128 && s.qr == 64) return launch_shape<T, 128, 64, 2, 0, 0, 0>(g, ph, a, P, nq, s);
   if (s.n == 128) return launch_shape<T, 128, 128, 2, 0, 0, 0>(g, ph, a, P, nq, s);
   if (s.nb == 1) return launch_shape<T, 64, 128, 1, 0, 0, 0>(g, ph, a, P, nq, s);

@@ -930,9 +930,17 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   return e;
 }
 
+// FP8-cache decode at 192/128 with H <= 64: fp16 key stages and E4M3 stages
+// (GLM-style decode: 37.2 us per decode call with 3 + 2, 39.2 us with 2 + 4;
+// a tile holds its fp16 stage from conversion through PV).
+constexpr int kFp8Stages16 = 3, kFp8Stages8 = 2;
+
 // The 192/128 shapes compiled with their geometry fixed (pa_tc_glm.cu).
 inline bool fixed_shape(const Shape& s) {
-  if (s.hs != 192 || s.vg != 128 || s.pair || s.stages8) return false;
+  if (s.hs != 192 || s.vg != 128 || s.pair) return false;
+  if (s.stages8)
+    return s.n == 128 && s.qr == 64 && s.nb == 2 && s.stages == kFp8Stages16 &&
+           s.stages8 == kFp8Stages8;
   return (s.n == 128 && s.qr == 64 && s.nb == 2 && s.stages == 4) ||
          (s.n == 64 && s.qr == 128 && s.nb == 1 && s.stages == 2) ||
          (s.n == 128 && s.qr == 128 && s.nb == 2 && s.stages == 3);
