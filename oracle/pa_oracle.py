@@ -444,3 +444,157 @@ def run_operator_bits(query_bits, key_bits, cache_bits, cos_bits, sin_bits, cums
         return stored.reshape(shape), round_f64_to_bits(out, dt), out
     sc = res[1].reshape(out.shape[0], 3, -1)
     return stored.reshape(shape), round_f64_to_bits(out, dt), out, sc
+
+
+# ---------------------------------------------------------------------------
+# SEPARATE layout: grouped-query attention over separate key and value caches
+# ---------------------------------------------------------------------------
+# The second dense mode of the op (PR #1940 page: the oracle covers
+# "SEPARATE (GQA, RoPE, softcap, local window, head_sink, q/k RMSNorm)";
+# "num_heads % kv_num_heads == 0"; the ORT v1.29 input list on the PR #1978
+# page: value(2), value_cache(4), head_sink(11), q_norm_weight(12),
+# k_norm_weight(13)). Readings where the pages are silent: key_cache is
+# [num_blocks, bs, kv_num_heads, hs] and value_cache [num_blocks, bs,
+# kv_num_heads, vhs] (slot-major like the LATENT cache); query head h reads kv
+# head h // (num_heads / kv_num_heads); RMSNorm y = x / sqrt(mean(x^2) + eps) * w
+# over a head's hs channels with one weight vector for all heads, applied
+# before RoPE; the sink is one raw logit per query head (no scale, no
+# softcap) that joins the softmax denominator only; values get neither norm
+# nor rotation.
+
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """x / sqrt(mean(x^2) + eps) * w over the last axis (float64)."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * w
+
+
+def separate_write(key, value, cos_tab, sin_tab, slot_mapping, cumseq, past, kcache, vcache,
+                   p: dict, k_norm=None):
+    """Write phase, SEPARATE layout. ``key(t)`` -> float64 [kvH, hs] and
+    ``value(t)`` -> [kvH, vhs] (arrays or callables). For every token with
+    slot >= 0 and every kv head g: k = RoPE(RMSNorm(key[t, g]) if k_norm
+    else key[t, g]) is stored at cache row slot * kvH + g, and value[t, g]
+    unchanged at the same row of the value cache (both rounded by the
+    caches)."""
+    kvh = p["kv_num_heads"]
+    get_k = key if callable(key) else (lambda t: key[t])
+    get_v = value if callable(value) else (lambda t: value[t])
+    for t in range(len(slot_mapping)):
+        slot = int(slot_mapping[t])
+        if slot < 0:  # slot -1: this token's rows are not written
+            continue
+        if (slot + 1) * kvh > kcache.num_rows:
+            raise ValueError(f"slot {slot} outside the cache")
+        _, pos = locate_token(t, cumseq, past)
+        k, v = get_k(t), get_v(t)
+        for g in range(kvh):
+            kg = rms_norm(k[g], k_norm, p["rms_eps"]) if k_norm is not None else k[g]
+            kcache.put(slot * kvh + g, rope_row(kg, pos, p["rotary_offset"], p["rotary_dim"],
+                                                cos_tab, sin_tab, bool(p["rotary_interleaved"])))
+            vcache.put(slot * kvh + g, v[g])
+    return kcache, vcache
+
+
+def separate_attend_token(t: int, q_row: np.ndarray, kcache, vcache, cos_tab, sin_tab, cumseq,
+                          past, block_table, p: dict, head_sink=None, q_norm=None,
+                          stats: bool = False):
+    """Read phase, SEPARATE layout, token t, all query heads: float64
+    [H, vhs]. q_h = RoPE(RMSNorm(q_row[h]) if q_norm else q_row[h]); keys
+    and values of the visible positions j are rows (block_table[b, j // bs]
+    * bs + j % bs) * kvH + g of the caches, g = h // (H / kvH); s_hj = scale
+    * q_h . K_j, softcap as in the LATENT mode; with a sink logit z_h the
+    softmax is exp(s_hj - m) / (sum_j exp(s_hj - m) + exp(z_h - m)), m =
+    max(max_j s_hj, z_h); out_h = sum_j p_hj V_j (zero when no key is
+    visible). ``stats``: also the ``error_scales`` [3, H, vhs]."""
+    H, kvh = p["num_heads"], p["kv_num_heads"]
+    hs = p["head_size"]
+    vhs = p["v_head_size"] or hs
+    grp = H // kvh
+    bs = p["block_size"]
+    num_blocks = kcache.num_rows // (bs * kvh)
+    b, pos = locate_token(t, cumseq, past)
+    keys = list(visible_keys(pos, p["local_window_size"]))
+    out = np.zeros((H, vhs))
+    scales = np.zeros((3, H, vhs))
+    slots = [cache_row_index(b, j, block_table, bs, num_blocks) for j in keys]
+    for h in range(H):
+        g = h // grp
+        qh = q_row[h * hs:(h + 1) * hs]
+        if q_norm is not None:
+            qh = rms_norm(qh, q_norm, p["rms_eps"])
+        qh = rope_row(qh, pos, p["rotary_offset"], p["rotary_dim"], cos_tab, sin_tab,
+                      bool(p["rotary_interleaved"]))
+        if not keys:
+            continue
+        K = kcache.get([s * kvh + g for s in slots])
+        V = vcache.get([s * kvh + g for s in slots])
+        s = (K @ qh) * p["scale"]
+        cap = p["softcap"]
+        if cap > 0.0:
+            s = cap * np.tanh(s / cap)
+        m = s.max()
+        extra = 0.0
+        if head_sink is not None:
+            m = max(m, float(head_sink[h]))
+            extra = np.exp(float(head_sink[h]) - m)
+        w = np.exp(s - m)
+        den = w.sum() + extra
+        out[h] = (w @ V) / den
+        if stats:
+            # the probability, query-rounding and diagonal terms, with V a
+            # separate matrix (the diagonal term needs K_jc = V_jc, which only
+            # holds when the value rows are the key rows; it is omitted here)
+            prob = (w / den)[None, :]
+            sc = error_scales_kv(qh[None, :], K, V, prob, out[h][None, :], p["scale"])
+            scales[:, h, :] = sc[:, 0, :]
+    return (out, scales) if stats else out
+
+
+def error_scales_kv(q: np.ndarray, K: np.ndarray, V: np.ndarray, prob: np.ndarray,
+                    out: np.ndarray, scale: float) -> np.ndarray:
+    """``error_scales`` for separate key and value rows (TEST-TOLERANCE
+    HELPER): n_p = sqrt(sum_j p_j^2 V_jc^2), n_q = sqrt(sum_j p_j^2 g_j^2
+    (V_jc - out_c)^2) with g_j = scale * sqrt(sum_d q_d^2 K_jd^2), and n_d =
+    0 (no query channel meets a value channel in every score). [3, H, vhs]."""
+    V2 = V * V
+    n_p = np.sqrt(np.maximum(np.square(prob) @ V2, 0.0))
+    g2 = (scale * scale) * ((q * q) @ (K * K).T)
+    a = prob * prob * g2
+    var_a = (a @ V2) - 2.0 * (a @ V) * out + out * out * a.sum(axis=1, keepdims=True)
+    n_q = np.sqrt(np.maximum(var_a, 0.0))
+    return np.stack([n_p, n_q, np.zeros_like(n_p)])
+
+
+def run_separate_bits(query_bits, key_bits, value_bits, kcache_bits, vcache_bits, cos_bits,
+                      sin_bits, cumseq, past, block_table, slot_mapping, p: dict,
+                      head_sink_bits=None, q_norm_bits=None, k_norm_bits=None, tokens=None,
+                      stats: bool = False):
+    """SEPARATE write then read on uint16 bit arrays of the operator dtype:
+    query [T, H*hs], key [T, kvH*hs], value [T, kvH*vhs], caches
+    [num_blocks, bs, kvH, hs|vhs], head_sink [H], norm weights [hs]. Returns
+    (key cache bits, value cache bits, output bits [len(tokens), H*vhs],
+    output float64[, error scales [len(tokens), 3, H*vhs]])."""
+    dt = p["dtype"]
+    hs, kvh = p["head_size"], p["kv_num_heads"]
+    vhs = p["v_head_size"] or hs
+    kc = BitsCache(np.asarray(kcache_bits).reshape(-1, hs), dt)
+    vc = BitsCache(np.asarray(vcache_bits).reshape(-1, vhs), dt)
+    cos_t, sin_t = bits_to_f64(cos_bits, dt), bits_to_f64(sin_bits, dt)
+    kn = None if k_norm_bits is None else bits_to_f64(k_norm_bits, dt)
+    qn = None if q_norm_bits is None else bits_to_f64(q_norm_bits, dt)
+    sink = None if head_sink_bits is None else bits_to_f64(head_sink_bits, dt)
+    separate_write(lambda t: bits_to_f64(key_bits[t], dt).reshape(kvh, hs),
+                   lambda t: bits_to_f64(value_bits[t], dt).reshape(kvh, vhs), cos_t, sin_t,
+                   np.asarray(slot_mapping), cumseq, past, kc, vc, p, kn)
+    tokens = range(int(cumseq[-1])) if tokens is None else tokens
+    res = [separate_attend_token(int(t), bits_to_f64(query_bits[int(t)], dt), kc, vc, cos_t,
+                                 sin_t, cumseq, past, block_table, p, sink, qn, stats)
+           for t in tokens]
+    if stats:
+        out = np.stack([r[0] for r in res]).reshape(len(res), -1)
+        sc = np.stack([r[1] for r in res]).reshape(len(res), 3, -1)
+    else:
+        out = np.stack(res).reshape(len(res), -1)
+    shp_k, shp_v = np.asarray(kcache_bits).shape, np.asarray(vcache_bits).shape
+    ret = (kc.bits.reshape(shp_k), vc.bits.reshape(shp_v), round_f64_to_bits(out, dt), out)
+    return ret + (sc,) if stats else ret

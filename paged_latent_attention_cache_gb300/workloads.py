@@ -400,3 +400,147 @@ def oracle_params(w: "Workload") -> Dict[str, object]:
     if w.cache_dtype is None:
         p.pop("k_scale")
     return p
+
+
+# ---------------------------------------------------------------------------
+# SEPARATE layout (grouped-query attention over separate key / value caches)
+# ---------------------------------------------------------------------------
+
+@dataclass
+class SeparateWorkload:
+    """Inputs of the op's SEPARATE mode: query [T, H*hs], key [T, kvH*hs],
+    value [T, kvH*vhs], key_cache [num_blocks, bs, kvH, hs], value_cache
+    [num_blocks, bs, kvH, vhs], optional head_sink [H] (a sink logit per
+    query head) and q/k RMSNorm weights [hs]; the index tensors as in
+    ``Workload``."""
+    name: str
+    dtype: torch.dtype
+    num_heads: int
+    kv_num_heads: int
+    head_size: int
+    v_head_size: int
+    rotary_offset: int
+    rotary_dim: int
+    rotary_interleaved: int
+    block_size: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    cos_rows: int
+    scale: float
+    softcap: float
+    local_window_size: int
+    rms_eps: float
+    q_lens: List[int]
+    past_lens: List[int]
+    num_decode_seqs: int
+    query: torch.Tensor
+    key: torch.Tensor
+    value: torch.Tensor
+    key_cache: torch.Tensor
+    value_cache: torch.Tensor
+    cos_cache: torch.Tensor
+    sin_cache: torch.Tensor
+    cumseq: torch.Tensor
+    past: torch.Tensor
+    block_table: torch.Tensor
+    slot_mapping: torch.Tensor
+    head_sink: Optional[torch.Tensor] = None
+    q_norm_weight: Optional[torch.Tensor] = None
+    k_norm_weight: Optional[torch.Tensor] = None
+    meta: Dict[str, object] = field(default_factory=dict)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query.shape[0])
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.q_lens)
+
+    def params(self) -> Dict[str, object]:
+        return dict(dtype=self.dtype, num_heads=self.num_heads, kv_num_heads=self.kv_num_heads,
+                    head_size=self.head_size, v_head_size=self.v_head_size,
+                    rotary_offset=self.rotary_offset, rotary_dim=self.rotary_dim,
+                    rotary_interleaved=self.rotary_interleaved, cos_rows=self.cos_rows,
+                    block_size=self.block_size, num_blocks=self.num_blocks,
+                    max_blocks_per_seq=self.max_blocks_per_seq, scale=self.scale,
+                    softcap=self.softcap, local_window_size=self.local_window_size,
+                    rms_eps=self.rms_eps)
+
+    def to(self, device) -> "SeparateWorkload":
+        out = SeparateWorkload(**{k: getattr(self, k) for k in self.__dataclass_fields__})
+        for k in ("query", "key", "value", "key_cache", "value_cache", "cos_cache", "sin_cache",
+                  "cumseq", "past", "block_table", "slot_mapping", "head_sink", "q_norm_weight",
+                  "k_norm_weight"):
+            v = getattr(self, k)
+            setattr(out, k, None if v is None else v.to(device))
+        out.meta = dict(self.meta)
+        return out
+
+
+def make_separate_workload(name: str, q_lens: Sequence[int], past_lens: Sequence[int], *,
+                           dtype=torch.bfloat16, num_heads: int, kv_num_heads: int,
+                           head_size: int, v_head_size: Optional[int] = None,
+                           rotary_offset: int = 0, rotary_dim: Optional[int] = None,
+                           rotary_interleaved: int = 0, block_size: int,
+                           num_blocks: Optional[int] = None,
+                           max_blocks_per_seq: Optional[int] = None,
+                           cos_rows: Optional[int] = None, scale: Optional[float] = None,
+                           softcap: float = 0.0, local_window_size: int = -1,
+                           rms_eps: float = 1e-6, head_sink: bool = False,
+                           qk_norm: bool = False, seed: int = 0, std: float = 0.5,
+                           drop_slots: int = 0, drop_frac: float = 0.0) -> SeparateWorkload:
+    """Draw one seeded SEPARATE-layout batch: the block placement, offsets
+    and slots as ``make_workload`` draws them; query/key/value and both
+    cache pools N(0, std^2); sink logits N(0, 1) per query head; RMSNorm
+    weights N(1, 0.2^2). Sequences with one new token come first."""
+    base = make_workload(name, q_lens, past_lens, dtype=dtype, num_heads=num_heads,
+                         head_size=head_size, v_head_size=v_head_size or head_size,
+                         rotary_offset=rotary_offset,
+                         rotary_dim=head_size if rotary_dim is None else rotary_dim,
+                         rotary_interleaved=rotary_interleaved, block_size=block_size,
+                         num_blocks=num_blocks, max_blocks_per_seq=max_blocks_per_seq,
+                         cos_rows=cos_rows, scale=scale, softcap=softcap,
+                         local_window_size=local_window_size, seed=seed, std=std,
+                         drop_slots=drop_slots, drop_frac=drop_frac)
+    assert num_heads % kv_num_heads == 0
+    vhs = base.v_head_size
+    gen = torch.Generator().manual_seed(seed + 7777)
+    T = base.num_tokens
+    key = _normal((T, kv_num_heads * head_size), gen, std, dtype)
+    value = _normal((T, kv_num_heads * vhs), gen, std, dtype)
+    kc = _normal((base.num_blocks, block_size, kv_num_heads, head_size), gen, std, dtype)
+    vc = _normal((base.num_blocks, block_size, kv_num_heads, vhs), gen, std, dtype)
+    sink = (torch.randn(num_heads, generator=gen)).to(dtype) if head_sink else None
+    qn = (1.0 + 0.2 * torch.randn(head_size, generator=gen)).to(dtype) if qk_norm else None
+    kn = (1.0 + 0.2 * torch.randn(head_size, generator=gen)).to(dtype) if qk_norm else None
+    return SeparateWorkload(
+        name=name, dtype=dtype, num_heads=num_heads, kv_num_heads=kv_num_heads,
+        head_size=head_size, v_head_size=vhs, rotary_offset=base.rotary_offset,
+        rotary_dim=base.rotary_dim, rotary_interleaved=rotary_interleaved,
+        block_size=block_size, num_blocks=base.num_blocks,
+        max_blocks_per_seq=base.max_blocks_per_seq, cos_rows=base.cos_rows, scale=base.scale,
+        softcap=softcap, local_window_size=local_window_size, rms_eps=rms_eps,
+        q_lens=base.q_lens, past_lens=base.past_lens, num_decode_seqs=base.num_decode_seqs,
+        query=base.query, key=key, value=value, key_cache=kc, value_cache=vc,
+        cos_cache=base.cos_cache, sin_cache=base.sin_cache, cumseq=base.cumseq, past=base.past,
+        block_table=base.block_table, slot_mapping=base.slot_mapping, head_sink=sink,
+        q_norm_weight=qn, k_norm_weight=kn, meta=dict(seed=seed, std=std))
+
+
+def gqa_decode(seed: int = 9, batch: int = 32) -> SeparateWorkload:
+    """Grouped-query decode: 32 query heads over 8 kv heads, head size 128
+    with full RoPE, batch 32 x one new token, contexts uniform in
+    [1024, 8192], bs = 64, q/k RMSNorm and a sink logit per head."""
+    g = torch.Generator().manual_seed(seed * 7919 + 1)
+    ctx = torch.randint(1024, 8193, (batch,), generator=g).tolist()
+    return make_separate_workload("gqa_decode", q_lens=[1] * batch,
+                                  past_lens=[c - 1 for c in ctx], num_heads=32, kv_num_heads=8,
+                                  head_size=128, block_size=64, cos_rows=8192, seed=seed,
+                                  head_sink=True, qk_norm=True)
+
+
+def separate_oracle_params(w: SeparateWorkload) -> Dict[str, object]:
+    p = w.params()
+    p["dtype"] = dtype_tag(w.dtype)
+    return p

@@ -43,6 +43,12 @@ MUTANTS = {
     "fp8_read_unscaled": ("return e4m3_to_f64(self.codes[idx]) * self.k_scale",
                           "return e4m3_to_f64(self.codes[idx])"),
     "fp8_multiplies": ("q32 = v32 / np.float32(k_scale)", "q32 = v32 * np.float32(k_scale)"),
+    "sep_kv_head_wrong": ("        g = h // grp\n", "        g = h % kvh\n"),
+    "sep_sink_not_in_denominator": ("        den = w.sum() + extra", "        den = w.sum()"),
+    "sep_rms_sum": ("np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)",
+                    "np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)"),
+    "sep_value_rotated": ("            vcache.put(slot * kvh + g, v[g])",
+                          "            vcache.put(slot * kvh + g, rope_row(v[g], pos, p[\"rotary_offset\"], p[\"rotary_dim\"], cos_tab, sin_tab, False))"),
 }
 
 PINS = [
@@ -68,6 +74,14 @@ PINS = [
     lambda: pins.test_fp8_write_is_exact_for_representable_rows(),
     lambda: pins.test_fp8_read_equals_plain_read_of_dequantized_cache(),
     lambda: pins.test_fp8_quantization_divides_by_k_scale_in_float32(),
+    lambda: pins.test_separate_matches_naive_dense(dict(num_heads=4, kv_num_heads=2, head_size=32,
+                                                        rotary_dim=16)),
+    lambda: pins.test_separate_matches_naive_dense(dict(num_heads=8, kv_num_heads=2, head_size=64,
+                                                        rotary_dim=64, head_sink=True,
+                                                        qk_norm=True, softcap=2.0,
+                                                        local_window_size=5)),
+    lambda: pins.test_rms_norm_matches_torch(),
+    lambda: pins.test_head_sink_closed_forms(),
 ]
 
 

@@ -691,3 +691,227 @@ def test_fp8_quantization_divides_by_k_scale_in_float32():
                        .astype(np.int64))
     assert np.all(np.abs(dec - q) <= spacing / 2 + 1e-12)
     assert np.isfinite(vals[got]).all()
+
+
+# ---------------------------------------------------------------------------
+# SEPARATE layout (grouped-query attention, head sink, q/k RMSNorm)
+# ---------------------------------------------------------------------------
+
+def _sep_params(**kw):
+    p = dict(dtype="bf16", num_heads=4, kv_num_heads=2, head_size=32, v_head_size=32,
+             rotary_offset=0, rotary_dim=16, rotary_interleaved=0, cos_rows=64, block_size=16,
+             num_blocks=8, max_blocks_per_seq=4, scale=0.2, softcap=0.0, local_window_size=-1,
+             rms_eps=1e-6)
+    p.update(kw)
+    return p
+
+
+def _complex_rope(x, pos, rd, theta=10000.0):
+    """Half-split RoPE of x's first rd channels as a complex rotation (float64)."""
+    half = rd // 2
+    ang = pos * theta ** (-2.0 * np.arange(half) / rd)
+    z = (x[:half] + 1j * x[half:rd]) * np.exp(1j * ang)
+    return np.concatenate([z.real, z.imag, x[rd:]])
+
+
+def _sep_case(seed, **kw):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    w = W.make_separate_workload("pin", q_lens=[1, 6, 3], past_lens=[21, 4, 30], block_size=16,
+                                 seed=seed, cos_rows=64, **kw)
+    p = W.separate_oracle_params(w)
+    return w, p
+
+
+def _naive_separate(w, p):
+    """Per sequence: contiguous keys/values (cached rows below the sequence's
+    past, new rows from the inputs: RMSNorm by torch, RoPE as a complex
+    rotation with exact angles, rounded to bf16 by torch), then per query
+    head a softmax over the visible keys and the sink logit."""
+    from paged_latent_attention_cache_gb300 import workloads as W
+    dt = torch.bfloat16
+    f = lambda t: t.to(torch.float64).numpy()
+    H, kvh, hs, vhs, bs = w.num_heads, w.kv_num_heads, w.head_size, w.v_head_size, w.block_size
+    grp = H // kvh
+    kc = f(w.key_cache).reshape(-1, kvh, hs)
+    vc = f(w.value_cache).reshape(-1, kvh, vhs)
+    out = []
+    cs = w.cumseq.tolist()
+    for b in range(w.num_seqs):
+        P, q = w.past_lens[b], w.q_lens[b]
+        ctx = P + q
+        Ks, Vs = np.zeros((ctx, kvh, hs)), np.zeros((ctx, kvh, vhs))
+        for j in range(P):
+            row = int(w.block_table[b, j // bs]) * bs + j % bs
+            Ks[j], Vs[j] = kc[row], vc[row]
+        for i in range(q):
+            t = cs[b] + i
+            kt = w.key[t].view(kvh, hs).to(torch.float32)
+            if w.k_norm_weight is not None:
+                kt = torch.nn.functional.rms_norm(kt.double(), (hs,), w.k_norm_weight.double(),
+                                                  eps=w.rms_eps)
+            kt = kt.double().numpy()
+            for g in range(kvh):
+                r = _complex_rope(kt[g], P + i, w.rotary_dim)
+                Ks[P + i, g] = torch.from_numpy(r).to(dt).double().numpy()
+            Vs[P + i] = f(w.value[t].view(kvh, vhs))
+        for i in range(q):
+            t, pos = cs[b] + i, P + i
+            lo = 0 if w.local_window_size < 0 else max(0, pos - w.local_window_size)
+            o = np.zeros((H, vhs))
+            for h in range(H):
+                qh = w.query[t, h * hs:(h + 1) * hs].double()
+                if w.q_norm_weight is not None:
+                    qh = torch.nn.functional.rms_norm(qh, (hs,), w.q_norm_weight.double(),
+                                                      eps=w.rms_eps)
+                qh = _complex_rope(qh.numpy(), pos, w.rotary_dim)
+                K, V = Ks[lo:pos + 1, h // grp], Vs[lo:pos + 1, h // grp]
+                s = w.scale * (K @ qh)
+                if w.softcap > 0:
+                    s = w.softcap * np.tanh(s / w.softcap)
+                z = [] if w.head_sink is None else [float(w.head_sink[h])]
+                m = max([s.max()] + z)
+                e = np.exp(s - m)
+                o[h] = (e @ V) / (e.sum() + sum(np.exp(zz - m) for zz in z))
+            out.append(o.reshape(-1))
+    return np.stack(out)
+
+
+def _sep_oracle(w, p, tokens=None, stats=False):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    tb = W.to_bits
+    return O.run_separate_bits(
+        tb(w.query), tb(w.key), tb(w.value), tb(w.key_cache), tb(w.value_cache),
+        _exact_bits(w.cos_cache), _exact_bits(w.sin_cache), w.cumseq.numpy(), w.past.numpy(),
+        w.block_table.numpy(), w.slot_mapping.numpy(), p,
+        None if w.head_sink is None else tb(w.head_sink),
+        None if w.q_norm_weight is None else tb(w.q_norm_weight),
+        None if w.k_norm_weight is None else tb(w.k_norm_weight), tokens, stats)
+
+
+def _exact_bits(t):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    return W.to_bits(t)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(num_heads=4, kv_num_heads=2, head_size=32, rotary_dim=16),
+    dict(num_heads=4, kv_num_heads=4, head_size=32, rotary_dim=32, head_sink=True),
+    dict(num_heads=6, kv_num_heads=1, head_size=48, rotary_dim=32, qk_norm=True),
+    dict(num_heads=8, kv_num_heads=2, head_size=64, rotary_dim=64, head_sink=True, qk_norm=True,
+         softcap=2.0, local_window_size=5),
+], ids=["gqa", "mha_sink", "mqa_norm", "all_options"])
+def test_separate_matches_naive_dense(kw):
+    """The SEPARATE oracle equals a naive per-sequence contiguous attention
+    written from the definitions (torch RMSNorm, complex RoPE with exact
+    angles: the tolerance covers the cos/sin tables' bf16 rounding)."""
+    w, p = _sep_case(41, **kw)
+    # exact angles in the naive form; the oracle reads the bf16 tables
+    got = _sep_oracle(w, p)[3]
+    ref = _naive_separate(w, p)
+    assert np.abs(got - ref).max() < 2e-2 * max(1.0, np.abs(ref).max())
+    # with exact float64 tables the two agree to rounding of the stored keys
+    p64 = dict(p)
+    w64 = w
+    cos, sin, _ = _exact_tables(w.cos_rows, w.rotary_dim)
+    kc, vc = (O.BitsCache(W_bits(w.key_cache).reshape(-1, w.head_size), "bf16"),
+              O.BitsCache(W_bits(w.value_cache).reshape(-1, w.v_head_size), "bf16"))
+    f = lambda t: O.bits_to_f64(W_bits(t), "bf16")
+    kn = None if w.k_norm_weight is None else f(w.k_norm_weight)
+    qn = None if w.q_norm_weight is None else f(w.q_norm_weight)
+    sink = None if w.head_sink is None else f(w.head_sink)
+    O.separate_write(lambda t: f(w.key)[t].reshape(w.kv_num_heads, -1),
+                     lambda t: f(w.value)[t].reshape(w.kv_num_heads, -1), cos, sin,
+                     w.slot_mapping.numpy(), w.cumseq.numpy(), w.past.numpy(), kc, vc, p64, kn)
+    q = f(w.query)
+    exact = np.stack([O.separate_attend_token(t, q[t], kc, vc, cos, sin, w.cumseq.numpy(),
+                                              w.past.numpy(), w.block_table.numpy(), p64, sink,
+                                              qn).reshape(-1) for t in range(w.num_tokens)])
+    assert np.abs(exact - ref).max() < 1e-9 + 4e-3 * np.abs(ref).max()
+
+
+def W_bits(t):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    return W.to_bits(t)
+
+
+def test_rms_norm_matches_torch():
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal((7, 64)) * 3
+    w = rng.standard_normal(64)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), torch.from_numpy(w),
+                                       eps=1e-6).numpy()
+    assert np.allclose(O.rms_norm(x, w, 1e-6), ref, rtol=1e-13, atol=1e-13)
+
+
+def test_head_sink_closed_forms():
+    """One visible key with score s and sink z: out = V * e^s / (e^s + e^z);
+    a sink of -inf-like size changes nothing; a huge sink sends the output
+    to zero."""
+    p = _sep_params(num_heads=2, kv_num_heads=1, rotary_dim=0, head_size=16, v_head_size=16,
+                    block_size=16, num_blocks=1, max_blocks_per_seq=1, scale=0.5)
+    rng = np.random.default_rng(43)
+    K = rng.standard_normal((16, 16))
+    V = rng.standard_normal((16, 16))
+    kc, vc = O.F64Cache(K), O.F64Cache(V)
+    q = rng.standard_normal(32)
+    args = (kc, vc, None, None, np.array([0, 1]), np.array([0]), np.array([[0]]), p)
+    for z in (-0.7, 1.3):
+        out = O.separate_attend_token(0, q, *args, head_sink=np.array([z, z]))
+        for h in range(2):
+            s = 0.5 * q[h * 16:(h + 1) * 16] @ K[0]
+            assert np.allclose(out[h], V[0] * np.exp(s) / (np.exp(s) + np.exp(z)), rtol=1e-12)
+    plain = O.separate_attend_token(0, q, *args)
+    assert np.allclose(O.separate_attend_token(0, q, *args, head_sink=np.array([-1e4, -1e4])),
+                       plain, rtol=1e-12)
+    assert np.abs(O.separate_attend_token(0, q, *args, head_sink=np.array([1e4, 1e4]))).max() == 0
+
+
+def test_separate_reduces_to_latent():
+    """One kv head, values equal to the keys, no rotation, no norm, no sink:
+    the SEPARATE read equals the LATENT read with v_head_size == head_size."""
+    rng = np.random.default_rng(44)
+    rows = rng.standard_normal((8 * 16, 32))
+    q = rng.standard_normal((5, 4 * 32))
+    cumseq, past, bt = np.array([0, 2, 5]), np.array([17, 30]), rng.permutation(8).reshape(2, 4)
+    ps = _sep_params(kv_num_heads=1, rotary_dim=0)
+    pl = _params(rotary_dim=0, rotary_offset=0, v_head_size=32, num_heads=4)
+    sep = np.stack([O.separate_attend_token(t, q[t], O.F64Cache(rows), O.F64Cache(rows), None,
+                                            None, cumseq, past, bt, ps) for t in range(5)])
+    lat = O.latent_attend(q, O.F64Cache(rows), None, None, cumseq, past, bt, pl)
+    assert np.allclose(sep, lat, rtol=1e-12, atol=1e-14)
+
+
+def test_separate_placement_invariance_and_slot_minus_one():
+    """Permuting the physical blocks (block table and slots remapped) leaves
+    the outputs bit-identical; slot -1 tokens leave both caches untouched."""
+    w, p = _sep_case(45, num_heads=4, kv_num_heads=2, head_size=32, rotary_dim=16,
+                     head_sink=True, qk_norm=True, drop_slots=2)
+    kb, vb, ob, _ = _sep_oracle(w, p)
+    nb, bs = w.num_blocks, w.block_size
+    perm = np.random.default_rng(46).permutation(nb)
+    inv = np.argsort(perm)
+    w2 = copy_sep(w)
+    w2.key_cache = w.key_cache[inv]
+    w2.value_cache = w.value_cache[inv]
+    bt = w.block_table.numpy().copy()
+    bt[bt >= 0] = perm[bt[bt >= 0]]
+    w2.block_table = torch.from_numpy(bt)
+    sl = w.slot_mapping.numpy().copy()
+    ok = sl >= 0
+    sl[ok] = perm[sl[ok] // bs] * bs + sl[ok] % bs
+    w2.slot_mapping = torch.from_numpy(sl)
+    kb2, vb2, ob2, _ = _sep_oracle(w2, p)
+    assert np.array_equal(ob, ob2)
+    skipped = w.slot_mapping.numpy()
+    untouched = np.ones(nb * bs, bool)
+    untouched[skipped[skipped >= 0]] = False
+    kv = w.kv_num_heads
+    assert np.array_equal(kb.reshape(nb * bs, -1)[untouched],
+                          W_bits(w.key_cache).reshape(nb * bs, -1)[untouched])
+    assert np.array_equal(vb.reshape(nb * bs, -1)[untouched],
+                          W_bits(w.value_cache).reshape(nb * bs, -1)[untouched])
+
+
+def copy_sep(w):
+    from paged_latent_attention_cache_gb300 import workloads as W
+    return W.SeparateWorkload(**{k: getattr(w, k) for k in w.__dataclass_fields__})
