@@ -264,6 +264,89 @@ const char* pa_latent_status_string(pa_status s);
  * (empty string if none). */
 const char* pa_latent_last_error(void);
 
+/* ======================================================================
+ * SEPARATE layout — the op's other dense mode (kv_cache_layout="SEPARATE"):
+ * grouped-query attention over separate key and value caches, with an
+ * optional sink logit per query head and optional RMSNorm of the query and
+ * key heads. The PR #1940 page lists it among the oracle's modes ("SEPARATE
+ * (GQA, RoPE, softcap, local window, head_sink, q/k RMSNorm)", "num_heads %
+ * kv_num_heads == 0"); the PR #1978 page gives the input order (value 2,
+ * value_cache 4, head_sink 11, q_norm_weight 12, k_norm_weight 13). Where
+ * the pages say no more, this library reads it as follows:
+ *   - key_cache [num_blocks, bs, kvH, hs], value_cache [num_blocks, bs, kvH,
+ *     vhs], slot-major like the LATENT cache (row slot*kvH + g);
+ *   - query head h reads kv head g = h / (H / kvH);
+ *   - RMSNorm: y = x / sqrt(mean(x^2) + rms_eps) * w over a head's hs
+ *     channels, one weight vector [hs] for all heads, in f32, before RoPE;
+ *   - head_sink[h] is a raw logit (no scale, no softcap) that joins the
+ *     softmax denominator only: out = sum_j e^(s_j-m) V_j / (sum_j e^(s_j-m)
+ *     + e^(z_h-m)), m = max(max_j s_j, z_h); values get no norm or RoPE.
+ * Conventions (ownership, errors, err_flags, streams) as for the LATENT
+ * entry points above. Kernels: tcgen05 tensor cores for head_size and
+ * v_head_size in 64..256 and up to 128 query heads per kv head (others:
+ * PA_ERR_NOT_IMPLEMENTED).
+ * ====================================================================== */
+typedef struct pa_separate_params {
+  int32_t dtype;              /* pa_dtype of every half-precision tensor             */
+  int32_t num_heads;          /* H query heads                                       */
+  int32_t kv_num_heads;       /* kvH >= 1, dividing H                                */
+  int32_t head_size;          /* hs, multiple of 16                                  */
+  int32_t v_head_size;        /* vhs in 1..hs; 0 means hs                            */
+  int32_t rotary_offset;      /* as pa_latent_params                                 */
+  int32_t rotary_dim;
+  int32_t rotary_interleaved;
+  int32_t cos_rows;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  float scale;                /* 0 selects 1/sqrt(hs)                                */
+  float softcap;
+  int32_t local_window_size;
+  float rms_eps;              /* RMSNorm epsilon (used when a norm weight is given)  */
+  int32_t flags;              /* PA_FLAG_AFTER_WRITE / PA_FLAG_OWN_SLOTS             */
+} pa_separate_params;
+
+pa_status pa_separate_validate(const pa_separate_params* p);
+
+/* Write phase: for every token t with slot_mapping[t] >= 0 and kv head g,
+ *   key_cache[slot, g]   = RoPE(RMSNorm(key[t, g]) * k_norm_weight)  (norm only
+ *                          when k_norm_weight is not NULL), rounded to the dtype;
+ *   value_cache[slot, g] = value[t, g].
+ *   key [T, kvH*hs], value [T, kvH*vhs], k_norm_weight [hs] or NULL; the rest
+ *   as pa_latent_write. head_size <= 256 and v_head_size a multiple of 8. */
+pa_status pa_separate_write(const pa_separate_params* p, const void* key, const void* value,
+                            int64_t num_tokens, const void* cos_cache, const void* sin_cache,
+                            const void* k_norm_weight, const int32_t* slot_mapping,
+                            const int32_t* cumseq, const int32_t* past, int32_t num_seqs,
+                            void* key_cache, void* value_cache, int32_t* err_flags,
+                            void* stream);
+
+/* Read phase (decode: one new token per sequence, split-KV + combine with
+ * the caller's workspace; prefill: any sequences), as defined above.
+ *   query [T, H*hs], q_norm_weight [hs] or NULL, head_sink [H] or NULL,
+ *   out [T, H*vhs]; the rest as pa_latent_decode. */
+pa_status pa_separate_decode(const pa_separate_params* p, const void* query, int64_t num_tokens,
+                             const void* key_cache, const void* value_cache,
+                             const void* cos_cache, const void* sin_cache,
+                             const void* q_norm_weight, const void* head_sink,
+                             const int32_t* cumseq, const int32_t* past,
+                             const int32_t* block_table, int32_t num_seqs, int32_t seq_begin,
+                             int32_t seq_end, void* workspace, size_t workspace_bytes, void* out,
+                             int32_t* err_flags, void* stream);
+pa_status pa_separate_prefill(const pa_separate_params* p, const void* query,
+                              int64_t num_tokens, const void* key_cache, const void* value_cache,
+                              const void* cos_cache, const void* sin_cache,
+                              const void* q_norm_weight, const void* head_sink,
+                              const int32_t* cumseq, const int32_t* past,
+                              const int32_t* block_table, int32_t num_seqs, int32_t seq_begin,
+                              int32_t seq_end, void* workspace, size_t workspace_bytes,
+                              void* out, int32_t* err_flags, void* stream);
+
+/* Workspace bytes pa_separate_decode needs for num_seqs sequences (prefill
+ * needs none); 0 for invalid parameters. */
+size_t pa_separate_workspace_size(const pa_separate_params* p, int32_t num_seqs,
+                                  int64_t num_tokens);
+
 #ifdef __cplusplus
 }
 #endif

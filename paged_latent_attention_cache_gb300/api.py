@@ -114,3 +114,74 @@ class PagedLatentAttention:
 
     def reset_error_flags(self):
         self.err_flags.zero_()
+
+
+class SeparateAttention:
+    """The op's SEPARATE mode (grouped-query attention over separate key and
+    value caches, optional head sink and q/k RMSNorm) over the C ABI: holds
+    the parameters, the decode workspace and the error word; ``forward``
+    issues write -> decode -> prefill like ``PagedLatentAttention``."""
+
+    def __init__(self, *, dtype: torch.dtype, num_heads: int, kv_num_heads: int, head_size: int,
+                 v_head_size: int = 0, rotary_offset: int = 0, rotary_dim: int = 0,
+                 rotary_interleaved: int = 0, cos_rows: int = 1, block_size: int,
+                 num_blocks: int, max_blocks_per_seq: int, scale: float = 0.0,
+                 softcap: float = 0.0, local_window_size: int = -1, rms_eps: float = 1e-6,
+                 max_seqs: int, max_tokens: int, device="cuda", own_slots: bool = False):
+        self.dtype = dtype
+        self.num_heads = num_heads
+        self.v_head_size = v_head_size or head_size
+        self.params = B.make_separate_params(
+            dtype=dtype, num_heads=num_heads, kv_num_heads=kv_num_heads, head_size=head_size,
+            v_head_size=v_head_size, rotary_offset=rotary_offset, rotary_dim=rotary_dim,
+            rotary_interleaved=rotary_interleaved, cos_rows=cos_rows, block_size=block_size,
+            num_blocks=num_blocks, max_blocks_per_seq=max_blocks_per_seq, scale=scale,
+            softcap=softcap, local_window_size=local_window_size, rms_eps=rms_eps)
+        s = B.pa_separate_validate(self.params)
+        if s != B.PA_OK:
+            raise B.PaError(s, B.last_error())
+        self.params_after_write = B.pa_separate_params.from_buffer_copy(self.params)
+        self.params_after_write.flags |= B.PA_FLAG_AFTER_WRITE | (
+            B.PA_FLAG_OWN_SLOTS if own_slots else 0)
+        self.device = torch.device(device)
+        n = B.pa_separate_workspace_size(self.params, max_seqs, max_tokens)
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=self.device) if n else None
+        self.err_flags = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    @classmethod
+    def from_workload(cls, w, device="cuda", own_slots=True) -> "SeparateAttention":
+        return cls(dtype=w.dtype, num_heads=w.num_heads, kv_num_heads=w.kv_num_heads,
+                   head_size=w.head_size, v_head_size=w.v_head_size,
+                   rotary_offset=w.rotary_offset, rotary_dim=w.rotary_dim,
+                   rotary_interleaved=w.rotary_interleaved, cos_rows=w.cos_rows,
+                   block_size=w.block_size, num_blocks=w.num_blocks,
+                   max_blocks_per_seq=w.max_blocks_per_seq, scale=w.scale, softcap=w.softcap,
+                   local_window_size=w.local_window_size, rms_eps=w.rms_eps,
+                   max_seqs=w.num_seqs, max_tokens=max(w.num_tokens, 1), device=device,
+                   own_slots=own_slots)
+
+    def forward(self, query, key, value, key_cache, value_cache, cos_cache, sin_cache, cumseq,
+                past, block_table, slot_mapping, num_decode_seqs: int, head_sink=None,
+                q_norm_weight=None, k_norm_weight=None, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+        T, nseq = query.shape[0], past.shape[0]
+        if out is None:
+            out = torch.empty(T, self.num_heads * self.v_head_size, dtype=self.dtype,
+                              device=query.device)
+        B.pa_separate_write(self.params, key, value, cos_cache, sin_cache, k_norm_weight,
+                            slot_mapping, cumseq, past, key_cache, value_cache, self.err_flags,
+                            stream)
+        if num_decode_seqs > 0:
+            B.pa_separate_decode(self.params_after_write, query, key_cache, value_cache,
+                                 cos_cache, sin_cache, q_norm_weight, head_sink, cumseq, past,
+                                 block_table, out, 0, num_decode_seqs, self.workspace,
+                                 self.err_flags, stream)
+        if num_decode_seqs < nseq:
+            p = self.params_after_write if num_decode_seqs == 0 else self.params
+            B.pa_separate_prefill(p, query, key_cache, value_cache, cos_cache, sin_cache,
+                                  q_norm_weight, head_sink, cumseq, past, block_table, out,
+                                  num_decode_seqs, nseq, self.workspace, self.err_flags, stream)
+        return out
+
+    def error_flags(self) -> int:
+        return int(self.err_flags.item())

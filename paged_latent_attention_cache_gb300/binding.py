@@ -46,7 +46,9 @@ PA_FLAG_OWN_SLOTS = 0x4
 
 EXPORTED = ("pa_latent_validate", "pa_latent_write", "pa_latent_decode", "pa_latent_prefill",
             "pa_latent_decode_noalloc", "pa_latent_workspace_size", "pa_latent_kernel_family",
-            "pa_latent_status_string", "pa_latent_last_error")
+            "pa_latent_status_string", "pa_latent_last_error", "pa_separate_validate",
+            "pa_separate_write", "pa_separate_decode", "pa_separate_prefill",
+            "pa_separate_workspace_size")
 
 
 class PaError(RuntimeError):
@@ -77,6 +79,28 @@ class pa_latent_params(ctypes.Structure):
     ]
 
 
+class pa_separate_params(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int32),
+        ("num_heads", ctypes.c_int32),
+        ("kv_num_heads", ctypes.c_int32),
+        ("head_size", ctypes.c_int32),
+        ("v_head_size", ctypes.c_int32),
+        ("rotary_offset", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32),
+        ("rotary_interleaved", ctypes.c_int32),
+        ("cos_rows", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int32),
+        ("max_blocks_per_seq", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+        ("local_window_size", ctypes.c_int32),
+        ("rms_eps", ctypes.c_float),
+        ("flags", ctypes.c_int32),
+    ]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run "
@@ -104,6 +128,18 @@ def _load() -> ctypes.CDLL:
     lib.pa_latent_status_string.restype = ctypes.c_char_p
     lib.pa_latent_last_error.argtypes = []
     lib.pa_latent_last_error.restype = ctypes.c_char_p
+    S = ctypes.POINTER(pa_separate_params)
+    lib.pa_separate_validate.argtypes = [S]
+    lib.pa_separate_validate.restype = ctypes.c_int
+    lib.pa_separate_write.argtypes = [S, vp, vp, i64, vp, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp]
+    lib.pa_separate_write.restype = ctypes.c_int
+    sread = [S, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, sz, vp, vp, vp]
+    lib.pa_separate_decode.argtypes = sread
+    lib.pa_separate_decode.restype = ctypes.c_int
+    lib.pa_separate_prefill.argtypes = sread
+    lib.pa_separate_prefill.restype = ctypes.c_int
+    lib.pa_separate_workspace_size.argtypes = [S, i32, i64]
+    lib.pa_separate_workspace_size.restype = sz
     return lib
 
 
@@ -223,6 +259,64 @@ def alloc_workspace(p: pa_latent_params, num_seqs: int, num_tokens: int,
     if n == 0:
         return None
     return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def make_separate_params(*, dtype, num_heads, kv_num_heads, head_size, v_head_size=0,
+                         rotary_offset=0, rotary_dim=0, rotary_interleaved=0, cos_rows=1,
+                         block_size, num_blocks, max_blocks_per_seq, scale=0.0, softcap=0.0,
+                         local_window_size=-1, rms_eps=1e-6, flags=0) -> pa_separate_params:
+    if isinstance(dtype, torch.dtype):
+        dtype = {torch.float16: PA_DTYPE_F16, torch.bfloat16: PA_DTYPE_BF16}.get(dtype, -1)
+    return pa_separate_params(int(dtype), int(num_heads), int(kv_num_heads), int(head_size),
+                              int(v_head_size), int(rotary_offset), int(rotary_dim),
+                              int(rotary_interleaved), int(cos_rows), int(block_size),
+                              int(num_blocks), int(max_blocks_per_seq), float(scale),
+                              float(softcap), int(local_window_size), float(rms_eps), int(flags))
+
+
+def pa_separate_validate(p: pa_separate_params) -> int:
+    return int(lib.pa_separate_validate(ctypes.byref(p)))
+
+
+def pa_separate_workspace_size(p: pa_separate_params, num_seqs: int, num_tokens: int) -> int:
+    return int(lib.pa_separate_workspace_size(ctypes.byref(p), int(num_seqs), int(num_tokens)))
+
+
+def pa_separate_write(p, key, value, cos_cache, sin_cache, k_norm_weight, slot_mapping, cumseq,
+                      past, key_cache, value_cache, err_flags=None, stream=None):
+    _check(lib.pa_separate_write(
+        ctypes.byref(p), _ptr(key), _ptr(value), int(key.shape[0]), _ptr(cos_cache),
+        _ptr(sin_cache), _ptr(k_norm_weight), _ptr(slot_mapping), _ptr(cumseq), _ptr(past),
+        int(past.shape[0]), _ptr(key_cache), _ptr(value_cache), _ptr(err_flags),
+        _stream(stream)))
+
+
+def _sread(fn, p, query, key_cache, value_cache, cos_cache, sin_cache, q_norm_weight, head_sink,
+           cumseq, past, block_table, out, seq_begin, seq_end, workspace, err_flags, stream):
+    B = past.shape[0]
+    se = B if seq_end is None else seq_end
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(fn(ctypes.byref(p), _ptr(query), int(query.shape[0]), _ptr(key_cache),
+              _ptr(value_cache), _ptr(cos_cache), _ptr(sin_cache), _ptr(q_norm_weight),
+              _ptr(head_sink), _ptr(cumseq), _ptr(past), _ptr(block_table), int(B),
+              int(seq_begin), int(se), _ptr(workspace), ctypes.c_size_t(ws_bytes), _ptr(out),
+              _ptr(err_flags), _stream(stream)))
+
+
+def pa_separate_decode(p, query, key_cache, value_cache, cos_cache, sin_cache, q_norm_weight,
+                       head_sink, cumseq, past, block_table, out, seq_begin=0, seq_end=None,
+                       workspace=None, err_flags=None, stream=None):
+    _sread(lib.pa_separate_decode, p, query, key_cache, value_cache, cos_cache, sin_cache,
+           q_norm_weight, head_sink, cumseq, past, block_table, out, seq_begin, seq_end,
+           workspace, err_flags, stream)
+
+
+def pa_separate_prefill(p, query, key_cache, value_cache, cos_cache, sin_cache, q_norm_weight,
+                        head_sink, cumseq, past, block_table, out, seq_begin=0, seq_end=None,
+                        workspace=None, err_flags=None, stream=None):
+    _sread(lib.pa_separate_prefill, p, query, key_cache, value_cache, cos_cache, sin_cache,
+           q_norm_weight, head_sink, cumseq, past, block_table, out, seq_begin, seq_end,
+           workspace, err_flags, stream)
 
 
 def default_scale(head_size: int) -> float:

@@ -132,6 +132,8 @@ pa_status resolve(const pa_latent_params* p, Geometry* g) {
   g->window = p->local_window_size < 0 ? -1 : p->local_window_size;
   g->fp8 = fp8 ? 1 : 0;
   g->k_scale = fp8 ? p->k_scale : 1.f;
+  g->kvh = 1;
+  g->rms_eps = 0.f;
   g->flags = p->flags;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
@@ -201,9 +203,10 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
   if (workspace && !aligned(workspace, 256))
     return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
 
-  ReadArgs a{query,   num_tokens,  key_cache, cos_cache, sin_cache, cumseq,
-             past,    block_table, num_seqs,  seq_begin, seq_end,   workspace,
-             workspace_bytes, out, err_flags, reinterpret_cast<cudaStream_t>(stream)};
+  ReadArgs a{query,    num_tokens, key_cache,   nullptr,  nullptr,   nullptr,
+             cos_cache, sin_cache, cumseq,      past,     block_table, num_seqs,
+             seq_begin, seq_end,   workspace,   workspace_bytes, out, err_flags,
+             reinterpret_cast<cudaStream_t>(stream)};
   const bool tc = use_tc(g, ph);
   if (g.fp8 && !tc)
     return fail(PA_ERR_NOT_IMPLEMENTED,
@@ -218,6 +221,96 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
 }
 
 }  // namespace
+
+// SEPARATE layout: the LATENT checks that apply (dtype, block size, rotary,
+// window, softcap, flags) plus kv_num_heads dividing num_heads and the
+// RMSNorm epsilon; scale 0 selects 1/sqrt(head_size).
+pa_status resolve_separate(const pa_separate_params* p, Geometry* g) {
+  if (!p) return fail(PA_ERR_INVALID_ARGUMENT, "params is NULL");
+  if (p->kv_num_heads < 1 || p->num_heads < 1 || p->num_heads % p->kv_num_heads != 0)
+    return fail(PA_ERR_INVALID_ARGUMENT,
+                "num_heads %d must be a positive multiple of kv_num_heads %d", p->num_heads,
+                p->kv_num_heads);
+  if (!(isfinite(p->rms_eps) && p->rms_eps >= 0.f))
+    return fail(PA_ERR_INVALID_ARGUMENT, "rms_eps must be finite and >= 0");
+  pa_latent_params q = {};
+  q.dtype = p->dtype;
+  q.num_heads = p->num_heads;
+  q.head_size = p->head_size;
+  q.v_head_size = p->v_head_size;
+  q.rotary_offset = p->rotary_offset;
+  q.rotary_dim = p->rotary_dim;
+  q.rotary_interleaved = p->rotary_interleaved;
+  q.cos_rows = p->cos_rows;
+  q.block_size = p->block_size;
+  q.num_blocks = p->num_blocks;
+  q.max_blocks_per_seq = p->max_blocks_per_seq;
+  q.softcap = p->softcap;
+  q.local_window_size = p->local_window_size;
+  q.flags = p->flags;
+  // the default scale is allowed for any value width here
+  q.scale = p->scale;
+  const int hs = p->head_size;
+  if (p->scale == 0.f && hs >= 16 && hs % 16 == 0) q.scale = 1.0f / sqrtf((float)hs);
+  if (q.v_head_size > hs && hs > 0)
+    return fail(PA_ERR_INVALID_ARGUMENT, "v_head_size %d must be in 1..=head_size %d",
+                q.v_head_size, hs);
+  const pa_status s = resolve(&q, g);
+  if (s != PA_OK) return s;
+  if (p->flags & PA_FLAG_PORTABLE)
+    return fail(PA_ERR_NOT_IMPLEMENTED, "the SEPARATE layout runs on the tensor-core kernels only");
+  g->kvh = p->kv_num_heads;
+  g->rms_eps = p->rms_eps;
+  return PA_OK;
+}
+
+pa_status separate_read(Phase ph, const pa_separate_params* p, const void* query,
+                        int64_t num_tokens, const void* key_cache, const void* value_cache,
+                        const void* cos_cache, const void* sin_cache, const void* q_norm,
+                        const void* head_sink, const int32_t* cumseq, const int32_t* past,
+                        const int32_t* block_table, int32_t num_seqs, int32_t seq_begin,
+                        int32_t seq_end, void* workspace, size_t workspace_bytes, void* out,
+                        int32_t* err_flags, void* stream) {
+  Geometry g;
+  pa_status s = resolve_separate(p, &g);
+  if (s != PA_OK) return s;
+  if ((s = check_tokens(num_tokens, num_seqs, g)) != PA_OK) return s;
+  if (seq_begin < 0 || seq_end < seq_begin || seq_end > num_seqs)
+    return fail(PA_ERR_INVALID_ARGUMENT, "sequence range [%d, %d) outside [0, %d)", seq_begin,
+                seq_end, num_seqs);
+  if (num_tokens == 0 || seq_end == seq_begin) return PA_OK;
+  if (ph == Phase::kDecode && (int64_t)(seq_end - seq_begin) > num_tokens)
+    return fail(PA_ERR_INVALID_ARGUMENT,
+                "decode over %d sequences needs at least that many tokens (have %lld)",
+                seq_end - seq_begin, (long long)num_tokens);
+  if (!query || !key_cache || !value_cache || !cumseq || !past || !block_table || !out)
+    return fail(PA_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
+  if (g.rd > 0 && (!cos_cache || !sin_cache))
+    return fail(PA_ERR_INVALID_ARGUMENT, "cos_cache/sin_cache are required when rotary_dim > 0");
+  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(out, 16) || (g.rd > 0 && (!aligned(cos_cache, 16) || !aligned(sin_cache, 16))) ||
+      (q_norm && !aligned(q_norm, 16)) || (head_sink && !aligned(head_sink, 2)))
+    return fail(PA_ERR_INVALID_ARGUMENT,
+                "half-precision tensors must be 16-byte aligned (head_sink 2-byte)");
+  if (!aligned(cumseq, 4) || !aligned(past, 4) || !aligned(block_table, 4) ||
+      !aligned(err_flags, 4))
+    return fail(PA_ERR_INVALID_ARGUMENT, "int32 tensors must be 4-byte aligned");
+  if (workspace && !aligned(workspace, 256))
+    return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if (!separate_supported(g, ph))
+    return fail(PA_ERR_NOT_IMPLEMENTED,
+                "SEPARATE layout: head_size and v_head_size in 64..256 and at most 128 query "
+                "heads per kv head run on the tensor-core kernels; this geometry does not");
+  const size_t need = separate_call_workspace(g, ph, seq_begin, seq_end);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace ? workspace_bytes : (size_t)0, need);
+  ReadArgs a{query,     num_tokens, key_cache,   value_cache, head_sink, q_norm,
+             cos_cache, sin_cache,  cumseq,      past,        block_table, num_seqs,
+             seq_begin, seq_end,    workspace,   workspace_bytes, out, err_flags,
+             reinterpret_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_separate_read(g, ph, a), "SEPARATE attention launch");
+}
 
 pa_status record_error(pa_status s, const char* msg) { return fail(s, "%s", msg); }
 
@@ -328,5 +421,75 @@ const char* pa_latent_status_string(pa_status s) {
 }
 
 const char* pa_latent_last_error(void) { return g_last_error.c_str(); }
+
+pa_status pa_separate_validate(const pa_separate_params* p) {
+  Geometry g;
+  return resolve_separate(p, &g);
+}
+
+pa_status pa_separate_write(const pa_separate_params* p, const void* key, const void* value,
+                            int64_t num_tokens, const void* cos_cache, const void* sin_cache,
+                            const void* k_norm_weight, const int32_t* slot_mapping,
+                            const int32_t* cumseq, const int32_t* past, int32_t num_seqs,
+                            void* key_cache, void* value_cache, int32_t* err_flags,
+                            void* stream) {
+  Geometry g;
+  pa_status s = resolve_separate(p, &g);
+  if (s != PA_OK) return s;
+  if ((s = check_tokens(num_tokens, num_seqs, g)) != PA_OK) return s;
+  if (num_tokens == 0) return PA_OK;
+  if (num_seqs < 1) return fail(PA_ERR_INVALID_ARGUMENT, "tokens given but num_seqs is 0");
+  if (g.hs > 256 || g.vhs % 8 != 0 || g.vhs > 256)
+    return fail(PA_ERR_NOT_IMPLEMENTED,
+                "SEPARATE write: head_size <= 256 and v_head_size a multiple of 8 <= 256");
+  if (!key || !value || !slot_mapping || !cumseq || !past || !key_cache || !value_cache)
+    return fail(PA_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
+  if (g.rd > 0 && (!cos_cache || !sin_cache))
+    return fail(PA_ERR_INVALID_ARGUMENT, "cos_cache/sin_cache are required when rotary_dim > 0");
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || (k_norm_weight && !aligned(k_norm_weight, 16)) ||
+      (g.rd > 0 && (!aligned(cos_cache, 16) || !aligned(sin_cache, 16))))
+    return fail(PA_ERR_INVALID_ARGUMENT, "half-precision tensors must be 16-byte aligned");
+  if (!aligned(slot_mapping, 4) || !aligned(cumseq, 4) || !aligned(past, 4) ||
+      !aligned(err_flags, 4))
+    return fail(PA_ERR_INVALID_ARGUMENT, "int32 tensors must be 4-byte aligned");
+  SeparateWriteArgs a{key,    value,       num_tokens, cos_cache, sin_cache, k_norm_weight,
+                      slot_mapping, cumseq, past, num_seqs, key_cache, value_cache, err_flags,
+                      reinterpret_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_separate_write(g, a), "SEPARATE write launch");
+}
+
+pa_status pa_separate_decode(const pa_separate_params* p, const void* query, int64_t num_tokens,
+                             const void* key_cache, const void* value_cache,
+                             const void* cos_cache, const void* sin_cache,
+                             const void* q_norm_weight, const void* head_sink,
+                             const int32_t* cumseq, const int32_t* past,
+                             const int32_t* block_table, int32_t num_seqs, int32_t seq_begin,
+                             int32_t seq_end, void* workspace, size_t workspace_bytes, void* out,
+                             int32_t* err_flags, void* stream) {
+  return separate_read(Phase::kDecode, p, query, num_tokens, key_cache, value_cache, cos_cache,
+                       sin_cache, q_norm_weight, head_sink, cumseq, past, block_table, num_seqs,
+                       seq_begin, seq_end, workspace, workspace_bytes, out, err_flags, stream);
+}
+
+pa_status pa_separate_prefill(const pa_separate_params* p, const void* query,
+                              int64_t num_tokens, const void* key_cache, const void* value_cache,
+                              const void* cos_cache, const void* sin_cache,
+                              const void* q_norm_weight, const void* head_sink,
+                              const int32_t* cumseq, const int32_t* past,
+                              const int32_t* block_table, int32_t num_seqs, int32_t seq_begin,
+                              int32_t seq_end, void* workspace, size_t workspace_bytes,
+                              void* out, int32_t* err_flags, void* stream) {
+  return separate_read(Phase::kPrefill, p, query, num_tokens, key_cache, value_cache, cos_cache,
+                       sin_cache, q_norm_weight, head_sink, cumseq, past, block_table, num_seqs,
+                       seq_begin, seq_end, workspace, workspace_bytes, out, err_flags, stream);
+}
+
+size_t pa_separate_workspace_size(const pa_separate_params* p, int32_t num_seqs,
+                                  int64_t num_tokens) {
+  Geometry g;
+  if (resolve_separate(p, &g) != PA_OK || num_seqs <= 0 || num_tokens <= 0) return 0;
+  return separate_call_workspace(g, Phase::kDecode, 0, num_seqs);
+}
 
 }  // extern "C"

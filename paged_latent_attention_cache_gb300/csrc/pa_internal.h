@@ -29,6 +29,8 @@ struct Geometry {
   int window;       // < 0: off
   int fp8;          // key_cache holds E4M3 codes (PA_CACHE_FP8_E4M3)
   float k_scale;    // FP8 cache: value = code * k_scale (1 otherwise)
+  int kvh;          // kv heads (1 in the LATENT layout)
+  float rms_eps;    // SEPARATE layout: RMSNorm epsilon
   int flags;
   int num_sms;      // SM count of the current device
   int device;       // current device ordinal
@@ -69,6 +71,9 @@ struct ReadArgs {
   const void* query;
   int64_t num_tokens;
   const void* key_cache;
+  const void* value_cache;  // SEPARATE layout only (null otherwise)
+  const void* head_sink;    // SEPARATE layout, optional
+  const void* q_norm;       // SEPARATE layout, optional
   const void* cos_cache;
   const void* sin_cache;
   const int32_t* cumseq;
@@ -95,6 +100,28 @@ size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t
 // Workspace one read call over sequences [seq_begin, seq_end) needs.
 size_t tc_call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end);
 cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a);
+
+// ---- SEPARATE layout (pa_gqa.cu)
+struct SeparateWriteArgs {
+  const void* key;
+  const void* value;
+  int64_t num_tokens;
+  const void* cos_cache;
+  const void* sin_cache;
+  const void* k_norm;  // optional
+  const int32_t* slot_mapping;
+  const int32_t* cumseq;
+  const int32_t* past;
+  int32_t num_seqs;
+  void* key_cache;
+  void* value_cache;
+  int32_t* err_flags;
+  cudaStream_t stream;
+};
+cudaError_t launch_separate_write(const Geometry& g, const SeparateWriteArgs& a);
+bool separate_supported(const Geometry& g, Phase ph);
+size_t separate_call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end);
+cudaError_t launch_separate_read(const Geometry& g, Phase ph, const ReadArgs& a);
 
 // ---- shared by the entry points (pa_api.cu)
 // Workspace bytes a decode call over sequences [seq_begin, seq_end) of these

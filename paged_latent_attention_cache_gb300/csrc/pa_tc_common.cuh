@@ -55,6 +55,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -249,6 +257,15 @@ struct Params {
   // factors and into out_scale, which multiplies the output (1 otherwise).
   int stages8, stage8_bytes;
   float out_scale;
+  // SEPARATE layout (grouped-query attention, pa_gqa.cu): a work unit holds
+  // tpc tokens x grp query heads of one kv head; keys and values come from
+  // their own caches into the two parts of a stage.
+  int kvh, grp;            // kv heads; query heads per kv head
+  const void* head_sink;   // [H] sink logits (query dtype), or null
+  const void* q_norm;      // [hs] RMSNorm weight of the query (query dtype), or null
+  float rms_eps;
+  int vslabs;              // 64-channel value slabs of a stage
+  int k_bytes;             // bytes of a stage's key part (the value part follows)
 };
 
 // Compile-time part of a single-CTA kernel configuration: N keys per tile,

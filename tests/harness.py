@@ -162,3 +162,58 @@ def sample_tokens(w: W.Workload, per_seq: int = 24, seed: int = 0):
                 out.add(t)
         out.update(int(x) for x in rng.integers(lo, hi, size=min(per_seq, hi - lo)))
     return sorted(out)
+
+
+# ---------------------------------------------------------------------------
+# SEPARATE layout
+# ---------------------------------------------------------------------------
+
+def run_gpu_separate(w, device="cuda"):
+    from paged_latent_attention_cache_gb300.api import SeparateAttention
+    d = w.to(device)
+    op = SeparateAttention.from_workload(w, device=device)
+    kc, vc = d.key_cache.clone(), d.value_cache.clone()
+    out = torch.full((w.num_tokens, w.num_heads * w.v_head_size), float("nan"), dtype=w.dtype,
+                     device=device)
+    op.forward(d.query, d.key, d.value, kc, vc, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+               d.block_table, d.slot_mapping, w.num_decode_seqs, head_sink=d.head_sink,
+               q_norm_weight=d.q_norm_weight, k_norm_weight=d.k_norm_weight, out=out)
+    torch.cuda.synchronize()
+    return dict(kcache=W.to_bits(kc), vcache=W.to_bits(vc), out=W.to_bits(out),
+                flags=op.error_flags(), op=op)
+
+
+def run_oracle_separate(w, tokens=None):
+    tb = W.to_bits
+    opt = lambda t: None if t is None else tb(t)
+    kb, vb, ob, out, sc = O.run_separate_bits(
+        tb(w.query), tb(w.key), tb(w.value), tb(w.key_cache), tb(w.value_cache),
+        tb(w.cos_cache), tb(w.sin_cache), w.cumseq.numpy(), w.past.numpy(),
+        w.block_table.numpy(), w.slot_mapping.numpy(), W.separate_oracle_params(w),
+        opt(w.head_sink), opt(w.q_norm_weight), opt(w.k_norm_weight), tokens, stats=True)
+    return dict(kcache=kb, vcache=vb, out_bits=ob, out=out, scales=sc)
+
+
+def check_separate_caches(w, got, ref):
+    """Value rows are copies: bit-exact. Key rows: unwritten rows bit-exact;
+    written rows bit-exact where neither RMSNorm nor RoPE touches a channel,
+    within 1 ulp elsewhere (f32 against the oracle's float64)."""
+    vg, vr = got["vcache"], ref["vcache"]
+    assert np.array_equal(vg, vr), f"{(vg != vr).sum()} value-cache values differ"
+    hs = w.head_size
+    g = got["kcache"].reshape(-1, hs)
+    r = ref["kcache"].reshape(-1, hs)
+    kvh = w.kv_num_heads
+    written = np.zeros(g.shape[0] // kvh, dtype=bool)
+    sl = w.slot_mapping.numpy()
+    written[sl[sl >= 0]] = True
+    written = np.repeat(written, kvh)
+    assert (g[~written] == r[~written]).all(), "unwritten key-cache rows changed"
+    touched = np.zeros(hs, dtype=bool)
+    if w.k_norm_weight is not None:
+        touched[:] = True
+    touched[w.rotary_offset:w.rotary_offset + w.rotary_dim] = True
+    gw, rw = g[written], r[written]
+    assert (gw[:, ~touched] == rw[:, ~touched]).all(), "untouched key channels differ"
+    d = np.abs(_ordered(gw[:, touched]) - _ordered(rw[:, touched]))
+    assert d.max(initial=0) <= 1, f"key channels differ by {d.max()} ulp"

@@ -22,7 +22,7 @@ def B():
 
 def _declared():
     src = open(os.path.join(ROOT, "include", "pa_latent.h")).read()
-    return sorted(set(re.findall(r"\b(pa_latent_\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(pa_(?:latent|separate)_\w+)\s*\(", src)))
 
 
 def test_header_declares_the_three_calls():
@@ -36,6 +36,40 @@ def test_library_exports_every_declared_symbol(B):
     for name in _declared():
         assert hasattr(lib, name), name
     assert sorted(B.EXPORTED) == _declared()
+
+
+def _sep(B, **kw):
+    base = dict(dtype=B.PA_DTYPE_BF16, num_heads=8, kv_num_heads=2, head_size=128,
+                rotary_dim=128, cos_rows=256, block_size=16, num_blocks=8, max_blocks_per_seq=4)
+    base.update(kw)
+    return B.make_separate_params(**base)
+
+
+def test_separate_params_checked(B):
+    """SEPARATE layout: kv_num_heads must divide num_heads; the default scale
+    is allowed for any value width; rms_eps must be finite and >= 0; the
+    portable flag is not a path this layout has."""
+    assert B.pa_separate_validate(_sep(B)) == B.PA_OK
+    assert B.pa_separate_validate(_sep(B, v_head_size=64)) == B.PA_OK
+    assert B.pa_separate_validate(_sep(B, kv_num_heads=3)) == B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_separate_validate(_sep(B, kv_num_heads=0)) == B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_separate_validate(_sep(B, rms_eps=-1.0)) == B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_separate_validate(_sep(B, rms_eps=float("nan"))) == B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_separate_validate(_sep(B, block_size=24)) == B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_separate_validate(_sep(B, flags=B.PA_FLAG_PORTABLE)) == B.PA_ERR_NOT_IMPLEMENTED
+    assert B.pa_separate_workspace_size(_sep(B), 32, 32) > 0
+    assert B.pa_separate_workspace_size(_sep(B, kv_num_heads=3), 32, 32) == 0
+
+
+def test_fp8_params_checked(B):
+    """An FP8 cache needs a finite k_scale > 0; unknown cache formats are
+    rejected."""
+    assert B.pa_latent_validate(_good(B, cache_dtype="e4m3", k_scale=0.02)) == B.PA_OK
+    assert B.pa_latent_validate(_good(B, cache_dtype="e4m3", k_scale=0.0)) == \
+        B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_latent_validate(_good(B, cache_dtype="e4m3", k_scale=float("inf"))) == \
+        B.PA_ERR_INVALID_ARGUMENT
+    assert B.pa_latent_validate(_good(B, cache_dtype=7)) == B.PA_ERR_INVALID_ARGUMENT
 
 
 def _good(B, **kw):
