@@ -101,6 +101,9 @@ def algorithmic_work(w, seqs=None, tokens=None, include_write=True):
     el = 2
     el_c = 1 if getattr(w, "cache_dtype", None) == "e4m3" else 2
     H, hs, vhs, bs = w.num_heads, w.head_size, w.v_head_size, w.block_size
+    # SEPARATE layout: a visible position is kvH key rows and kvH value rows
+    kvh = getattr(w, "kv_num_heads", None)
+    row_bytes = kvh * (hs + vhs) * el if kvh else hs * el_c
     win = w.local_window_size
     cs = w.cumseq.tolist()
     seqs = range(w.num_seqs) if seqs is None else seqs
@@ -124,12 +127,13 @@ def algorithmic_work(w, seqs=None, tokens=None, include_write=True):
         cache_rows += span
         bt_entries += last_pos // bs - first_lo // bs + 1
         q_rows += len(toks)
-    read_bytes = (cache_rows * hs * el_c + q_rows * H * hs * el + q_rows * H * vhs * el +
+    read_bytes = (cache_rows * row_bytes + q_rows * H * hs * el + q_rows * H * vhs * el +
                   q_rows * w.rotary_dim * el + bt_entries * 4)
     write_bytes = 0
     if include_write:
         n_written = int((w.slot_mapping >= 0).sum())
-        write_bytes = (w.num_tokens * hs * el + n_written * hs * el_c +
+        new_row = kvh * (hs + vhs) * el if kvh else hs * el
+        write_bytes = (w.num_tokens * new_row + n_written * row_bytes +
                        w.num_tokens * (w.rotary_dim * el + 4))
     return dict(bytes=read_bytes + write_bytes, read_bytes=read_bytes, flops=flops,
                 cache_rows=cache_rows, tokens=q_rows)
@@ -321,22 +325,45 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
 
     w = build_workload(name, rank_seed(0, rank) if world > 1 else 0)
     d = w.to(device)
-    op = PagedLatentAttention.from_workload(w, device=device, portable=args.portable)
     out = torch.empty(w.num_tokens, w.num_heads * w.v_head_size, dtype=w.dtype, device=device)
     cache = d.key_cache
     nd = w.num_decode_seqs
     stream = torch.cuda.current_stream(device)
+    separate = hasattr(w, "kv_num_heads")
+    if separate:
+        from paged_latent_attention_cache_gb300 import binding as B
+        from paged_latent_attention_cache_gb300.api import SeparateAttention
+        op = SeparateAttention.from_workload(w, device=device)
+        vcache = d.value_cache
 
-    def write():
-        op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
+        def write():
+            B.pa_separate_write(op.params, d.key, d.value, d.cos_cache, d.sin_cache,
+                                d.k_norm_weight, d.slot_mapping, d.cumseq, d.past, cache, vcache,
+                                op.err_flags)
 
-    def decode():
-        op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                  d.block_table, out, 0, nd, after_write=True)
+        def decode():
+            B.pa_separate_decode(op.params_after_write, d.query, cache, vcache, d.cos_cache,
+                                 d.sin_cache, d.q_norm_weight, d.head_sink, d.cumseq, d.past,
+                                 d.block_table, out, 0, nd, op.workspace, op.err_flags)
 
-    def prefill():
-        op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
-                   d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
+        def prefill():
+            B.pa_separate_prefill(op.params_after_write if nd == 0 else op.params, d.query,
+                                  cache, vcache, d.cos_cache, d.sin_cache, d.q_norm_weight,
+                                  d.head_sink, d.cumseq, d.past, d.block_table, out, nd,
+                                  w.num_seqs, op.workspace, op.err_flags)
+    else:
+        op = PagedLatentAttention.from_workload(w, device=device, portable=args.portable)
+
+        def write():
+            op.write(d.key, d.cos_cache, d.sin_cache, d.slot_mapping, d.cumseq, d.past, cache)
+
+        def decode():
+            op.decode(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                      d.block_table, out, 0, nd, after_write=True)
+
+        def prefill():
+            op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
+                       d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
 
     phases = [("write", write), ("decode", decode if nd > 0 else None),
               ("prefill", prefill if nd < w.num_seqs else None)]
@@ -411,7 +438,7 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
             "p90": round(q[-1], 5)}
 
     e2e_ms = h2d = d2h = None
-    if e2e:
+    if e2e and not separate:
         # End to end through the operator object: H2D of the step's inputs
         # from pinned memory, the three phases, D2H of the output.
         host = {k: getattr(w, k).pin_memory() for k in
@@ -453,7 +480,8 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
                tflops=work["flops"] * world / (ms_per_step * 1e-3) / 1e12,
                ms_per_step=ms_per_step, dist=dist, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h,
                clocks=clocks, wall=wall, launches=launches_per_step, phase_ms=phase_ms,
-               family=(op.kernel_family(0), op.kernel_family(1)), steps=K)
+               family=(1, 1) if separate else (op.kernel_family(0), op.kernel_family(1)),
+               steps=K)
     return res
 
 
@@ -507,8 +535,14 @@ def roofline(res, peaks):
 
 def config_of(w, world):
     """The workload description both arms print."""
+    extra = {}
+    if hasattr(w, "kv_num_heads"):
+        extra = {"layout": "SEPARATE", "kv_num_heads": w.kv_num_heads,
+                 "head_sink": w.head_sink is not None, "qk_norm": w.q_norm_weight is not None}
+    elif getattr(w, "cache_dtype", None):
+        extra = {"cache_dtype": w.cache_dtype, "k_scale": w.k_scale}
     return {"workload": w.name, "dtype": {"torch.bfloat16": "bf16",
-                                           "torch.float16": "f16"}[str(w.dtype)],
+                                           "torch.float16": "f16"}[str(w.dtype)], **extra,
             "num_heads": w.num_heads, "head_size": w.head_size, "v_head_size": w.v_head_size,
             "rotary": [w.rotary_offset, w.rotary_dim], "block_size": w.block_size,
             "num_seqs": w.num_seqs, "num_decode_seqs": w.num_decode_seqs,
@@ -545,7 +579,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dsv3_decode")
-    ap.add_argument("--extras", default="dsv3_prefill,glm_decode,mixed_serving",
+    ap.add_argument("--extras",
+                    default="dsv3_prefill,glm_decode,mixed_serving,glm_decode_fp8,gqa_decode",
                     help="comma-separated workloads timed after the headline one "
                          "('none' to skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -544,3 +544,6 @@ def separate_oracle_params(w: SeparateWorkload) -> Dict[str, object]:
     p = w.params()
     p["dtype"] = dtype_tag(w.dtype)
     return p
+
+
+WORKLOADS["gqa_decode"] = gqa_decode

@@ -62,3 +62,17 @@ def test_accounting_write_bytes():
     assert a["bytes"] - r["bytes"] == (w.num_tokens * w.head_size * el +
                                        written * w.head_size * el +
                                        w.num_tokens * (w.rotary_dim * el + 4))
+
+
+def test_accounting_separate_layout():
+    """SEPARATE layout: a visible position is kv_num_heads key rows and
+    kv_num_heads value rows."""
+    w = W.make_separate_workload("accs", q_lens=[1, 5, 0, 17], past_lens=[40, 0, 3, 9],
+                                 num_heads=8, kv_num_heads=2, head_size=64, block_size=16,
+                                 seed=7)
+    got = bench.algorithmic_work(w, include_write=False)
+    rows, flops, q_rows, bt = _brute(w)
+    assert got["cache_rows"] == rows and got["flops"] == flops
+    want = (rows * 2 * (64 + 64) * 2 + q_rows * 8 * (64 + 64) * 2 + q_rows * w.rotary_dim * 2 +
+            bt * 4)
+    assert got["read_bytes"] == want
