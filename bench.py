@@ -365,8 +365,16 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
             op.prefill(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past,
                        d.block_table, out, nd, w.num_seqs, after_write=nd == 0)
 
-    phases = [("write", write), ("decode", decode if nd > 0 else None),
-              ("prefill", prefill if nd < w.num_seqs else None)]
+        def mixed():
+            op.mixed(d.query, cache, d.cos_cache, d.sin_cache, d.cumseq, d.past, d.block_table,
+                     out, nd, after_write=True)
+
+    if not separate and 0 < nd < w.num_seqs:
+        # a mixed batch: one read call (one grid for decode and prefill work)
+        phases = [("write", write), ("read", mixed)]
+    else:
+        phases = [("write", write), ("decode", decode if nd > 0 else None),
+                  ("prefill", prefill if nd < w.num_seqs else None)]
 
     def step():
         for _, f in phases:
@@ -504,7 +512,12 @@ def roofline(res, peaks):
     over the call's mean duration, timed live with CUDA events."""
     w = res["w"]
     hbm, bf16, bf16_sus, peak_src = peaks
-    if w.num_decode_seqs:
+    if "read" in res["phase_ms"]:
+        dw, pw = res["dec_work"], res["pre_work"]
+        dom = {"bytes": dw["bytes"] + pw["bytes"], "flops": dw["flops"] + pw["flops"]}
+        dom_ms = res["phase_ms"]["read"]
+        dom_name = "mixed read call (decode splits + prefill units in one grid, + combine)"
+    elif w.num_decode_seqs:
         dom, dom_ms = res["dec_work"], res["phase_ms"]["decode"]
         dom_name = "decode call (split-KV attention + combine)"
     else:

@@ -216,6 +216,25 @@ pa_status pa_latent_prefill(const pa_latent_params* p, const void* query, int64_
                             int32_t* err_flags, void* stream);
 
 /*
+ * Read phase for a whole mixed batch in one call: sequences [0,
+ * num_decode_seqs) are decodes (one new token each, as pa_latent_decode)
+ * and [num_decode_seqs, num_seqs) prefills (as pa_latent_prefill), the
+ * serving batch the op receives. Where the single-CTA tensor-core kernel
+ * runs (latent widths 64..256), both kinds of work are one grid: the decode
+ * splits first, the prefill units after them on the SMs the decode tail
+ * frees, then the split combine. Otherwise (576/512, PA_FLAG_PORTABLE) the
+ * call is a pa_latent_decode followed by a pa_latent_prefill. Workspace as
+ * pa_latent_decode (pa_latent_workspace_size for num_seqs sequences is
+ * enough). PA_FLAG_AFTER_WRITE / PA_FLAG_OWN_SLOTS apply to this one call.
+ */
+pa_status pa_latent_mixed(const pa_latent_params* p, const void* query, int64_t num_tokens,
+                          const void* key_cache, const void* cos_cache, const void* sin_cache,
+                          const int32_t* cumseq, const int32_t* past,
+                          const int32_t* block_table, int32_t num_seqs,
+                          int32_t num_decode_seqs, void* workspace, size_t workspace_bytes,
+                          void* out, int32_t* err_flags, void* stream);
+
+/*
  * Allocation-free decode. The operator definition has no counterpart for
  * this call; it exists for callers that cannot allocate device memory and so
  * cannot hand pa_latent_decode a workspace: an execution provider whose host

@@ -89,17 +89,31 @@ class PagedLatentAttention:
                             block_table, out, seq_begin, seq_end, self.workspace,
                             self.err_flags, stream)
 
+    def mixed(self, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+              num_decode_seqs: int, stream=None, after_write: bool = False):
+        """Read phase of the whole batch in one call: decode over
+        [0, num_decode_seqs), prefill over the rest (see pa_latent_mixed)."""
+        B.pa_latent_mixed(self._read_params(after_write), query, key_cache, cos_cache, sin_cache,
+                          cumseq, past, block_table, out, num_decode_seqs, self.workspace,
+                          self.err_flags, stream)
+
     def forward(self, query, key, key_cache, cos_cache, sin_cache, cumseq, past, block_table,
                 slot_mapping, num_decode_seqs: int, out: Optional[torch.Tensor] = None,
-                stream=None) -> torch.Tensor:
+                stream=None, one_call: bool = True) -> torch.Tensor:
         """Write phase over all tokens, then decode over sequences
-        [0, num_decode_seqs) and prefill over the rest; returns ``out``."""
+        [0, num_decode_seqs) and prefill over the rest; returns ``out``. A
+        batch with both kinds of sequences is read by one pa_latent_mixed
+        call (``one_call=False``: a decode call and a prefill call)."""
         T = query.shape[0]
         nseq = past.shape[0]
         if out is None:
             out = torch.empty(T, self.num_heads * self.v_head_size, dtype=self.dtype,
                               device=query.device)
         self.write(key, cos_cache, sin_cache, slot_mapping, cumseq, past, key_cache, stream)
+        if one_call and 0 < num_decode_seqs < nseq:
+            self.mixed(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+                       num_decode_seqs, stream, after_write=True)
+            return out
         if num_decode_seqs > 0:
             self.decode(query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
                         0, num_decode_seqs, stream, after_write=True)

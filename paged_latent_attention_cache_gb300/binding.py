@@ -45,6 +45,7 @@ PA_FLAG_AFTER_WRITE = 0x2
 PA_FLAG_OWN_SLOTS = 0x4
 
 EXPORTED = ("pa_latent_validate", "pa_latent_write", "pa_latent_decode", "pa_latent_prefill",
+            "pa_latent_mixed",
             "pa_latent_decode_noalloc", "pa_latent_workspace_size", "pa_latent_kernel_family",
             "pa_latent_status_string", "pa_latent_last_error", "pa_separate_validate",
             "pa_separate_write", "pa_separate_decode", "pa_separate_prefill",
@@ -117,6 +118,9 @@ def _load() -> ctypes.CDLL:
     lib.pa_latent_decode.restype = ctypes.c_int
     lib.pa_latent_prefill.argtypes = read
     lib.pa_latent_prefill.restype = ctypes.c_int
+    lib.pa_latent_mixed.argtypes = [P, vp, i64, vp, vp, vp, vp, vp, vp, i32, i32, vp, sz, vp, vp,
+                                    vp]
+    lib.pa_latent_mixed.restype = ctypes.c_int
     lib.pa_latent_decode_noalloc.argtypes = [P, vp, i64, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                              vp, vp, vp]
     lib.pa_latent_decode_noalloc.restype = ctypes.c_int
@@ -236,6 +240,18 @@ def pa_latent_prefill(p, query, key_cache, cos_cache, sin_cache, cumseq, past, b
                       num_tokens=None, num_seqs=None):
     _read(lib.pa_latent_prefill, p, query, key_cache, cos_cache, sin_cache, cumseq, past,
           block_table, out, seq_begin, seq_end, workspace, err_flags, stream, num_tokens, num_seqs)
+
+
+def pa_latent_mixed(p, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,
+                    num_decode_seqs, workspace=None, err_flags=None, stream=None):
+    """Decodes [0, num_decode_seqs) and prefills the rest of the batch in one
+    call (one grid where the single-CTA tensor-core kernel runs)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_latent_mixed(ctypes.byref(p), _ptr(query), int(query.shape[0]),
+                               _ptr(key_cache), _ptr(cos_cache), _ptr(sin_cache), _ptr(cumseq),
+                               _ptr(past), _ptr(block_table), int(past.shape[0]),
+                               int(num_decode_seqs), _ptr(workspace), ctypes.c_size_t(ws_bytes),
+                               _ptr(out), _ptr(err_flags), _stream(stream)))
 
 
 def pa_latent_decode_noalloc(p, query, key_cache, cos_cache, sin_cache, cumseq, past,

@@ -203,10 +203,10 @@ pa_status read_phase(Phase ph, const pa_latent_params* p, const void* query, int
   if (workspace && !aligned(workspace, 256))
     return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
 
-  ReadArgs a{query,    num_tokens, key_cache,   nullptr,  nullptr,   nullptr,
-             cos_cache, sin_cache, cumseq,      past,     block_table, num_seqs,
-             seq_begin, seq_end,   workspace,   workspace_bytes, out, err_flags,
-             reinterpret_cast<cudaStream_t>(stream)};
+  ReadArgs a{query,     num_tokens, key_cache,   nullptr,   nullptr,     nullptr,
+             cos_cache, sin_cache,  cumseq,      past,      block_table, num_seqs,
+             seq_begin, seq_end,    seq_begin,   seq_end,   workspace,   workspace_bytes,
+             out,       err_flags,  reinterpret_cast<cudaStream_t>(stream)};
   const bool tc = use_tc(g, ph);
   if (g.fp8 && !tc)
     return fail(PA_ERR_NOT_IMPLEMENTED,
@@ -305,11 +305,69 @@ pa_status separate_read(Phase ph, const pa_separate_params* p, const void* query
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace ? workspace_bytes : (size_t)0, need);
-  ReadArgs a{query,     num_tokens, key_cache,   value_cache, head_sink, q_norm,
+  ReadArgs a{query,     num_tokens, key_cache,   value_cache, head_sink,   q_norm,
              cos_cache, sin_cache,  cumseq,      past,        block_table, num_seqs,
-             seq_begin, seq_end,    workspace,   workspace_bytes, out, err_flags,
-             reinterpret_cast<cudaStream_t>(stream)};
+             seq_begin, seq_end,    seq_begin,   seq_end,     workspace,   workspace_bytes,
+             out,       err_flags,  reinterpret_cast<cudaStream_t>(stream)};
   return cuda_status(launch_separate_read(g, ph, a), "SEPARATE attention launch");
+}
+
+// One read call over a whole batch: decode splits for sequences [0, nd)
+// and prefill units for [nd, num_seqs) in one attention launch where the
+// single-CTA tensor-core kernels run; otherwise a decode call and a prefill
+// call in that order.
+pa_status mixed_read(const pa_latent_params* p, const void* query, int64_t num_tokens,
+                     const void* key_cache, const void* cos_cache, const void* sin_cache,
+                     const int32_t* cumseq, const int32_t* past, const int32_t* block_table,
+                     int32_t num_seqs, int32_t nd, void* workspace, size_t workspace_bytes,
+                     void* out, int32_t* err_flags, void* stream) {
+  Geometry g;
+  pa_status s = resolve(p, &g);
+  if (s != PA_OK) return s;
+  if (nd < 0 || nd > num_seqs)
+    return fail(PA_ERR_INVALID_ARGUMENT, "num_decode_seqs %d outside [0, %d]", nd, num_seqs);
+  const bool one_grid = nd > 0 && nd < num_seqs && use_tc(g, Phase::kMixed);
+  if (!one_grid) {
+    if (nd > 0) {
+      s = read_phase(Phase::kDecode, p, query, num_tokens, key_cache, cos_cache, sin_cache,
+                     cumseq, past, block_table, num_seqs, 0, nd, workspace, workspace_bytes, out,
+                     err_flags, stream);
+      if (s != PA_OK) return s;
+    }
+    if (nd == num_seqs) return PA_OK;
+    // a prefill call that follows the decode call reads no earlier write
+    pa_latent_params q = *p;
+    if (nd > 0) q.flags &= ~(PA_FLAG_AFTER_WRITE | PA_FLAG_OWN_SLOTS);
+    return read_phase(Phase::kPrefill, &q, query, num_tokens, key_cache, cos_cache, sin_cache,
+                      cumseq, past, block_table, num_seqs, nd, num_seqs, workspace,
+                      workspace_bytes, out, err_flags, stream);
+  }
+  if ((s = check_tokens(num_tokens, num_seqs, g)) != PA_OK) return s;
+  if ((int64_t)nd > num_tokens)
+    return fail(PA_ERR_INVALID_ARGUMENT,
+                "decode over %d sequences needs at least that many tokens (have %lld)", nd,
+                (long long)num_tokens);
+  if (!query || !key_cache || !cumseq || !past || !block_table || !out)
+    return fail(PA_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
+  if (g.rd > 0 && (!cos_cache || !sin_cache))
+    return fail(PA_ERR_INVALID_ARGUMENT, "cos_cache/sin_cache are required when rotary_dim > 0");
+  if (!aligned(query, 16) || !aligned(key_cache, 16) || !aligned(out, 16) ||
+      (g.rd > 0 && (!aligned(cos_cache, 16) || !aligned(sin_cache, 16))))
+    return fail(PA_ERR_INVALID_ARGUMENT, "half-precision tensors must be 16-byte aligned");
+  if (!aligned(cumseq, 4) || !aligned(past, 4) || !aligned(block_table, 4) ||
+      !aligned(err_flags, 4))
+    return fail(PA_ERR_INVALID_ARGUMENT, "int32 tensors must be 4-byte aligned");
+  if (workspace && !aligned(workspace, 256))
+    return fail(PA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  const size_t need = tc_call_workspace(g, Phase::kMixed, 0, nd);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(PA_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace ? workspace_bytes : (size_t)0, need);
+  ReadArgs a{query,     num_tokens, key_cache, nullptr, nullptr,     nullptr,
+             cos_cache, sin_cache,  cumseq,    past,    block_table, num_seqs,
+             0,         nd,         nd,        num_seqs, workspace,  workspace_bytes,
+             out,       err_flags,  reinterpret_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_tc(g, Phase::kMixed, a), "tensor-core attention launch (mixed)");
 }
 
 pa_status record_error(pa_status s, const char* msg) { return fail(s, "%s", msg); }
@@ -387,6 +445,17 @@ pa_status pa_latent_prefill(const pa_latent_params* p, const void* query, int64_
   return read_phase(Phase::kPrefill, p, query, num_tokens, key_cache, cos_cache, sin_cache,
                     cumseq, past, block_table, num_seqs, seq_begin, seq_end, workspace,
                     workspace_bytes, out, err_flags, stream);
+}
+
+pa_status pa_latent_mixed(const pa_latent_params* p, const void* query, int64_t num_tokens,
+                          const void* key_cache, const void* cos_cache, const void* sin_cache,
+                          const int32_t* cumseq, const int32_t* past,
+                          const int32_t* block_table, int32_t num_seqs,
+                          int32_t num_decode_seqs, void* workspace, size_t workspace_bytes,
+                          void* out, int32_t* err_flags, void* stream) {
+  return mixed_read(p, query, num_tokens, key_cache, cos_cache, sin_cache, cumseq, past,
+                    block_table, num_seqs, num_decode_seqs, workspace, workspace_bytes, out,
+                    err_flags, stream);
 }
 
 size_t pa_latent_workspace_size(const pa_latent_params* p, int32_t num_seqs,

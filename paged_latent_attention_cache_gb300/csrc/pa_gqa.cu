@@ -936,6 +936,9 @@ cudaError_t launch_separate_read(const Geometry& g, Phase ph, const ReadArgs& a)
   P.early = (g.flags & PA_FLAG_AFTER_WRITE) ? 1 : 0;
   P.own_slots = (g.flags & PA_FLAG_OWN_SLOTS) ? 1 : 0;
   P.tpc = tpc;
+  P.mixed = 0;
+  P.pf_begin = a.seq_begin;
+  P.pf_end = a.seq_end;
   P.kvh = g.kvh;
   P.grp = grp;
   P.head_sink = a.head_sink;

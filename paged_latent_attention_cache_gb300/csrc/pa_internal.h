@@ -36,7 +36,9 @@ struct Geometry {
   int device;       // current device ordinal
 };
 
-enum class Phase { kDecode = 0, kPrefill = 1 };
+// kMixed: one launch over a batch whose first sequences are decodes (one
+// new token each) and the rest prefills.
+enum class Phase { kDecode = 0, kPrefill = 1, kMixed = 2 };
 
 // Runs an idempotent per-device set-up action (a kernel attribute) once per
 // device ordinal < 64. Safe when several host threads make their first call
@@ -80,6 +82,7 @@ struct ReadArgs {
   const int32_t* past;
   const int32_t* block_table;
   int32_t num_seqs, seq_begin, seq_end;
+  int32_t pf_begin, pf_end;  // kMixed: the prefill sequences (decode: [seq_begin, seq_end))
   void* workspace;
   size_t workspace_bytes;
   void* out;

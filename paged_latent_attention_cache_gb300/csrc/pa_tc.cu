@@ -10,6 +10,12 @@ namespace tc {
 
 bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.H > kRows) return false;
+  // a mixed batch runs in one grid on the single-CTA kernel, in its prefill
+  // shape (the decode splits then use that shape too)
+  if (ph == Phase::kMixed) {
+    if (g.hs == 576 && g.vhs == 512) return false;
+    ph = Phase::kPrefill;
+  }
   if (g.hs == 576 && g.vhs == 512) {
     // CTA-pair kernel (pa_tc_pair.cu): each CTA rotates the query channels it
     // holds, so the rotary channels must lie in one CTA's range. It reads a
@@ -89,7 +95,7 @@ size_t tc_workspace_bytes(const Geometry& g, Phase ph, int32_t num_seqs, int64_t
 
 size_t tc_call_workspace(const Geometry& g, Phase ph, int32_t seq_begin, int32_t seq_end) {
   tc::Shape s;
-  if (ph == Phase::kPrefill || !tc::pick(g, ph, &s)) return 0;
+  if (ph == Phase::kPrefill || seq_end <= seq_begin || !tc::pick(g, ph, &s)) return 0;
   const int64_t nq = (int64_t)(seq_end - seq_begin);
   return tc::decode_ws_bytes(s, tc::decode_units(g, s, nq), nq);
 }
@@ -98,13 +104,16 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   tc::Shape s;
   if (!tc::pick(g, ph, &s)) return cudaErrorNotSupported;
   // prefill units: 128 / H consecutive tokens of one sequence (one token on
-  // the CTA pair); at most ceil(T / tpc) + nseq units are needed
-  const int tpc = (ph == Phase::kPrefill && s.groups == 1) ? tc::kRows / g.H : 1;
+  // the CTA pair); at most ceil(T / tpc) + nseq units are needed. A mixed
+  // launch has the decode splits of [seq_begin, seq_end) first, then the
+  // prefill units of [pf_begin, pf_end).
+  const int tpc = (ph != Phase::kDecode && s.groups == 1) ? tc::kRows / g.H : 1;
   const int64_t nseq = (int64_t)(a.seq_end - a.seq_begin);
+  const int64_t npf = ph == Phase::kMixed ? (int64_t)(a.pf_end - a.pf_begin) : nseq;
   const int64_t nq = ph == Phase::kDecode ? nseq
-                     : tpc > 1             ? (a.num_tokens + tpc - 1) / tpc + nseq
-                                           : a.num_tokens;
-  if (nq <= 0 || (ph == Phase::kPrefill && a.num_tokens <= 0)) return cudaSuccess;
+                     : tpc > 1 || ph == Phase::kMixed ? (a.num_tokens + tpc - 1) / tpc + npf
+                                                      : a.num_tokens;
+  if (nq <= 0 || (ph != Phase::kDecode && a.num_tokens <= 0)) return cudaSuccess;
   tc::Params P;
   P.query = a.query;
   P.out = a.out;
@@ -166,17 +175,20 @@ cudaError_t launch_tc(const Geometry& g, Phase ph, const ReadArgs& a) {
   P.early = (g.flags & PA_FLAG_AFTER_WRITE) ? 1 : 0;
   P.tpc = tpc;
   P.own_slots = (g.flags & PA_FLAG_OWN_SLOTS) ? 1 : 0;
+  P.mixed = ph == Phase::kMixed ? 1 : 0;
+  P.pf_begin = a.pf_begin;
+  P.pf_end = a.pf_end;
   P.ws_o = nullptr;
   P.ws_ml = nullptr;
   P.ws_plan = nullptr;
   P.units = 0;
-  if (ph == Phase::kDecode) {
-    const int64_t units = tc::decode_units(g, s, nq);
+  if (ph != Phase::kPrefill) {
+    const int64_t units = tc::decode_units(g, s, nseq);
     P.units = (int)units;
     const size_t per = (size_t)units * s.groups * tc::kRows;
     const size_t o = ((per * s.vg * sizeof(float)) + 255) & ~(size_t)255;
     const size_t ml = ((per * 2 * sizeof(float)) + 255) & ~(size_t)255;
-    if (a.workspace == nullptr || a.workspace_bytes < tc::decode_ws_bytes(s, units, nq)) {
+    if (a.workspace == nullptr || a.workspace_bytes < tc::decode_ws_bytes(s, units, nseq)) {
       set_launch_step("decode workspace");
       return cudaErrorInvalidValue;
     }

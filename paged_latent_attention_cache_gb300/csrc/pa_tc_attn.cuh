@@ -201,7 +201,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   if (warp == 0) {
     if (!P.early) grid_dep_wait();
     Work w;
-    if (P.decode) {
+    if (P.mixed ? unit < P.units : P.decode != 0) {
       // the query region is free until the query load that follows the plan
       w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), q_bytes / 4);
       if (w.status == 0) {
@@ -220,8 +220,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           w.ntok = 1;
         }
       }
-    } else if (P.tpc > 1) {
-      w = prefill_group_warp(P, unit, P.tpc);
+    } else if (P.tpc > 1 || P.mixed) {
+      w = prefill_group_warp(P, P.mixed ? unit - P.units : unit, P.tpc);
       if (w.status == 0) {
         const int64_t lo_key = P.window >= 0 ? max((int64_t)0, w.pos - P.window) : 0;
         w.t_begin = lo_key / N;
@@ -232,6 +232,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       int64_t pos;
       w.status = 1;
       w.splits = 1;
+      w.decode = 0;
       // CTA `unit` takes token T - 1 - unit: the tokens with the most keys
       // (the last of each sequence) start first, short ones fill in behind
       const int64_t tok = P.num_tokens - 1 - unit;
@@ -635,7 +636,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (lane == 0)
             okw = wait_bar(smem_u32(&pempty[stage]), ((k / pst) & 1) ^ 1, abort, P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
-        } else if (P.decode && k == 2 && nsub <= 2) {
+        } else if (W.decode && k == 2 && nsub <= 2) {
           // Decode: every CTA starts at once, and with few copies per tile
           // their first stages would all be in flight together; the first
           // tile then lands only behind most of that burst. The first two
@@ -918,14 +919,17 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
     set_launch_step("query tensor map");
     return cudaErrorInvalidValue;
   }
-  const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
+  // grid: the decode units, the prefill units, or (mixed) both
+  const int64_t units = ph == Phase::kDecode  ? (int64_t)P.units
+                        : ph == Phase::kMixed ? (int64_t)P.units + nq
+                                              : nq;
   e = launch_pdl(kern, dim3((unsigned)units), dim3(C::kThreads), smem, a.stream, map, qmap, P);
   if (e != cudaSuccess) {
     set_launch_step("attention kernel launch");
     return e;
   }
-  if (ph != Phase::kDecode) return e;
-  e = launch_combine<T>(P, g.H, nq, a.stream);
+  if (ph == Phase::kPrefill) return e;
+  e = launch_combine<T>(P, g.H, (int64_t)(P.seq_end - P.seq_begin), a.stream);
   if (e != cudaSuccess) set_launch_step("combine kernel launch");
   return e;
 }

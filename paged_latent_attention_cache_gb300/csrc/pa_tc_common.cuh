@@ -240,6 +240,11 @@ struct Params {
                      // the cache may be read before griddepcontrol.wait
   int tpc;           // prefill: consecutive tokens per work unit (rows = tpc * H <= 128)
   int own_slots;     // with early: the write touches no row below a sequence's past
+  // One grid for a mixed batch: units [0, units) are the decode splits of
+  // sequences [seq_begin, seq_end), the units after them prefill units of
+  // sequences [pf_begin, pf_end) (a prefill-only launch has pf_* = seq_*).
+  int mixed;
+  int pf_begin, pf_end;
   // Accumulator layout: `groups` CTAs (or CTAs of a pair) each hold `vg`
   // value channels of a head (vg a multiple of 64, groups * vg >= vhs).
   int vg, groups;
@@ -310,6 +315,7 @@ struct Work {
   int b, splits, first, split;
   int ntok;    // consecutive tokens of sequence b in the unit (rows = ntok * H)
   int status;  // 0 = run, 1 = idle, 2 = error already reported (write nothing more)
+  int decode;  // the unit is a decode split
 };
 
 // Block ids of the key boxes a producer warp copies, requested 32 boxes at
@@ -569,6 +575,7 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
   Work w;
   w.status = 1;
   w.b = -1;
+  w.decode = 1;
   w.t_begin = w.t_end = 0;
   int hit = 0, tiles_hit = 0;
   for (int i = lane; i < nseq; i += 32) {
@@ -613,11 +620,12 @@ __device__ Work decode_plan_warp(const Params& P, int unit, int* more, int cap) 
 // first and short ones fill in behind them. Run by one full warp.
 __device__ __forceinline__ Work prefill_group_warp(const Params& P, int unit, int tpc) {
   const int lane = threadIdx.x & 31;
-  const int seq_begin = P.seq_begin, nseq = P.seq_end - seq_begin;
+  const int seq_begin = P.pf_begin, nseq = P.pf_end - seq_begin;
   Work w;
   w.status = 1;
   w.splits = 1;
   w.ntok = 0;
+  w.decode = 0;
   int total = 0;
   for (int i = lane; i < nseq; i += 32) {
     const int q = P.cumseq[seq_begin + i + 1] - P.cumseq[seq_begin + i];

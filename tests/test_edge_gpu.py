@@ -214,6 +214,61 @@ def test_pair_kernel_logits_beyond_fp16_range(dtype, gain):
     print(f"RATIO pair_huge x{gain} {W.dtype_tag(dtype)}: {ties} near-tied rows")
 
 
+def _graph_kernel_nodes(fn):
+    """Kernel launches of fn() captured in a CUDA graph (driver API count)."""
+    import ctypes
+    g = torch.cuda.CUDAGraph(keep_graph=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    with torch.cuda.graph(g):
+        fn()
+    g.instantiate()
+    cu = ctypes.CDLL("libcuda.so.1")
+    h = ctypes.c_void_p(g.raw_cuda_graph())
+    n = ctypes.c_size_t(0)
+    assert cu.cuGraphGetNodes(h, None, ctypes.byref(n)) == 0
+    nodes = (ctypes.c_void_p * n.value)()
+    assert cu.cuGraphGetNodes(h, nodes, ctypes.byref(n)) == 0
+    cnt = 0
+    for nd in nodes:
+        t = ctypes.c_int(-1)
+        cu.cuGraphNodeGetType(ctypes.c_void_p(nd), ctypes.byref(t))
+        cnt += t.value == 0
+    return cnt
+
+
+@pytest.mark.parametrize("name", ["mixed_serving", "tiny"])
+def test_mixed_batch_in_one_grid(name):
+    """A batch of decode and prefill sequences read by one pa_latent_mixed
+    call: one attention grid (write + attention + combine = 3 launches,
+    against 4 for a decode call and a prefill call), and both forms meet the
+    bounds against the oracle."""
+    w = Hn.workload(name)
+    d = w.to("cuda")
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    op = PagedLatentAttention.from_workload(w)
+    base = d.key_cache.clone()
+    ref = Hn.run_oracle(w)
+    shape = (w.num_tokens, w.num_heads * w.v_head_size)
+    for one_call, launches in ((True, 3), (False, 4)):
+        cache = base.clone()
+        out = torch.full(shape, float("nan"), dtype=w.dtype, device="cuda")
+        fn = lambda: op.forward(d.query, d.key, cache, d.cos_cache, d.sin_cache, d.cumseq,
+                                d.past, d.block_table, d.slot_mapping, w.num_decode_seqs,
+                                out=out, one_call=one_call)
+        assert _graph_kernel_nodes(fn) == launches
+        cache.copy_(base)
+        fn()
+        torch.cuda.synchronize()
+        assert op.error_flags() == 0
+        Hn.check_cache(w, W.to_bits(cache), ref["cache"])
+        err, ratio = Hn.check_out(w, W.to_bits(out), ref["out"], scales=ref["scales"])
+        print(f"RATIO {name} one_call={one_call}: max abs err {err:.3e}, {ratio:.3f} of bound")
+
+
 def test_long_decode_splits():
     """Long contexts (many key splits merged by the combine step)."""
     w = W.make_workload("long", q_lens=[1, 1, 1], past_lens=[20000, 3, 777], num_heads=16,
