@@ -19,10 +19,9 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.hs == 576 && g.vhs == 512) {
     // CTA-pair kernel (pa_tc_pair.cu): each CTA rotates the query channels it
     // holds, so the rotary channels must lie in one CTA's range. It reads a
-    // cache in the query dtype only.
-    if (g.fp8) return false;
+    // cache in the query dtype, or (FP8) two fp16 stages and two E4M3 stages.
     if (!(g.rd == 0 || g.ro >= 320 || g.ro + g.rd <= 256)) return false;
-    *s = Shape{576, 256, 2, 64, 3, 128, 2, true};
+    *s = Shape{576, 256, 2, 64, g.fp8 ? 2 : 3, 128, 2, true, g.fp8 ? 2 : 0};
     return true;
   }
   // (a latent narrower than one 64-channel TMA box runs on the portable kernels)

@@ -56,26 +56,6 @@ constexpr int fixed_tmem_cols(int used) {
   return used <= 32 ? 32 : used <= 64 ? 64 : used <= 128 ? 128 : used <= 256 ? 256 : 512;
 }
 
-// Two E4M3 codes (low byte first) as an fp16x2 word (low half first).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
-// Eight f32 values as fp16, saturated to +-65504; records in *big whether one
-// was beyond that range (NaN stays NaN).
-__device__ __forceinline__ uint4 pack8_f16_sat(const float (&f)[8], bool* big) {
-  uint32_t w[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float a = f[2 * i], b = f[2 * i + 1];
-    *big |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;
-    a = fminf(fmaxf(a, -65504.f), 65504.f);
-    b = fminf(fmaxf(b, -65504.f), 65504.f);
-    w[i] = pack2<__half>(a, b);
-  }
-  return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 // FP8 cache with a bf16 query: one query row, in place in its swizzled
 // slabs (16-byte chunk c of row r at c ^ (r & 7)), from bf16 to fp16 (the
@@ -774,12 +754,13 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // (empty, committed after PV of the tile that used it before), convert
       // (every E4M3 value is an fp16 normal, so exactly) into the 128-byte-
       // swizzled K-major layout the MMAs read (16-byte chunk c of row r at
-      // c ^ (r & 7) in its 64-channel slab), then release both. Thread ct
-      // handles row ct / (128 / N) of the tile.
-      constexpr int kTpr = 128 / N;  // converter threads per key row
+      // c ^ (r & 7) in its 64-channel slab), then release both. The tile's
+      // N rows x hs/16 chunks are dealt to the 128 threads chunk by chunk,
+      // so consecutive threads read consecutive chunks of a row (no bank
+      // conflicts on the E4M3 reads).
       const int ct = tid - C::kConvWarp * 32;
-      const int r = ct / kTpr, j0 = ct % kTpr;
       const int hs16 = hs / 16;
+      const int dr = 128 / hs16, dj = 128 - dr * hs16;  // (row, chunk) step of 128 chunks
       const int st8 = P.stages8;
       for (int k = 0; k < n; ++k) {
         const int s8 = k % st8, s16 = k % stages;
@@ -788,11 +769,17 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           okc = wait_bar(smem_u32(&bars->empty[s16]), ((k / stages) & 1) ^ 1, abort,
                          P.err_flags);
         if (!__all_sync(0xffffffffu, okc)) break;
-        const uint8_t* src = k8_s + s8 * P.stage8_bytes + r * hs;
-        uint8_t* dst = k_s + s16 * stage_bytes + r * 128;
+        const uint8_t* src8 = k8_s + s8 * P.stage8_bytes;
+        int r = ct / hs16, j = ct - r * hs16;
 #pragma unroll 2
-        for (int j = j0; j < hs16; j += kTpr) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + j * 16);
+        for (; r < N; r += dr, j += dj) {
+          if (j >= hs16) {
+            j -= hs16;
+            ++r;
+            if (r >= N) break;
+          }
+          uint8_t* dst = k_s + s16 * stage_bytes + r * 128;
+          const uint4 v = *reinterpret_cast<const uint4*>(src8 + r * hs + j * 16);
           const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
                                       e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
           const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),

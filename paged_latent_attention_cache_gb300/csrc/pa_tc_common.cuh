@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp8.h>
 
 #include <type_traits>
 
@@ -426,6 +427,27 @@ template <>
 __device__ __forceinline__ uint32_t pack2<__half>(float a, float b) {
   __half2 v = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two E4M3 codes (low byte first) as an fp16x2 word (low half first).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Eight f32 values as fp16, saturated to +-65504; records in *big whether one
+// was beyond that range (NaN stays NaN).
+__device__ __forceinline__ uint4 pack8_f16_sat(const float (&f)[8], bool* big) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float a = f[2 * i], b = f[2 * i + 1];
+    *big |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;
+    a = fminf(fmaxf(a, -65504.f), 65504.f);
+    b = fminf(fmaxf(b, -65504.f), 65504.f);
+    w[i] = pack2<__half>(a, b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 // Probabilities of one 32-column chunk of a row's scores (softmax pass 2):

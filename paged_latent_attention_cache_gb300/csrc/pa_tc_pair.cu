@@ -31,9 +31,71 @@
 namespace pa {
 namespace tc {
 
-template <int N, int STAGES>
+// FP8 cache with a bf16 query: one query row of this CTA's slabs (four full
+// 128-byte-swizzled slabs from global slab q_full0, and a 32-channel half
+// slab) from bf16 to fp16 in place. Rotary channels (inside the full slabs)
+// are rotated in f32 and rounded once; every other 16-byte chunk of the row
+// is converted where it lies (an element-wise conversion needs no
+// unswizzling). A value beyond 65504 is saturated and flags PA_DEVERR_RANGE.
+template <typename T, int QBOX, int QHALF>
+__device__ __noinline__ void pair_q_row_to_f16(uint8_t* q_s, int row, int q_full0, int q_full_off,
+                                               int q_half_off, const Params& P, int64_t pos) {
+  const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;
+  const bool rope = P.rd > 0 && P.ro >= c_lo && P.ro + P.rd <= c_hi;
+  const int ro = P.ro, rd = P.rd, half = rd >> 1;
+  bool big = false;
+  auto at = [&](int d0) -> uint4* {
+    const int slab = (d0 >> 6) - q_full0, ch = (d0 >> 3) & 7;
+    return reinterpret_cast<uint4*>(q_s + q_full_off + slab * QBOX + row * 128 +
+                                    ((ch ^ (row & 7)) << 4));
+  };
+  if (rope) {
+    const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * half;
+    const T* srow = reinterpret_cast<const T*>(P.sin_cache) + pos * half;
+    if (!P.interleaved) {
+      for (int d0 = ro; d0 < ro + half; d0 += 8) {
+        float a[8], bb[8], na[8], nb[8];
+        unpack8<T>(*at(d0), a);
+        unpack8<T>(*at(d0 + half), bb);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) { na[e] = a[e]; nb[e] = bb[e]; }
+        rope8<T>(na, bb, d0, ro, rd, 0, crow, srow);
+        rope8<T>(nb, a, d0 + half, ro, rd, 0, crow, srow);
+        *at(d0) = pack8_f16_sat(na, &big);
+        *at(d0 + half) = pack8_f16_sat(nb, &big);
+      }
+    } else {
+      for (int d0 = ro; d0 < ro + rd; d0 += 8) {
+        float a[8], dummy[8];
+        unpack8<T>(*at(d0), a);
+        rope8<T>(a, dummy, d0, ro, rd, 1, crow, srow);
+        *at(d0) = pack8_f16_sat(a, &big);
+      }
+    }
+  }
+  for (int s = 0; s < 4; ++s) {
+    uint4* base = reinterpret_cast<uint4*>(q_s + q_full_off + s * QBOX + row * 128);
+    for (int pc = 0; pc < 8; ++pc) {
+      const int d0 = (q_full0 + s) * 64 + ((pc ^ (row & 7)) << 3);
+      if (rope && d0 >= ro && d0 < ro + rd) continue;  // already fp16
+      float a[8];
+      unpack8<T>(base[pc], a);
+      base[pc] = pack8_f16_sat(a, &big);
+    }
+  }
+  uint4* hb = reinterpret_cast<uint4*>(q_s + q_half_off + row * 64);
+  for (int pc = 0; pc < 4; ++pc) {
+    float a[8];
+    unpack8<T>(hb[pc], a);
+    hb[pc] = pack8_f16_sat(a, &big);
+  }
+  if (big) raise_flag(P.err_flags, PA_DEVERR_RANGE);
+}
+
+template <int N, int STAGES, bool FP8 = false>
 struct PairCfg {
-  static constexpr int kThreads = 320;              // warps 0-3, 4, 5, 6-9 (see above)
+  // warps 0-3, 4, 5, 6-9 (see above); FP8: converter warps 10-11
+  static constexpr int kThreads = FP8 ? 384 : 320;
   static constexpr int kSlabs = 5;                  // 64-channel slabs per CTA (of 9)
   static constexpr int kSteps = 18;                 // 16-channel QK^T K-steps per CTA
   static constexpr int kQBox = kRows * 128;         // bytes per full query slab (SW128)
@@ -42,7 +104,12 @@ struct PairCfg {
   static constexpr int kKBox = N * 128;             // bytes per key slab of a stage
   static constexpr int kStageBytes = kSlabs * kKBox;
   static constexpr int kXBytes = kRows * N * 4;     // incoming partial-S rows
-  static constexpr int kSmemData = kQBytes + STAGES * kStageBytes + kXBytes;
+  // FP8 cache: two E4M3 stages of N rows x this CTA's 320 channels (a box
+  // of 256 channels and one of 64: a TMA box is at most 256 elements wide)
+  static constexpr int kStages8 = FP8 ? 2 : 0;
+  static constexpr int kStage8Bytes = N * kSlabs * 64;
+  static constexpr int kSmemData =
+      kQBytes + STAGES * kStageBytes + kXBytes + kStages8 * kStage8Bytes;
   static constexpr int kVG = 256;                   // output channels per CTA
   static constexpr int kSBufs = 3;                  // S buffers in TMEM
   static constexpr int kColO = 0;
@@ -55,6 +122,7 @@ struct PairCfg {
 
 struct PairBarriers {
   uint64_t full[4], empty[4];
+  uint64_t full8[2], empty8[2];  // FP8 cache: E4M3 ring (TMA -> converter warps)
   uint64_t s_part[3];  // QK^T(k) has written this CTA's partial S (tcgen05.commit)
   uint64_t s_sum[3];   // the exchange warps have written S_0 + S_1 back (128 arrivals)
   uint64_t s_free[3];  // the softmax warps are done with the S buffer (128 arrivals)
@@ -70,11 +138,16 @@ struct PairBarriers {
   int xfail;  // an exchange warp's wait failed: all four leave after the tile's barrier
 };
 
-template <typename T, int N, int STAGES>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<N, STAGES>::kThreads, 1)
+// FP8: the cache holds E4M3 codes; two converter warps turn each E4M3 tile
+// into the fp16 tile the MMAs read, the query is rounded to fp16 once, and
+// P is fp16 (every E4M3 value is an fp16 normal, so the keys are exact).
+template <typename T, int N, int STAGES, bool FP8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<N, STAGES, FP8>::kThreads, 1)
 tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-               const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ Params P) {
-  using C = PairCfg<N, STAGES>;
+               const __grid_constant__ CUtensorMap qmap64, const __grid_constant__ CUtensorMap kmap8b,
+               const __grid_constant__ Params P) {
+  using C = PairCfg<N, STAGES, FP8>;
+  using TM = typename std::conditional<FP8, __half, T>::type;  // MMA operand type
   constexpr int G = 2, VG = C::kVG, NS = C::kSBufs;
   // Score exchange: f32 partials, one 32 KB tile in x_s at a time. (A 16-bit
   // format would hold two tiles, but it rounds a partial logit L by |L| *
@@ -89,6 +162,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   uint8_t* q_s = smem;
   uint8_t* k_s = smem + C::kQBytes;
   float* x_s = reinterpret_cast<float*>(smem + C::kQBytes + STAGES * C::kStageBytes);
+  uint8_t* k8_s = smem + C::kQBytes + STAGES * C::kStageBytes + C::kXBytes;  // FP8 ring
   PairBarriers* bars = reinterpret_cast<PairBarriers*>(smem + C::kSmemData);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -161,8 +235,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if (lane == 0) work = w;
   } else if (warp == 1 && lane == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(smem_u32(&bars->full[s]), 1);
+      // (FP8: complete when both converter warps have written their rows)
+      mbar_init(smem_u32(&bars->full[s]), FP8 ? 64 : 1);
       mbar_init(smem_u32(&bars->empty[s]), 1);
+    }
+    for (int s = 0; s < C::kStages8; ++s) {
+      mbar_init(smem_u32(&bars->full8[s]), 1);
+      mbar_init(smem_u32(&bars->empty8[s]), 64);
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&bars->s_part[i]), 1);
@@ -188,6 +267,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     prefetch_tmap(&kmap);
     prefetch_tmap(&qmap);
     prefetch_tmap(&qmap64);
+    if (FP8) prefetch_tmap(&kmap8b);
   } else if (warp == 5) {
     tmem_alloc(smem_u32(&bars->tmem_base), C::kTmemCols);
     tmem_relinquish();
@@ -236,7 +316,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
           // RoPE in place on this CTA's slabs (the pair kernel only runs when
           // the rotary channels and their partners lie inside one CTA's slabs).
-          if (ok && P.rd > 0 && row < P.H) {
+          if (FP8 && !std::is_same<T, __half>::value) {
+            // bf16 query, fp16 MMA operands: this CTA's query channels of the
+            // row become fp16 in place (rotary channels rotated in f32 first)
+            if (ok && row < P.H)
+              pair_q_row_to_f16<T, C::kQBox, C::kQHalf>(q_s, row, q_full0, q_full_off,
+                                                        q_half_off, P, pos);
+          } else if (ok && P.rd > 0 && row < P.H) {
             const int c_lo = q_full0 * 64, c_hi = c_lo + 4 * 64;  // full query slabs only
             if (P.ro >= c_lo && P.ro + P.rd <= c_hi) {
               const T* crow = reinterpret_cast<const T*>(P.cos_cache) + pos * (P.rd >> 1);
@@ -355,7 +441,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
               const float p0 = ex2(fmaf(__uint_as_float(r[2 * e]), sl, -m_used));
               const float p1 = ex2(fmaf(__uint_as_float(r[2 * e + 1]), sl, -m_used));
               lsum += p0 + p1;
-              pk[e] = pack2<T>(p0, p1);
+              pk[e] = pack2<TM>(p0, p1);
             }
             tmem_st16(lane_addr + C::kColP + pb * (N / 2) + c / 2, pk);
           }
@@ -396,7 +482,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         tc_fence_after();
         const bool bad = bars->bad != 0;
         if (splits == 1) {
-          const float inv = (l > 0.f && !bad) ? 1.f / l : 0.f;
+          const float inv = (l > 0.f && !bad) ? P.out_scale / l : 0.f;
 #pragma unroll 1
           for (int c = 0; c < VG; c += 16) {
             uint32_t r[16];
@@ -421,10 +507,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             tmem_ld16(lane_addr + C::kColO + c, r);
             if (row < P.H) {
               float4* dst = reinterpret_cast<float4*>(wo + c);
+              const float os = P.out_scale;
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                dst[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                     __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+                dst[e] = make_float4(__uint_as_float(r[4 * e]) * os,
+                                     __uint_as_float(r[4 * e + 1]) * os,
+                                     __uint_as_float(r[4 * e + 2]) * os,
+                                     __uint_as_float(r[4 * e + 3]) * os);
             }
           }
           if (row < P.H) {
@@ -433,7 +522,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           }
         }
       }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {  // (FP8: warps 10-11 convert, below)
       // =================== partial-score exchange ===================
       // Warp w handles TMEM lanes 32*(w%4)..+31 (the quadrant its SM
       // sub-partition may access). Per tile: read this CTA's partial S rows,
@@ -530,18 +619,21 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
                    P.box_rows, P.bs, n * nsub};
       ids.start(lane);
+      // the ring the copies land in: key stages, or (FP8) the E4M3 stages
+      constexpr int PST = FP8 ? C::kStages8 : STAGES;
+      uint64_t* pfull = FP8 ? bars->full8 : bars->full;
+      uint64_t* pempty = FP8 ? bars->empty8 : bars->empty;
       int issued = 0;
       for (int k = 0; k < n; ++k) {
-        const int stage = k % STAGES;
+        const int stage = k % PST;
         if (!waited && k >= dirty_from) {
           grid_dep_wait();  // the write phase's cache rows are complete and visible
           waited = true;
         }
-        if (k >= STAGES) {
+        if (k >= PST) {
           bool okw = true;
           if (lane == 0)
-            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / STAGES) & 1) ^ 1, abort,
-                           P.err_flags);
+            okw = wait_bar(smem_u32(&pempty[stage]), ((k / PST) & 1) ^ 1, abort, P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
@@ -555,14 +647,23 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             raise_flag(P.err_flags, PA_DEVERR_BLOCK);
           }
         }
-        if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), C::kStageBytes);
+        if (lane == 0)
+          mbar_expect_tx(smem_u32(&pfull[stage]), FP8 ? C::kStage8Bytes : C::kStageBytes);
         __syncwarp();
         if (lane < nsub) {
-          const uint32_t full = smem_u32(&bars->full[stage]);
-          const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
+          const uint32_t full = smem_u32(&pfull[stage]);
+          if (FP8) {
+            // this CTA's 320 E4M3 channels of box_rows rows: 256 into the
+            // stage's first part (256-byte rows), 64 into its second part
+            const uint32_t d8 = smem_u32(k8_s + stage * C::kStage8Bytes);
+            tma_load_2d(d8 + lane * P.box_rows * 256, &kmap, slab0 * 64, y, full);
+            tma_load_2d(d8 + N * 256 + lane * P.box_rows * 64, &kmap8b, slab0 * 64 + 256, y, full);
+          } else {
+            const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
 #pragma unroll 1
-          for (int j = 0; j < C::kSlabs; ++j)
-            tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+            for (int j = 0; j < C::kSlabs; ++j)
+              tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+          }
         }
         issued = k + 1;
         __syncwarp();
@@ -570,9 +671,9 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       if (!waited) grid_dep_wait();  // the grid completes after the write grid
       if (*abort && lane == 0) {
         drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
-        for (int st = 0; st < STAGES && st < issued; ++st) {
-          const int kl = issued - 1 - ((issued - 1 - st) % STAGES);
-          drain_wait(smem_u32(&bars->full[st]), (kl / STAGES) & 1, P.err_flags);
+        for (int st = 0; st < PST && st < issued; ++st) {
+          const int kl = issued - 1 - ((issued - 1 - st) % PST);
+          drain_wait(smem_u32(&pfull[st]), (kl / PST) & 1, P.err_flags);
         }
       }
       __syncwarp();
@@ -580,7 +681,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     } else if (warp == 5) {
       // =================== MMA issuer ===================
       if (lane == 0) {
-        constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+        constexpr bool kBf16 = std::is_same<TM, __nv_bfloat16>::value;
         constexpr uint32_t kIdQK = idesc_f16(kBf16, kRows, N, false);
         constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
         const uint32_t q_base = smem_u32(q_s);
@@ -668,6 +769,43 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
       }
       __syncwarp();
+    } else if (FP8 && warp >= 10) {
+      // =============== E4M3 -> fp16 key tiles (FP8 cache) ===============
+      // The tile's 64 rows x 20 chunks of 16 channels are dealt to the 64
+      // threads chunk by chunk (consecutive threads read consecutive 16-byte
+      // chunks of a row, so the E4M3 reads do not collide in the shared-
+      // memory banks): from the two parts of the E4M3 stage into the five
+      // swizzled fp16 slabs (16-byte chunk c of row r at c ^ (r & 7)), once
+      // the fp16 stage is free (PV of the tile that used it before is done).
+      const int ct = tid - 320;  // 0..63
+      for (int k = 0; k < n; ++k) {
+        const int s8 = k % C::kStages8, s16 = k % STAGES;
+        bool okc = wait_bar(smem_u32(&bars->full8[s8]), (k / C::kStages8) & 1, abort,
+                            P.err_flags);
+        if (okc && k >= STAGES)
+          okc = wait_bar(smem_u32(&bars->empty[s16]), ((k / STAGES) & 1) ^ 1, abort,
+                         P.err_flags);
+        if (!__all_sync(0xffffffffu, okc)) break;
+        const uint8_t* s8p = k8_s + s8 * C::kStage8Bytes;
+#pragma unroll 4
+        for (int i = ct; i < N * 20; i += 64) {  // chunk j of row r
+          const int r = i / 20, j = i - r * 20;
+          uint8_t* dst = k_s + s16 * C::kStageBytes + r * 128;
+          const uint4 v = *reinterpret_cast<const uint4*>(
+              j < 16 ? s8p + r * 256 + j * 16 : s8p + N * 256 + r * 64 + (j - 16) * 16);
+          const uint4 lo = make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
+                                      e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
+          const uint4 hi = make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),
+                                      e4m3x2_to_f16x2(v.w & 0xffffu), e4m3x2_to_f16x2(v.w >> 16));
+          const int ch = (j & 3) * 2;  // first 16-byte chunk of the pair in its slab
+          uint8_t* d = dst + (j >> 2) * C::kKBox;
+          *reinterpret_cast<uint4*>(d + ((ch ^ (r & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(d + (((ch + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        fence_proxy_async();
+        mbar_arrive(smem_u32(&bars->full[s16]));
+        mbar_arrive(smem_u32(&bars->empty8[s8]));
+      }
     }
   }
 
@@ -680,49 +818,92 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   }
 }
 
-template <typename T>
-cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
-  constexpr int N = 64, STAGES = 3;
-  using C = PairCfg<N, STAGES>;
+template <typename T, bool FP8>
+cudaError_t launch_pair_impl(const Geometry& g, Phase ph, const ReadArgs& a, Params& P,
+                             int64_t nq) {
+  // bf16/fp16 cache: three key stages; FP8 cache: two fp16 key stages fed
+  // by the converter warps from two E4M3 stages (the same shared memory)
+  constexpr int N = 64, STAGES = FP8 ? 2 : 3;
+  using C = PairCfg<N, STAGES, FP8>;
   const size_t smem = C::kSmemData + sizeof(PairBarriers) + 1024;
   static std::atomic<bool> configured[64];
-  auto kern = tc_pair_kernel<T, N, STAGES>;
+  auto kern = tc_pair_kernel<T, N, STAGES, FP8>;
   cudaError_t e = once_per_device(configured, g.device, [&] {
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   });
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    set_launch_step("kernel shared-memory attribute");
+    return e;
+  }
   EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
+  if (!enc) {
+    set_launch_step("driver tensor-map encoder lookup");
+    return cudaErrorNotSupported;
+  }
   const CUtensorMapDataType dt = std::is_same<T, __nv_bfloat16>::value
                                      ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                      : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  CUtensorMap map, qmap;
+  CUtensorMap map, qmap, map8b;
   const cuuint64_t dims[2] = {576, (cuuint64_t)g.num_blocks * g.bs};
   const cuuint64_t strides[1] = {576 * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  CUresult r;
+  if (FP8) {
+    // E4M3 rows of 576 bytes: boxes of 256 and of 64 channels x box_rows rows
+    const cuuint64_t strides8[1] = {576};
+    const cuuint32_t box_a[2] = {256, (cuuint32_t)P.box_rows};
+    const cuuint32_t box_b[2] = {64, (cuuint32_t)P.box_rows};
+    r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.key_cache), dims,
+            strides8, box_a, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS)
+      r = enc(&map8b, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a.key_cache), dims,
+              strides8, box_b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint32_t box[2] = {64, (cuuint32_t)P.box_rows};
+    r = enc(&map, dt, 2, const_cast<void*>(a.key_cache), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    map8b = map;  // (unused)
+  }
+  if (r != CUDA_SUCCESS) {
+    set_launch_step("cache tensor map");
+    return cudaErrorInvalidValue;
+  }
   const cuuint64_t qdims[2] = {576, (cuuint64_t)a.num_tokens * g.H};
   const cuuint32_t qbox[2] = {64, (cuuint32_t)kRows};
   r = enc(&qmap, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox, estr,
           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // 32-channel boxes (64-byte rows, 64-byte swizzle) for the half query slab
   CUtensorMap qmap64;
   const cuuint32_t qbox64[2] = {32, (cuuint32_t)kRows};
-  r = enc(&qmap64, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox64, estr,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  if (r == CUDA_SUCCESS)
+    r = enc(&qmap64, dt, 2, const_cast<void*>(a.query), qdims, strides, qbox64, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_launch_step("query tensor map");
+    return cudaErrorInvalidValue;
+  }
   const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
   e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem, a.stream, map, qmap,
-                 qmap64, P);
-  if (e != cudaSuccess || ph != Phase::kDecode) return e;
-  return launch_combine<T>(P, g.H, nq, a.stream);
+                 qmap64, map8b, P);
+  if (e != cudaSuccess) {
+    set_launch_step("attention kernel launch");
+    return e;
+  }
+  if (ph != Phase::kDecode) return e;
+  e = launch_combine<T>(P, g.H, nq, a.stream);
+  if (e != cudaSuccess) set_launch_step("combine kernel launch");
+  return e;
+}
+
+template <typename T>
+cudaError_t launch_pair(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq) {
+  return g.fp8 ? launch_pair_impl<T, true>(g, ph, a, P, nq)
+               : launch_pair_impl<T, false>(g, ph, a, P, nq);
 }
 
 template cudaError_t launch_pair<__nv_bfloat16>(const Geometry&, Phase, const ReadArgs&, Params&,

@@ -98,15 +98,28 @@ def test_fp8_query_beyond_fp16_range_is_flagged():
 
 
 def test_fp8_cache_not_built_paths_say_so():
-    """FP8 on the CTA-pair geometry (576/512) and on the portable kernels is
-    not built: the read calls return PA_ERR_NOT_IMPLEMENTED before any
-    launch."""
-    for kw, portable in ((dict(num_heads=16, **W.DSV3), False), (dict(num_heads=4, **W.GLM), True)):
-        w = W.make_workload("fp8_nyi", q_lens=[1], past_lens=[10], block_size=16, seed=31,
-                            cache_dtype="e4m3", **kw)
-        with pytest.raises(B.PaError) as e:
-            Hn.run_gpu(w, portable=portable)
-        assert e.value.status == B.PA_ERR_NOT_IMPLEMENTED
+    """FP8 on the portable kernels is not built: the read calls return
+    PA_ERR_NOT_IMPLEMENTED before any launch."""
+    w = W.make_workload("fp8_nyi", q_lens=[1], past_lens=[10], block_size=16, seed=31,
+                        cache_dtype="e4m3", num_heads=4, **W.GLM)
+    with pytest.raises(B.PaError) as e:
+        Hn.run_gpu(w, portable=True)
+    assert e.value.status == B.PA_ERR_NOT_IMPLEMENTED
+
+
+@pytest.mark.parametrize("kw", [dict(block_size=64), dict(block_size=16),
+                                dict(block_size=64, dtype=torch.float16),
+                                dict(block_size=64, k_scale=0.0123, softcap=4.0),
+                                dict(block_size=128, local_window_size=100)],
+                         ids=["bs64", "bs16", "fp16", "odd_scale_softcap", "bs128_window"])
+def test_fp8_cache_pair_kernel(kw):
+    """FP8 (E4M3) cache on the 576/512 CTA-pair kernel (two converter warps,
+    two fp16 and two E4M3 stages): decode and prefill tokens with several
+    key tiles and ragged tails."""
+    w = W.make_workload("fp8_pair", q_lens=[1, 1, 70, 1], past_lens=[300, 1, 200, 129],
+                        num_heads=128, **W.DSV3, seed=32, scale=W.DSV3_SCALE, drop_slots=1,
+                        cache_dtype="e4m3", **kw)
+    _check(w, family=1)
 
 
 @pytest.mark.parametrize("hs,vhs,ro,rd,H,family", [

@@ -78,12 +78,13 @@ def test_peaked_decode_parity(name, gain):
     print(f"RATIO {w.name}: max abs err {err:.3e}, {ratio:.3f} of the scale-aware bound")
 
 
-def test_fp8_cache_glm_decode_parity(oracle_results):
+@pytest.mark.parametrize("name", ["glm_decode_fp8", "dsv3_decode_fp8"])
+def test_fp8_cache_decode_parity(name, oracle_results):
     """GLM-style decode (H=64, 192/128, 32 sequences, contexts U[1024, 8192])
-    over an FP8 (E4M3) latent cache with k_scale = 1/64: the written codes
-    are bit-exact outside the rotary channels and within one code inside;
-    the outputs meet the bounds against the oracle of the FP8 operator."""
-    name = "glm_decode_fp8"
+    and DeepSeek-style decode (H=128, 576/512, 64 x 4096) over an FP8 (E4M3)
+    latent cache with k_scale = 1/64: the written codes are bit-exact outside
+    the rotary channels and within one code inside; the outputs meet the
+    bounds against the oracle of the FP8 operator."""
     w = Hn.workload(name)
     got = Hn.run_gpu(w)
     ref = _oracle(oracle_results, name)
