@@ -57,16 +57,19 @@ UNIT = "TB/s"
 # the kernel and the roofline reports null traffic until a new capture
 # replaces it.
 KERNEL_SOURCES = {
-    "tc_attn_kernel": ("pa_tc_attn.cuh", "pa_tc_common.cuh"),
+    "tc_attn_kernel": ("pa_tc_attn.cuh", "pa_tc_common.cuh", "pa_tc.cu", "pa_tc_glm.cu",
+                       "pa_tc_fp8.cu"),
     "tc_pair_kernel": ("pa_tc_pair.cu", "pa_tc_cluster.cuh", "pa_tc_common.cuh"),
 }
 # workload -> (kernel, bytes per launch, source digest, how the figure was taken)
 NCU_TRAFFIC = {
-    "dsv3_decode": ("tc_pair_kernel", 315302912, "6bfdcaeb45ee9672", "measured on this workload"),
+    "dsv3_decode": ("tc_pair_kernel", 314881536, "1f091fa36fe04250", "measured on this workload"),
     # traffic grows with the tokens (query in, output out, each sequence's
     # cache rows): the quarter-size capture times four
-    "dsv3_prefill": ("tc_pair_kernel", 4 * 1100012288, "6bfdcaeb45ee9672",
+    "dsv3_prefill": ("tc_pair_kernel", 4 * 1100246016, "1f091fa36fe04250",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
+    "glm_decode": ("tc_attn_kernel", 54297600, "6ae28b5c2d9db131", "measured on this workload"),
+    "glm_decode_fp8": ("tc_attn_kernel", 25966848, "6ae28b5c2d9db131", "measured on this workload"),
 }
 
 
@@ -446,11 +449,12 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
             "p90": round(q[-1], 5)}
 
     e2e_ms = h2d = d2h = None
-    if e2e and not separate:
+    if e2e:
         # End to end through the operator object: H2D of the step's inputs
-        # from pinned memory, the three phases, D2H of the output.
-        host = {k: getattr(w, k).pin_memory() for k in
-                ("query", "key", "cumseq", "past", "block_table", "slot_mapping")}
+        # from pinned memory, the phases, D2H of the output.
+        names = ("query", "key") + (("value",) if separate else ()) + \
+            ("cumseq", "past", "block_table", "slot_mapping")
+        host = {k: getattr(w, k).pin_memory() for k in names}
         dev_in = {k: torch.empty_like(v, device=device) for k, v in host.items()}
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host.values())
@@ -459,9 +463,16 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
         def e2e_step():
             for k, v in host.items():
                 dev_in[k].copy_(v, non_blocking=True)
-            op.forward(dev_in["query"], dev_in["key"], cache, d.cos_cache, d.sin_cache,
-                       dev_in["cumseq"], dev_in["past"], dev_in["block_table"],
-                       dev_in["slot_mapping"], nd, out=out)
+            if separate:
+                op.forward(dev_in["query"], dev_in["key"], dev_in["value"], cache, vcache,
+                           d.cos_cache, d.sin_cache, dev_in["cumseq"], dev_in["past"],
+                           dev_in["block_table"], dev_in["slot_mapping"], nd,
+                           head_sink=d.head_sink, q_norm_weight=d.q_norm_weight,
+                           k_norm_weight=d.k_norm_weight, out=out)
+            else:
+                op.forward(dev_in["query"], dev_in["key"], cache, d.cos_cache, d.sin_cache,
+                           dev_in["cumseq"], dev_in["past"], dev_in["block_table"],
+                           dev_in["slot_mapping"], nd, out=out)
             out_host.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -593,7 +604,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="dsv3_decode")
     ap.add_argument("--extras",
-                    default="dsv3_prefill,glm_decode,mixed_serving,glm_decode_fp8,gqa_decode",
+                    default="dsv3_prefill,glm_decode,mixed_serving,glm_decode_fp8,dsv3_decode_fp8,gqa_decode",
                     help="comma-separated workloads timed after the headline one "
                          "('none' to skip)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
