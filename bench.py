@@ -60,16 +60,19 @@ KERNEL_SOURCES = {
     "tc_attn_kernel": ("pa_tc_attn.cuh", "pa_tc_common.cuh", "pa_tc.cu", "pa_tc_glm.cu",
                        "pa_tc_fp8.cu"),
     "tc_pair_kernel": ("pa_tc_pair.cu", "pa_tc_cluster.cuh", "pa_tc_common.cuh"),
+    "tc_gqa_kernel": ("pa_gqa.cu", "pa_tc_common.cuh"),
 }
 # workload -> (kernel, bytes per launch, source digest, how the figure was taken)
 NCU_TRAFFIC = {
-    "dsv3_decode": ("tc_pair_kernel", 314881536, "1f091fa36fe04250", "measured on this workload"),
+    "dsv3_decode": ("tc_pair_kernel", 315040256, "be6bf68bd06a091f", "measured on this workload"),
     # traffic grows with the tokens (query in, output out, each sequence's
     # cache rows): the quarter-size capture times four
-    "dsv3_prefill": ("tc_pair_kernel", 4 * 1100246016, "1f091fa36fe04250",
+    "dsv3_prefill": ("tc_pair_kernel", 4 * 1099542528, "be6bf68bd06a091f",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
-    "glm_decode": ("tc_attn_kernel", 54297600, "6ae28b5c2d9db131", "measured on this workload"),
-    "glm_decode_fp8": ("tc_attn_kernel", 25966848, "6ae28b5c2d9db131", "measured on this workload"),
+    "glm_decode": ("tc_attn_kernel", 54257664, "53e331d2f8ef9cb5", "measured on this workload"),
+    "mixed_serving": ("tc_attn_kernel", 99262208, "53e331d2f8ef9cb5", "measured on this workload"),
+    "gqa_decode": ("tc_gqa_kernel", 580619008, "e5fd8ae0e2ff9a81", "measured on this workload"),
+    "glm_decode_fp8": ("tc_attn_kernel", 25967360, "53e331d2f8ef9cb5", "measured on this workload"),
 }
 
 
@@ -233,29 +236,62 @@ def barrier(device=None):
 # Oracle timing (cpu_baseline and --impl reference)
 # ---------------------------------------------------------------------------
 
+def oracle_session(w):
+    """The CPU oracle's write phase over the whole batch, then a function
+    that runs its read phase for one token (rounded to the output dtype):
+    LATENT with a 16-bit or E4M3 cache, or the SEPARATE layout."""
+    from oracle import pa_oracle as O
+    from paged_latent_attention_cache_gb300 import workloads as W
+    cumseq, past, bt = w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy()
+    if hasattr(w, "kv_num_heads"):
+        p = W.separate_oracle_params(w)
+        dt, hs, kvh = p["dtype"], w.head_size, w.kv_num_heads
+        vhs = p["v_head_size"] or hs
+        kc = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
+        vc = O.BitsCache(W.to_bits(w.value_cache).reshape(-1, vhs), dt)
+        cos_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt)
+        sin_t = O.bits_to_f64(W.to_bits(w.sin_cache), dt)
+        opt = lambda x: None if x is None else O.bits_to_f64(W.to_bits(x), dt)  # noqa: E731
+        kn, qn, sink = opt(w.k_norm_weight), opt(w.q_norm_weight), opt(w.head_sink)
+        kb, vb, qb = W.to_bits(w.key), W.to_bits(w.value), W.to_bits(w.query)
+        O.separate_write(lambda t: O.bits_to_f64(kb[t], dt).reshape(kvh, hs),
+                         lambda t: O.bits_to_f64(vb[t], dt).reshape(kvh, vhs), cos_t, sin_t,
+                         w.slot_mapping.numpy(), cumseq, past, kc, vc, p, kn)
+
+        def read(t):
+            out = O.separate_attend_token(t, O.bits_to_f64(qb[t], dt), kc, vc, cos_t, sin_t,
+                                          cumseq, past, bt, p, sink, qn)
+            return O.round_f64_to_bits(out, dt)
+        return read
+    p = W.oracle_params(w)
+    dt, hs = p["dtype"], w.head_size
+    if p.get("cache_dtype") == O.E4M3:
+        cache = O.E4M3Cache(W.to_bits(w.key_cache).reshape(-1, hs), p["k_scale"])
+    else:
+        cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
+    cos_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt)
+    sin_t = O.bits_to_f64(W.to_bits(w.sin_cache), dt)
+    kb, qb = W.to_bits(w.key), W.to_bits(w.query)
+    O.latent_write(lambda t: O.bits_to_f64(kb[t], dt), cos_t, sin_t, w.slot_mapping.numpy(),
+                   cumseq, past, cache, p)
+
+    def read(t):
+        out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
+                                    past, bt, p)
+        return O.round_f64_to_bits(out, dt)
+    return read
+
+
 def time_oracle(w, budget_s: float, tokens_order=None):
     """Runs the CPU oracle's read phase token by token (after its write phase
     over the whole batch) until ``budget_s`` of wall time is used. Returns
     (seconds, algorithmic bytes of the sampled work, tokens done)."""
-    import numpy as np
-    from oracle import pa_oracle as O
-    from paged_latent_attention_cache_gb300 import workloads as W
-    p = W.oracle_params(w)
-    dt = p["dtype"]
-    hs = w.head_size
     t0 = time.perf_counter()
-    cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
-    cos_t, sin_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt), O.bits_to_f64(W.to_bits(w.sin_cache), dt)
-    kb, qb = W.to_bits(w.key), W.to_bits(w.query)
-    cumseq, past, bt = w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy()
-    O.latent_write(lambda t: O.bits_to_f64(kb[t], dt), cos_t, sin_t, w.slot_mapping.numpy(),
-                   cumseq, past, cache, p)
+    read = oracle_session(w)
     done = []
     order = list(range(w.num_tokens)) if tokens_order is None else tokens_order
     for t in order:
-        out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
-                                    past, bt, p)
-        O.round_f64_to_bits(out, dt)
+        read(t)
         done.append(t)
         if time.perf_counter() - t0 >= budget_s:
             break
@@ -504,6 +540,74 @@ def measure_workload(args, name, rank, world, device, steps, warmup, flush, e2e=
     return res
 
 
+PROBE_WORKLOADS = ("glm_decode", "dsv3_decode")
+
+
+def run_probe(args, device, flush, peaks):
+    """Sweeps pa_latent_gather_probe (every visible cache row of a decode
+    batch gathered through the block table by the decode kernels' TMA boxes,
+    no arithmetic) over tile size, stages and CTAs per SM on the decode
+    workloads' caches; one JSON line per workload with the visible rows'
+    bytes over the CUDA-event time, against the measured copy bandwidth."""
+    import torch
+    from paged_latent_attention_cache_gb300 import binding as B
+    from paged_latent_attention_cache_gb300 import workloads as W
+    hbm = peaks[0]
+    steps = min(args.steps, 200)
+    names = [args.workload] if args.workload in PROBE_WORKLOADS and args.extras == "none" \
+        else list(PROBE_WORKLOADS)
+    for name in names:
+        w = W.WORKLOADS[name]()
+        d = w.to(device)
+        p = B.make_params(dtype=w.dtype, num_heads=w.num_heads, head_size=w.head_size,
+                          v_head_size=w.v_head_size, rotary_offset=w.rotary_offset,
+                          rotary_dim=w.rotary_dim, cos_rows=w.cos_cache.shape[0],
+                          block_size=w.block_size, num_blocks=w.key_cache.shape[0],
+                          max_blocks_per_seq=w.block_table.shape[1], scale=w.scale)
+        err = torch.zeros(1, dtype=torch.int32, device=device)
+        rows = int((w.past + 1).sum())
+        nbytes = rows * w.head_size * w.key_cache.element_size()
+        sweep = []
+        shapes = [(t, st, c) for t in (64, 128) for st in (2, 3, 4, 6, 8) for c in (1, 2, 3, 4)]
+        if args.probe_config:
+            shapes = [tuple(int(x) for x in args.probe_config.split(","))]
+        for tile_keys, stages, ctas in shapes:
+            slabs = (w.head_size + 63) // 64
+            smem = stages * slabs * tile_keys * 128 + 8 * stages + 4 * (w.num_seqs + 1) + 1024
+            if smem > 226 * 1024 or ctas * (smem + 1024) > 228 * 1024:
+                continue
+
+            def go():
+                B.pa_latent_gather_probe(p, d.key_cache, d.past, d.block_table, tile_keys,
+                                         stages, ctas, err)
+            for _ in range(3):
+                flush.zero_()
+                go()
+            torch.cuda.synchronize(device)
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                   for _ in range(steps)]
+            for e0, e1 in evs:
+                flush.zero_()
+                e0.record()
+                go()
+                e1.record()
+            torch.cuda.synchronize(device)
+            ms = statistics.median(a.elapsed_time(b) for a, b in evs)
+            if int(err.item()) != 0:
+                raise RuntimeError(f"probe {name}: device error flags {int(err.item()):#x}")
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            sweep.append({"tile_keys": tile_keys, "stages": stages, "ctas_per_sm": ctas,
+                          "us": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+                          "frac_of_copy": round(gbs / hbm, 3)})
+        best = max(sweep, key=lambda r: r["gbs"])
+        print(json.dumps({"probe": "paged gather (TMA boxes through the block table, no "
+                                   "arithmetic)", "workload": name, "visible_row_bytes": nbytes,
+                          "copy_peak_gbs": hbm, "peak_source": peaks[3], "steps": steps,
+                          "l2": "flushed before every run", "best": best, "sweep": sweep}),
+              flush=True)
+    return 0
+
+
 def load_peaks():
     """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     try:
@@ -612,6 +716,11 @@ def main(argv=None):
                     help="force the portable CUDA-core attention kernels")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--probe", action="store_true",
+                    help="instead of the operator: sweep the paged streaming probe "
+                         "(pa_latent_gather_probe) over the decode workloads' caches")
+    ap.add_argument("--probe-config", default="",
+                    help="with --probe: one TILE_KEYS,STAGES,CTAS_PER_SM shape instead of the sweep")
     args = ap.parse_args(argv)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -632,6 +741,8 @@ def main(argv=None):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(2 * max(l2, 64 << 20), dtype=torch.uint8, device=device)
     peaks = load_peaks()
+    if args.probe:
+        return run_probe(args, device, flush, peaks)
     res = measure_workload(args, args.workload, rank, world, device, args.steps, args.warmup,
                            flush)
     extras = [] if args.extras in ("", "none") else \
@@ -697,26 +808,12 @@ def run_reference(args, rank, world):
     through the batch) after its write phase."""
     if rank != 0:
         return 0
-    w = build_workload(args.workload, 0)
-    from oracle import pa_oracle as O
     from paged_latent_attention_cache_gb300 import workloads as W
-    p = W.oracle_params(w)
-    dt, hs = p["dtype"], w.head_size
-    cache = O.BitsCache(W.to_bits(w.key_cache).reshape(-1, hs), dt)
-    cos_t = O.bits_to_f64(W.to_bits(w.cos_cache), dt)
-    sin_t = O.bits_to_f64(W.to_bits(w.sin_cache), dt)
-    kb, qb = W.to_bits(w.key), W.to_bits(w.query)
-    cumseq, past, bt = w.cumseq.numpy(), w.past.numpy(), w.block_table.numpy()
-    O.latent_write(lambda t: O.bits_to_f64(kb[t], dt), cos_t, sin_t, w.slot_mapping.numpy(),
-                   cumseq, past, cache, p)
+    w = build_workload(args.workload, 0)
+    one = oracle_session(w)
     T = w.num_tokens
     # keep the whole run within a few minutes
     per_step_budget = max(0.02, 120.0 / max(1, args.steps + args.warmup))
-
-    def one(t):
-        out = O.latent_attend_token(t, O.bits_to_f64(qb[t], dt), cache, cos_t, sin_t, cumseq,
-                                    past, bt, p)
-        O.round_f64_to_bits(out, dt)
 
     for i in range(max(args.warmup, 3)):
         one(i % T)

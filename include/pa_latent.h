@@ -283,6 +283,33 @@ const char* pa_latent_status_string(pa_status s);
  * (empty string if none). */
 const char* pa_latent_last_error(void);
 
+/*
+ * Paged streaming probe: a measurement aid, not part of the operator. It
+ * reads every visible cache row of a decode batch (positions 0..past[b] of
+ * sequence b, addressed through block_table exactly as the read phase
+ * addresses them) with the tensor-core kernels' TMA boxes (64 channels x
+ * min(block_size, tile_keys) rows) into a ring of `stages` shared-memory
+ * stages of tile_keys rows, on num_SMs x ctas_per_sm CTAs, and does nothing
+ * with the data. The caller times it (CUDA events on `stream`); the
+ * visible rows x head_size x 2 bytes over that time is the ceiling of paged
+ * TMA streaming that the decode kernels run against.
+ *   p            geometry (dtype, head_size, block_size, num_blocks,
+ *                max_blocks_per_seq are used; 16-bit caches only)
+ *   key_cache    device, [num_blocks, block_size, 1, head_size], read only
+ *   past         device int32 [num_seqs] (context of sequence b: past[b] + 1)
+ *   block_table  device int32 [num_seqs, max_blocks_per_seq]
+ *   num_seqs     1..4096; tile_keys 32, 64 or 128; stages 1..8;
+ *   ctas_per_sm  1..4 (stages x tile must fit in 226 KB of shared memory)
+ *   err_flags    device int32: PA_DEVERR_BLOCK / PA_DEVERR_CONTEXT as the
+ *                read phase reports them
+ * Returns PA_OK, PA_ERR_INVALID_ARGUMENT, PA_ERR_NOT_IMPLEMENTED (FP8 cache)
+ * or PA_ERR_CUDA; enqueues one kernel and allocates nothing.
+ */
+pa_status pa_latent_gather_probe(const pa_latent_params* p, const void* key_cache,
+                                 const int32_t* past, const int32_t* block_table,
+                                 int32_t num_seqs, int32_t tile_keys, int32_t stages,
+                                 int32_t ctas_per_sm, int32_t* err_flags, void* stream);
+
 /* ======================================================================
  * SEPARATE layout — the op's other dense mode (kv_cache_layout="SEPARATE"):
  * grouped-query attention over separate key and value caches, with an

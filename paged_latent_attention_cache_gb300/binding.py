@@ -45,7 +45,7 @@ PA_FLAG_AFTER_WRITE = 0x2
 PA_FLAG_OWN_SLOTS = 0x4
 
 EXPORTED = ("pa_latent_validate", "pa_latent_write", "pa_latent_decode", "pa_latent_prefill",
-            "pa_latent_mixed",
+            "pa_latent_mixed", "pa_latent_gather_probe",
             "pa_latent_decode_noalloc", "pa_latent_workspace_size", "pa_latent_kernel_family",
             "pa_latent_status_string", "pa_latent_last_error", "pa_separate_validate",
             "pa_separate_write", "pa_separate_decode", "pa_separate_prefill",
@@ -124,6 +124,8 @@ def _load() -> ctypes.CDLL:
     lib.pa_latent_decode_noalloc.argtypes = [P, vp, i64, vp, vp, vp, vp, vp, vp, i32, i32, i32,
                                              vp, vp, vp]
     lib.pa_latent_decode_noalloc.restype = ctypes.c_int
+    lib.pa_latent_gather_probe.argtypes = [P, vp, vp, vp, i32, i32, i32, i32, vp, vp]
+    lib.pa_latent_gather_probe.restype = ctypes.c_int
     lib.pa_latent_workspace_size.argtypes = [P, i32, i64]
     lib.pa_latent_workspace_size.restype = sz
     lib.pa_latent_kernel_family.argtypes = [P, i32]
@@ -214,6 +216,16 @@ def pa_latent_write(p: pa_latent_params, key, cos_cache, sin_cache, slot_mapping
     _check(lib.pa_latent_write(ctypes.byref(p), _ptr(key), int(T), _ptr(cos_cache),
                                _ptr(sin_cache), _ptr(slot_mapping), _ptr(cumseq), _ptr(past),
                                int(B), _ptr(key_cache), _ptr(err_flags), _stream(stream)))
+
+
+def pa_latent_gather_probe(p: pa_latent_params, key_cache, past, block_table, tile_keys: int,
+                           stages: int, ctas_per_sm: int, err_flags, stream=None, num_seqs=None):
+    """The paged streaming probe (measurement aid): reads every visible
+    cache row of the batch through the block table, computes nothing."""
+    B = past.shape[0] if num_seqs is None else num_seqs
+    _check(lib.pa_latent_gather_probe(ctypes.byref(p), _ptr(key_cache), _ptr(past),
+                                      _ptr(block_table), int(B), int(tile_keys), int(stages),
+                                      int(ctas_per_sm), _ptr(err_flags), _stream(stream)))
 
 
 def _read(fn, p, query, key_cache, cos_cache, sin_cache, cumseq, past, block_table, out,

@@ -458,6 +458,35 @@ pa_status pa_latent_mixed(const pa_latent_params* p, const void* query, int64_t 
                     err_flags, stream);
 }
 
+pa_status pa_latent_gather_probe(const pa_latent_params* p, const void* key_cache,
+                                 const int32_t* past, const int32_t* block_table,
+                                 int32_t num_seqs, int32_t tile_keys, int32_t stages,
+                                 int32_t ctas_per_sm, int32_t* err_flags, void* stream) {
+  Geometry g;
+  pa_status s = resolve(p, &g);
+  if (s != PA_OK) return s;
+  if (g.fp8) return fail(PA_ERR_NOT_IMPLEMENTED, "the gather probe reads 16-bit caches only");
+  if (num_seqs < 1 || num_seqs > 4096)
+    return fail(PA_ERR_INVALID_ARGUMENT, "num_seqs must be in 1..4096");
+  if (tile_keys != 32 && tile_keys != 64 && tile_keys != 128)
+    return fail(PA_ERR_INVALID_ARGUMENT, "tile_keys must be 32, 64 or 128");
+  if (stages < 1 || stages > 8) return fail(PA_ERR_INVALID_ARGUMENT, "stages must be in 1..8");
+  if (ctas_per_sm < 1 || ctas_per_sm > 4)
+    return fail(PA_ERR_INVALID_ARGUMENT, "ctas_per_sm must be in 1..4");
+  if (gather_probe_smem(g, tile_keys, stages, num_seqs) > kMaxProbeSmem)
+    return fail(PA_ERR_INVALID_ARGUMENT, "stages x tile exceed the probe's shared memory");
+  if (!key_cache || !past || !block_table || !err_flags)
+    return fail(PA_ERR_INVALID_ARGUMENT, "a required pointer is NULL");
+  if (!aligned(key_cache, 16))
+    return fail(PA_ERR_INVALID_ARGUMENT, "key_cache must be 16-byte aligned");
+  if (!aligned(past, 4) || !aligned(block_table, 4) || !aligned(err_flags, 4))
+    return fail(PA_ERR_INVALID_ARGUMENT, "int32 tensors must be 4-byte aligned");
+  return cuda_status(launch_gather_probe(g, key_cache, past, block_table, num_seqs, tile_keys,
+                                         stages, ctas_per_sm, err_flags,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+                     "gather probe launch");
+}
+
 size_t pa_latent_workspace_size(const pa_latent_params* p, int32_t num_seqs,
                                 int64_t num_tokens) {
   Geometry g;

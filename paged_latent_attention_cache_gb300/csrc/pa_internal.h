@@ -36,6 +36,14 @@ struct Geometry {
   int device;       // current device ordinal
 };
 
+// Paged streaming probe (pa_probe.cu): shared memory per CTA, and the launch.
+extern const size_t kMaxProbeSmem;
+size_t gather_probe_smem(const Geometry& g, int tile_keys, int stages, int num_seqs);
+cudaError_t launch_gather_probe(const Geometry& g, const void* key_cache, const int32_t* past,
+                                const int32_t* block_table, int num_seqs, int tile_keys,
+                                int stages, int ctas_per_sm, int32_t* err_flags,
+                                cudaStream_t stream);
+
 // kMixed: one launch over a batch whose first sequences are decodes (one
 // new token each) and the rest prefills.
 enum class Phase { kDecode = 0, kPrefill = 1, kMixed = 2 };

@@ -184,6 +184,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if (P.mixed ? unit < P.units : P.decode != 0) {
       // the query region is free until the query load that follows the plan
       w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), q_bytes / 4);
+      fence_proxy_async();  // the scratch is overwritten by the query TMA later
       if (w.status == 0) {
         const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
         if (lane == 0 && w.split == 0) P.ws_plan[w.b - P.seq_begin] = make_int2(w.first, w.splits);

@@ -181,6 +181,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     if (P.decode) {
       // the query region is free until the query load after the plan
       w = decode_plan_warp<N>(P, unit, reinterpret_cast<int*>(q_s), C::kQBytes / 4);
+      fence_proxy_async();  // the scratch is overwritten by the query TMA later
       if (w.status == 0) {
         const int32_t q0 = P.cumseq[w.b], q1 = P.cumseq[w.b + 1];
         if (lane == 0 && w.split == 0 && g == 0)
@@ -778,9 +779,10 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // swizzled fp16 slabs (16-byte chunk c of row r at c ^ (r & 7)), once
       // the fp16 stage is free (PV of the tile that used it before is done).
       const int ct = tid - 320;  // 0..63
+      constexpr int kS8 = C::kStages8 > 0 ? C::kStages8 : 1;  // (non-FP8 builds never run this)
       for (int k = 0; k < n; ++k) {
-        const int s8 = k % C::kStages8, s16 = k % STAGES;
-        bool okc = wait_bar(smem_u32(&bars->full8[s8]), (k / C::kStages8) & 1, abort,
+        const int s8 = k % kS8, s16 = k % STAGES;
+        bool okc = wait_bar(smem_u32(&bars->full8[s8]), (k / kS8) & 1, abort,
                             P.err_flags);
         if (okc && k >= STAGES)
           okc = wait_bar(smem_u32(&bars->empty[s16]), ((k / STAGES) & 1) ^ 1, abort,

@@ -176,6 +176,31 @@ def test_write_host_rejections(B):
     assert B.lib.pa_latent_write(ctypes.byref(p), *bad) == B.PA_ERR_INVALID_ARGUMENT
 
 
+def test_gather_probe_host_rejections(B):
+    """The paged streaming probe checks its sweep parameters, pointers and
+    shared-memory budget on the host (no call here reaches a launch)."""
+    p = _good(B)
+    vp = ctypes.c_void_p
+    good = [vp(0x10000), vp(0x20000), vp(0x30000), 2, 64, 4, 1, vp(0x40000), None]
+
+    def call(params=p, **over):
+        a = list(good)
+        for i, v in over.items():
+            a[int(i[1:])] = v
+        return B.lib.pa_latent_gather_probe(ctypes.byref(params), *a)
+    for over, needle in [(dict(a4=48), "tile_keys"), (dict(a5=0), "stages"),
+                         (dict(a5=9), "stages"), (dict(a6=5), "ctas_per_sm"),
+                         (dict(a3=0), "num_seqs"), (dict(a3=5000), "num_seqs"),
+                         (dict(a0=None), "NULL"), (dict(a7=None), "NULL"),
+                         (dict(a0=vp(0x10008)), "aligned"), (dict(a1=vp(0x20002)), "aligned")]:
+        assert call(**over) == B.PA_ERR_INVALID_ARGUMENT, (over, B.last_error())
+        assert needle in B.last_error(), (over, B.last_error())
+    big = _good(B, head_size=576, v_head_size=512, rotary_offset=512)
+    assert call(params=big, a4=128, a5=8) == B.PA_ERR_INVALID_ARGUMENT
+    assert "shared memory" in B.last_error()
+    assert call(params=_good(B, cache_dtype="e4m3", k_scale=0.02)) == B.PA_ERR_NOT_IMPLEMENTED
+
+
 def test_status_strings(B):
     for s, name in [(0, "PA_OK"), (1, "PA_ERR_INVALID_ARGUMENT"), (2, "PA_ERR_NOT_IMPLEMENTED"),
                     (3, "PA_ERR_CUDA"), (4, "PA_ERR_WORKSPACE")]:

@@ -481,3 +481,28 @@ def test_flag_context_beyond_block_table():
     def m(w):
         w.past[1] = w.max_blocks_per_seq * w.block_size   # cos_rows too small as well
     w, got = _flag_case(m, B.PA_DEVERR_CONTEXT | B.PA_DEVERR_POSITION)
+
+
+def test_gather_probe_reads_the_batch():
+    """The paged streaming probe (a measurement aid that reads every visible
+    cache row through the block table with the decode kernels' TMA boxes)
+    runs over ragged contexts, block sizes 16 and 64 and every sweep shape
+    without a device error, and reports a block-table entry outside the
+    pool as the read phase does."""
+    from paged_latent_attention_cache_gb300.api import PagedLatentAttention
+    for bs in (16, 64):
+        w = W.make_workload("probe", q_lens=[1] * 5, past_lens=[0, 63, 64, 200, 1000],
+                            num_heads=4, **W.GLM, block_size=bs, seed=40, scale=0.07)
+        d = w.to("cuda")
+        p = PagedLatentAttention.from_workload(w, device="cuda").params
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for tile_keys, stages, ctas in [(64, 2, 1), (128, 4, 1), (64, 4, 2), (32, 3, 4)]:
+            B.pa_latent_gather_probe(p, d.key_cache, d.past, d.block_table, tile_keys, stages,
+                                     ctas, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        bt = d.block_table.clone()
+        bt[4, 2] = w.key_cache.shape[0] + 5
+        B.pa_latent_gather_probe(p, d.key_cache, d.past, bt, 64, 2, 1, err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == B.PA_DEVERR_BLOCK
