@@ -26,6 +26,14 @@
 // Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
 // TMA producer, warp 5 TMEM allocation + the MMA-issuing thread, warps 6-9
 // score exchange. Key tiles of 64 keys, 3 stages; every wait is bounded.
+//
+// Work units: decode runs one pair per unit of the device plan (a sequence's
+// key split). Prefill is persistent: at most one wave of pairs, each looping
+// over tokens T-1-p, T-1-p-npairs, ... (the longest first). Every role
+// resolves the units itself and counts key tiles across them, so the key
+// ring, the S/P buffers and the exchange carry on from one token to the next;
+// a token's query is loaded once QK^T of the previous token's last tile has
+// completed, and its first PV starts the O accumulator afresh.
 #include "pa_tc_cluster.cuh"
 
 namespace pa {
@@ -92,6 +100,57 @@ __device__ __noinline__ void pair_q_row_to_f16(uint8_t* q_s, int row, int q_full
   if (big) raise_flag(P.err_flags, PA_DEVERR_RANGE);
 }
 
+// Work of prefill unit u: token T - 1 - u (the tokens with the most keys,
+// the last of each sequence, come first), with its key-tile range. status
+// 0: attend; 1: no work here (a token outside [seq_begin, seq_end), or one
+// that cannot be located); 2: an invalid context or position (reported,
+// output rows to be zeroed). Errors are raised into `flags` when non-null.
+template <int N>
+__device__ Work pair_prefill_work(const Params& P, int64_t u, int32_t* flags) {
+  Work w;
+  w.status = 1;
+  w.splits = 1;
+  int32_t b;
+  int64_t pos;
+  const int64_t tok = P.num_tokens - 1 - u;
+  if (locate_token(tok, P.cumseq, P.past, P.num_seqs, flags, &b, &pos) && b >= P.seq_begin &&
+      b < P.seq_end) {
+    w.status = 0;
+    w.b = b;
+    w.t = tok;
+    w.pos = pos;
+    w.past = P.past[b];
+    const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+    w.t_begin = lo_key / N;
+    w.t_end = pos / N + 1;
+    const bool bad_ctx = w.past < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
+    const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
+    if (bad_ctx || bad_pos) {
+      raise_flag(flags, bad_ctx ? PA_DEVERR_CONTEXT : PA_DEVERR_POSITION);
+      w.status = 2;
+    }
+  }
+  return w;
+}
+
+// The i-th work unit of a CTA pair. Decode: the one unit of the device plan
+// (`first`, i == 0). Prefill: the grid is at most one wave of pairs, and
+// pair p takes units p, p + npairs, p + 2 npairs, ... of the P.units tokens
+// (`first` is unit p, resolved in the prologue). False past the last unit.
+template <int N>
+__device__ __forceinline__ bool pair_unit(const Params& P, const Work& first, int i, int pair,
+                                          int npairs, int32_t* flags, Work* w) {
+  if (i == 0) {
+    *w = first;
+    return P.decode || pair < P.units;
+  }
+  if (P.decode) return false;
+  const int64_t u = pair + (int64_t)i * npairs;
+  if (u >= P.units) return false;
+  *w = pair_prefill_work<N>(P, u, flags);
+  return true;
+}
+
 template <int N, int STAGES, bool FP8 = false>
 struct PairCfg {
   // warps 0-3, 4, 5, 6-9 (see above); FP8: converter warps 10-11
@@ -133,7 +192,7 @@ struct PairBarriers {
   uint64_t x_out[1];  // the peer has read the rows this CTA sent into its x_s
   uint64_t drain;
   uint32_t tmem_base;
-  int bad;
+  int bad_mask;  // bit (a & 31): attended unit a read a block id outside the pool
   int abort;
   int xfail;  // an exchange warp's wait failed: all four leave after the tile's barrier
 };
@@ -199,27 +258,17 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
       }
     } else {
-      int32_t b;
-      int64_t pos;
-      w.status = 1;
-      w.splits = 1;
-      // CTA `unit` takes token T - 1 - unit: the tokens with the most keys
-      // (the last of each sequence) start first, short ones fill in behind
-      const int64_t tok = P.num_tokens - 1 - unit;
-      if (locate_token(tok, P.cumseq, P.past, P.num_seqs,
-                       (lane == 0 && g == 0) ? P.err_flags : nullptr, &b, &pos) &&
-          b >= P.seq_begin && b < P.seq_end) {
-        w.status = 0;
-        w.b = b;
-        w.t = tok;
-        w.pos = pos;
-        w.past = P.past[b];
-        const int64_t lo_key = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-        w.t_begin = lo_key / N;
-        w.t_end = pos / N + 1;
+      // this pair's first unit (later ones are resolved as the roles reach them)
+      w = pair_prefill_work<N>(P, unit, (lane == 0 && g == 0) ? P.err_flags : nullptr);
+      if (w.status == 2) {  // invalid context or position: the token's output rows are zero
+        T* out_row = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs;
+        for (int i = lane; i < P.H * VG; i += 32) {
+          const int h = i / VG, c = i % VG;
+          out_row[(int64_t)h * vhs + g * VG + c] = Half<T>::from_f32(0.f);
+        }
       }
     }
-    if (w.status == 0) {
+    if (P.decode && w.status == 0) {
       const bool bad_ctx = w.past < 0 || w.pos >= (int64_t)P.max_blocks * P.bs;
       const bool bad_pos = P.rd > 0 && w.pos >= P.cos_rows;
       if (bad_ctx || bad_pos) {
@@ -260,7 +309,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
     // armed for tile 0
     mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
     mbar_init(smem_u32(&bars->drain), 1);
-    bars->bad = 0;
+    bars->bad_mask = 0;
     bars->abort = 0;
     bars->xfail = 0;
     fence_barrier_init();
@@ -281,14 +330,14 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   volatile int* abort = &bars->abort;
   const Work W = work;
 
-  if (W.status == 0) {
-    const int64_t t = W.t, pos = W.pos, t_begin = W.t_begin;
-    const int32_t b = W.b;
-    const int splits = W.splits;
-    const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
-    const int n = (int)max((int64_t)0, W.t_end - t_begin);
-    const int64_t part = (int64_t)unit * G + g;
-    T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
+  {
+    // Every role walks the pair's units (pair_unit) on its own and counts key
+    // tiles globally across them, so the ring stages, S/P buffers, exchange
+    // buffer and their barrier phases simply continue from one unit to the
+    // next; the query region, q_tma and q_full turn over once per attended
+    // unit (a: the number of units attended so far).
+    const int npairs = (int)(gridDim.x / G);
+    const int pair = unit;
     const int slab0 = 4 * (int)g;  // global slab of local key slab 0
     // Query layout in shared memory: CTA 0 holds full slabs 0-3 (SW128) then
     // channels 256-287 as a 64-byte-swizzled half slab; CTA 1 holds channels
@@ -302,19 +351,39 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const int row = tid;
       const bool live = warp * 32 < P.H;
       const uint32_t lane_addr = tmem + ((uint32_t)(warp * 32) << 16);
-      float m_used = -INFINITY, l = 0.f;
+      int32_t* rflags = (tid == 0 && g == 0) ? P.err_flags : nullptr;  // (units after the first)
       bool ok = true;
-      // Pass k = -1 runs the tile code once with every wait, arrive, shared
-      // memory write and state update switched off, on whatever TMEM holds:
-      // it brings the loop's instructions into the instruction cache while
-      // the query and the first key tile are still in flight. (The opaque
-      // start keeps the compiler from peeling it into a copy of its own.)
-      int k_first = -1;
-      asm volatile("" : "+r"(k_first));
-      for (int k = k_first; k < n && ok; ++k) {
-        const bool dry = k < 0;
-        if (k == 0) {  // every work item has n >= 1 tiles
-          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), 0, abort, P.err_flags));
+      int kbase = 0;  // global index of the unit's first key tile
+      int au = 0;     // units attended so far
+      for (int iu = 0; ok; ++iu) {
+        Work w;
+        if (!pair_unit<N>(P, W, iu, pair, npairs, iu == 0 ? nullptr : rflags, &w)) break;
+        if (w.status == 2 && iu > 0 && row < P.H) {  // invalid context or position: zero rows
+          T* zrow = reinterpret_cast<T*>(P.out) + w.t * (int64_t)P.H * vhs + (int64_t)row * vhs +
+                    g * VG;
+          for (int c = 0; c < VG; ++c) zrow[c] = Half<T>::from_f32(0.f);
+        }
+        if (w.status != 0) continue;
+        const int64_t t = w.t, pos = w.pos, t_begin = w.t_begin;
+        const int splits = w.splits;
+        const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        const int n = (int)max((int64_t)0, w.t_end - t_begin);
+        const int64_t part = (int64_t)pair * G + g;
+        T* out_row = reinterpret_cast<T*>(P.out) + t * (int64_t)P.H * vhs;
+        float m_used = -INFINITY, l = 0.f;
+        // Pass kk = -1 (first attended unit only) runs the tile code once with
+        // every wait, arrive, shared memory write and state update switched
+        // off, on whatever TMEM holds: it brings the loop's instructions into
+        // the instruction cache while the query and the first key tile are
+        // still in flight. (The opaque start keeps the compiler from peeling
+        // it into a copy of its own.)
+        int k_first = au == 0 ? -1 : 0;
+        asm volatile("" : "+r"(k_first));
+        for (int kk = k_first; kk < n && ok; ++kk) {
+        const bool dry = kk < 0;
+        const int k = dry ? -1 : kbase + kk;  // global tile index (stages, buffers, phases)
+        if (kk == 0) {  // every attended unit has n >= 1 tiles: its query
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->q_tma), au & 1, abort, P.err_flags));
           // RoPE in place on this CTA's slabs (the pair kernel only runs when
           // the rotary channels and their partners lie inside one CTA's slabs).
           if (FP8 && !std::is_same<T, __half>::value) {
@@ -362,7 +431,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         }
         const int sb = dry ? 0 : k % NS;   // S buffer
         const int pb = dry ? 1 : k & 1;    // P buffer
-        const int64_t j0 = (t_begin + k) * N;
+        const int64_t j0 = (t_begin + kk) * N;
         const bool edge = !dry && (j0 < lo || j0 + N - 1 > pos);
         if (!dry) {
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_sum[sb]), (k / NS) & 1, abort,
@@ -402,7 +471,7 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           if (rewrite) tmem_wait_st();
           mt *= sl;
           if (dry) {
-          } else if (k == 0) {
+          } else if (kk == 0) {
             m_used = mt;
           } else if (mt > m_used + kRescaleLog2) {
             factor = ex2(m_used - mt);
@@ -472,16 +541,16 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         mbar_arrive(smem_u32(&bars->p_full[pb]));
       }
 
-      // ---- epilogue ----
-      grid_dep_launch();
-      named_sync(2, 160);
-      ok = __all_sync(0xffffffffu, ok && !*abort);
-      if (ok)
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[(n - 1) & 1]),
-                                              ((n - 1) >> 1) & 1, abort, P.err_flags));
-      if (ok && live) {
+        // ---- epilogue of the unit ----
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, *abort == 0);
+        const int kl = kbase + n - 1;  // the unit's last tile
+        if (ok)
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[kl & 1]), (kl >> 1) & 1,
+                                                abort, P.err_flags));
+        if (ok && live) {
         tc_fence_after();
-        const bool bad = bars->bad != 0;
+        const bool bad = ((*reinterpret_cast<volatile int*>(&bars->bad_mask) >> (au & 31)) & 1) != 0;
         if (splits == 1) {
           const float inv = (l > 0.f && !bad) ? P.out_scale / l : 0.f;
 #pragma unroll 1
@@ -522,7 +591,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             P.ws_ml[(part * kRows + row) * 2 + 1] = bad ? 0.f : l;
           }
         }
+        }
+        kbase += n;
+        ++au;
       }
+      grid_dep_launch();
+      named_sync(2, 160);
     } else if (warp >= 6 && warp < 10) {  // (FP8: warps 10-11 convert, below)
       // =================== partial-score exchange ===================
       // Warp w handles TMEM lanes 32*(w%4)..+31 (the quadrant its SM
@@ -542,7 +616,13 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       const uint32_t x_out_peer = map_peer(smem_u32(&bars->x_out[0]), peer);
       volatile int* xfail = &bars->xfail;
       bool ok = true;
-      for (int k = 0; k < n; ++k) {
+      int k = 0;  // global tile index
+      for (int iu = 0; ok && *xfail == 0; ++iu) {
+        Work w;
+        if (!pair_unit<N>(P, W, iu, pair, npairs, nullptr, &w)) break;
+        if (w.status != 0) continue;
+        const int n = (int)max((int64_t)0, w.t_end - w.t_begin);
+        for (int kk = 0; kk < n; ++kk, ++k) {
         const int sb = k % NS;
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->s_part[sb]), (k / NS) & 1, abort,
                                               P.err_flags));
@@ -590,7 +670,8 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         named_sync(3, 128);
         if (*xfail != 0) break;
         if (xt == 0) {
-          if (k + 1 < n) mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
+          // armed for the next tile (after the last one it is never used)
+          mbar_expect_tx(smem_u32(&bars->x_in[0]), kXTile);
           arrive_peer_relaxed(x_out_peer);
         }
 #pragma unroll
@@ -599,81 +680,111 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         tmem_wait_st();
         tc_fence_before();
         mbar_arrive(smem_u32(&bars->s_sum[sb]));
+        }
       }
     } else if (warp == 4) {
       // =================== TMA producer ===================
-      if (lane == 0) {  // this CTA's five query slabs (QR = 128 rows: the token's heads)
-        const uint32_t qb = smem_u32(&bars->q_tma);
-        mbar_expect_tx(qb, C::kQBytes);
-        for (int j = 0; j < 4; ++j)
-          tma_load_2d(smem_u32(q_s) + q_full_off + j * C::kQBox, &qmap, (q_full0 + j) * 64,
-                      (int)(t * P.H), qb);
-        tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
-      }
       // With P.early the write grid may still run: cache rows are read only
-      // after griddepcontrol.wait, except (P.own_slots) the tiles below the
-      // sequence's first new position, which the write does not touch.
-      int dirty_from = 0;
-      if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, W.past / N - t_begin);
+      // after griddepcontrol.wait, except (P.own_slots) the first unit's tiles
+      // below its sequence's first new position, which the write does not touch.
       bool waited = !P.early;
       const int nsub = N / P.box_rows;
-      BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
-                   P.box_rows, P.bs, n * nsub};
-      ids.start(lane);
       // the ring the copies land in: key stages, or (FP8) the E4M3 stages
       constexpr int PST = FP8 ? C::kStages8 : STAGES;
       uint64_t* pfull = FP8 ? bars->full8 : bars->full;
       uint64_t* pempty = FP8 ? bars->empty8 : bars->empty;
-      int issued = 0;
-      for (int k = 0; k < n; ++k) {
-        const int stage = k % PST;
-        if (!waited && k >= dirty_from) {
-          grid_dep_wait();  // the write phase's cache rows are complete and visible
-          waited = true;
-        }
-        if (k >= PST) {
+      int k = 0;        // global tile index
+      int au = 0;       // units attended so far (query loads issued)
+      int last_k = -1;  // the previous attended unit's last tile
+      bool okp = true;
+      for (int iu = 0; okp; ++iu) {
+        Work w;
+        if (!pair_unit<N>(P, W, iu, pair, npairs, nullptr, &w)) break;
+        if (w.status != 0) continue;
+        const int64_t t = w.t, pos = w.pos, t_begin = w.t_begin;
+        const int32_t b = w.b;
+        const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
+        const int n = (int)max((int64_t)0, w.t_end - t_begin);
+        // the query region is free once QK^T of the previous unit's last tile
+        // has completed
+        if (last_k >= 0) {
           bool okw = true;
           if (lane == 0)
-            okw = wait_bar(smem_u32(&pempty[stage]), ((k / PST) & 1) ^ 1, abort, P.err_flags);
+            okw = wait_bar(smem_u32(&bars->s_part[last_k % NS]), (last_k / NS) & 1, abort,
+                           P.err_flags);
           if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
-        int y = (int)P.num_slots;  // out of range: TMA fills zeros
-        const int phys = ids.get(k * nsub, lane & (nsub - 1), lane);
-        if (lane < nsub && ids.visible(k * nsub + lane)) {
-          if (phys >= 0 && phys < P.num_blocks) {
-            const int64_t key0 = (t_begin + k) * N + (int64_t)lane * P.box_rows;
-            y = (int)((int64_t)phys * P.bs + key0 % P.bs);
-          } else {
-            bars->bad = 1;
-            raise_flag(P.err_flags, PA_DEVERR_BLOCK);
-          }
+        if (lane == 0) {  // this CTA's five query slabs (QR = 128 rows: the token's heads)
+          atomicAnd(&bars->bad_mask, ~(1 << (au & 31)));
+          const uint32_t qb = smem_u32(&bars->q_tma);
+          mbar_expect_tx(qb, C::kQBytes);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(smem_u32(q_s) + q_full_off + j * C::kQBox, &qmap, (q_full0 + j) * 64,
+                        (int)(t * P.H), qb);
+          tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
         }
-        if (lane == 0)
-          mbar_expect_tx(smem_u32(&pfull[stage]), FP8 ? C::kStage8Bytes : C::kStageBytes);
-        __syncwarp();
-        if (lane < nsub) {
-          const uint32_t full = smem_u32(&pfull[stage]);
-          if (FP8) {
-            // this CTA's 320 E4M3 channels of box_rows rows: 256 into the
-            // stage's first part (256-byte rows), 64 into its second part
-            const uint32_t d8 = smem_u32(k8_s + stage * C::kStage8Bytes);
-            tma_load_2d(d8 + lane * P.box_rows * 256, &kmap, slab0 * 64, y, full);
-            tma_load_2d(d8 + N * 256 + lane * P.box_rows * 64, &kmap8b, slab0 * 64 + 256, y, full);
-          } else {
-            const uint32_t dst0 = smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
+        int dirty_from = 0;
+        if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, w.past / N - t_begin);
+        BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
+                     P.box_rows, P.bs, n * nsub};
+        ids.start(lane);
+        for (int kk = 0; kk < n; ++kk, ++k) {
+          const int stage = k % PST;
+          if (!waited && kk >= dirty_from) {
+            grid_dep_wait();  // the write phase's cache rows are complete and visible
+            waited = true;
+          }
+          if (k >= PST) {
+            bool okw = true;
+            if (lane == 0)
+              okw = wait_bar(smem_u32(&pempty[stage]), ((k / PST) & 1) ^ 1, abort, P.err_flags);
+            if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
+              okp = false;
+              break;
+            }
+          }
+          int y = (int)P.num_slots;  // out of range: TMA fills zeros
+          const int phys = ids.get(kk * nsub, lane & (nsub - 1), lane);
+          if (lane < nsub && ids.visible(kk * nsub + lane)) {
+            if (phys >= 0 && phys < P.num_blocks) {
+              const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
+              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
+            } else {
+              atomicOr(&bars->bad_mask, 1 << (au & 31));
+              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+            }
+          }
+          if (lane == 0)
+            mbar_expect_tx(smem_u32(&pfull[stage]), FP8 ? C::kStage8Bytes : C::kStageBytes);
+          __syncwarp();
+          if (lane < nsub) {
+            const uint32_t full = smem_u32(&pfull[stage]);
+            if (FP8) {
+              // this CTA's 320 E4M3 channels of box_rows rows: 256 into the
+              // stage's first part (256-byte rows), 64 into its second part
+              const uint32_t d8 = smem_u32(k8_s + stage * C::kStage8Bytes);
+              tma_load_2d(d8 + lane * P.box_rows * 256, &kmap, slab0 * 64, y, full);
+              tma_load_2d(d8 + N * 256 + lane * P.box_rows * 64, &kmap8b, slab0 * 64 + 256, y,
+                          full);
+            } else {
+              const uint32_t dst0 =
+                  smem_u32(k_s + stage * C::kStageBytes) + lane * P.box_rows * 128;
 #pragma unroll 1
-            for (int j = 0; j < C::kSlabs; ++j)
-              tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+              for (int j = 0; j < C::kSlabs; ++j)
+                tma_load_2d(dst0 + j * C::kKBox, &kmap, (slab0 + j) * 64, y, full);
+            }
           }
+          __syncwarp();
         }
-        issued = k + 1;
-        __syncwarp();
+        ++au;
+        last_k = k - 1;
       }
       if (!waited) grid_dep_wait();  // the grid completes after the write grid
       if (*abort && lane == 0) {
-        drain_wait(smem_u32(&bars->q_tma), 0, P.err_flags);
-        for (int st = 0; st < PST && st < issued; ++st) {
-          const int kl = issued - 1 - ((issued - 1 - st) % PST);
+        // copies still in flight land before the CTA leaves
+        if (au > 0) drain_wait(smem_u32(&bars->q_tma), (au - 1) & 1, P.err_flags);
+        for (int st = 0; st < PST && st < k; ++st) {
+          const int kl = k - 1 - ((k - 1 - st) % PST);
           drain_wait(smem_u32(&pfull[st]), (kl / PST) & 1, P.err_flags);
         }
       }
@@ -687,85 +798,107 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         constexpr uint32_t kIdPV = idesc_f16(kBf16, kRows, VG, true);
         const uint32_t q_base = smem_u32(q_s);
         const uint32_t k_base = smem_u32(k_s);
-        bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
-        if (ok) {
-          tc_fence_after();
-          int kq = 0, kp = 0;
-          const uint64_t t0 = globaltimer();
-          uint32_t spins = 0;
-          while (kp < n) {
-            bool progressed = false;
-            if (kp < kq) {
-              const int stage = kp % STAGES, pb = kp & 1;
-              if (mbar_test_wait(smem_u32(&bars->p_full[pb]), (kp >> 1) & 1)) {
-                tc_fence_after();
-                const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
-                // descriptor address field (bytes / 16) advances 2048 / 16 per 16 keys
-                const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
+        // Two cursors over the attended units: the one QK^T is in and the one
+        // PV is in (global first tile, tile count, attended index).
+        struct Cursor {
+          int iu, first, n, a;
+        };
+        auto advance = [&](Cursor& c) -> bool {
+          for (;;) {
+            Work w;
+            if (!pair_unit<N>(P, W, ++c.iu, pair, npairs, nullptr, &w)) return false;
+            if (w.status != 0) continue;
+            c.first += c.n;
+            c.n = (int)max((int64_t)0, w.t_end - w.t_begin);
+            ++c.a;
+            return true;
+          }
+        };
+        Cursor cq{-1, 0, 0, -1}, cp{-1, 0, 0, -1};
+        bool more_q = advance(cq), more_p = advance(cp);
+        bool ok = true;
+        int kq = 0, kp = 0;  // global tiles whose QK^T / PV have been issued
+        uint64_t t0 = globaltimer();
+        uint32_t spins = 0;
+        while (more_p) {
+          bool progressed = false;
+          if (kp < kq) {
+            const int stage = kp % STAGES, pb = kp & 1;
+            if (mbar_test_wait(smem_u32(&bars->p_full[pb]), (kp >> 1) & 1)) {
+              tc_fence_after();
+              const uint32_t vb = k_base + stage * C::kStageBytes;  // V = local slabs 0-3
+              // descriptor address field (bytes / 16) advances 2048 / 16 per 16 keys
+              const uint64_t b0 = sdesc(vb, C::kKBox, 1024);
+              const bool fresh = kp == cp.first;  // the unit's first tile: O starts over
 #pragma unroll
-                for (int kk = 0; kk < N / 16; ++kk)
-                  mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (N / 2) + kk * 8,
-                         b0 + (uint64_t)(kk * 128), kIdPV, (kp > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(smem_u32(&bars->pv_done[pb]));
-                tc_commit(smem_u32(&bars->empty[stage]));
-                ++kp;
-                progressed = true;
-              }
+              for (int kk = 0; kk < N / 16; ++kk)
+                mma_ts(tmem + C::kColO, tmem + C::kColP + pb * (N / 2) + kk * 8,
+                       b0 + (uint64_t)(kk * 128), kIdPV, (!fresh || kk > 0) ? 1u : 0u);
+              tc_commit(smem_u32(&bars->pv_done[pb]));
+              tc_commit(smem_u32(&bars->empty[stage]));
+              ++kp;
+              if (kp == cp.first + cp.n) more_p = advance(cp);
+              progressed = true;
             }
-            // QK^T(kq): needs its key tile and a free S buffer (s_free of kq-NS)
-            // (at most two tiles ahead of PV: a PV queued behind more QK^T
-            // in the in-order tensor pipe would hold its key stage longer)
-            if (kq < n && kq < kp + 2) {
-              const int stage = kq % STAGES, sb = kq % NS;
-              if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
-                  (kq < NS ||
-                   mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NS) / NS) & 1))) {
-                tc_fence_after();
-                const uint32_t kb = k_base + stage * C::kStageBytes;
-                // Descriptors built once; per step only the address field
-                // (bytes / 16) moves.
-                const uint64_t b0 = sdesc(kb, 16, 1024);
-                const uint64_t af0 = sdesc(q_base + q_full_off, 16, 1024);
-                const uint64_t ah0 = sdesc64(q_base + q_half_off);
+          }
+          // QK^T(kq): needs its key tile, a free S buffer (s_free of kq-NS)
+          // and, for a unit's first tile, the unit's rotated query (q_full)
+          // (at most two tiles ahead of PV: a PV queued behind more QK^T in
+          // the in-order tensor pipe would hold its key stage longer)
+          if (more_q && kq < kp + 2) {
+            const int stage = kq % STAGES, sb = kq % NS;
+            if ((kq != cq.first || mbar_test_wait(smem_u32(&bars->q_full), cq.a & 1)) &&
+                mbar_test_wait(smem_u32(&bars->full[stage]), (kq / STAGES) & 1) &&
+                (kq < NS ||
+                 mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NS) / NS) & 1))) {
+              tc_fence_after();
+              const uint32_t kb = k_base + stage * C::kStageBytes;
+              // Descriptors built once; per step only the address field
+              // (bytes / 16) moves.
+              const uint64_t b0 = sdesc(kb, 16, 1024);
+              const uint64_t af0 = sdesc(q_base + q_full_off, 16, 1024);
+              const uint64_t ah0 = sdesc64(q_base + q_half_off);
 #pragma unroll
-                for (int i = 0; i < C::kSteps; ++i) {
-                  // CTA g covers K steps [18g, 18g+18) = channels [288g, 288g+288):
-                  // the key operand is local slab e>>2, step e&3 (e = i + 2g); the
-                  // query operand is a full slab, or the 32-channel half slab.
-                  const int e = i + 2 * (int)g;
-                  const uint32_t kslab = (uint32_t)(e >> 2), w = (uint32_t)(e & 3) * 2;
-                  const bool half = g ? (i < 2) : (i >= 16);
-                  uint64_t a;
-                  if (half) {
-                    a = ah0 + (uint64_t)((g ? i : i - 16) * 2);
-                  } else {
-                    const uint32_t j = (uint32_t)(g ? (i - 2) >> 2 : i >> 2);
-                    const uint32_t wq = (uint32_t)(g ? (i - 2) & 3 : i & 3) * 2;
-                    a = af0 + (j * (C::kQBox >> 4) + wq);
-                  }
-                  mma_ss(tmem + C::kColS + sb * N, a, b0 + (kslab * (C::kKBox >> 4) + w), kIdQK,
-                         i > 0 ? 1u : 0u);
+              for (int i = 0; i < C::kSteps; ++i) {
+                // CTA g covers K steps [18g, 18g+18) = channels [288g, 288g+288):
+                // the key operand is local slab e>>2, step e&3 (e = i + 2g); the
+                // query operand is a full slab, or the 32-channel half slab.
+                const int e = i + 2 * (int)g;
+                const uint32_t kslab = (uint32_t)(e >> 2), w = (uint32_t)(e & 3) * 2;
+                const bool half = g ? (i < 2) : (i >= 16);
+                uint64_t a;
+                if (half) {
+                  a = ah0 + (uint64_t)((g ? i : i - 16) * 2);
+                } else {
+                  const uint32_t j = (uint32_t)(g ? (i - 2) >> 2 : i >> 2);
+                  const uint32_t wq = (uint32_t)(g ? (i - 2) & 3 : i & 3) * 2;
+                  a = af0 + (j * (C::kQBox >> 4) + wq);
                 }
-                tc_commit(smem_u32(&bars->s_part[sb]));
-                ++kq;
-                progressed = true;
+                mma_ss(tmem + C::kColS + sb * N, a, b0 + (kslab * (C::kKBox >> 4) + w), kIdQK,
+                       i > 0 ? 1u : 0u);
               }
+              tc_commit(smem_u32(&bars->s_part[sb]));
+              ++kq;
+              if (kq == cq.first + cq.n) more_q = advance(cq);
+              progressed = true;
             }
-            if (progressed) {
-              spins = 0;
-              continue;
-            }
-            if ((++spins & 15u) == 0) {
-              if (*abort) { ok = false; break; }
-              if (globaltimer() - t0 > kWaitLimitNs * 4) {
-                *abort = 1;
-                raise_flag(P.err_flags, PA_DEVERR_TIMEOUT);
-                ok = false;
-                break;
-              }
+          }
+          if (progressed) {
+            spins = 0;
+            t0 = globaltimer();
+            continue;
+          }
+          if ((++spins & 15u) == 0) {
+            if (*abort) { ok = false; break; }
+            if (globaltimer() - t0 > kWaitLimitNs * 4) {  // no progress for that long
+              *abort = 1;
+              raise_flag(P.err_flags, PA_DEVERR_TIMEOUT);
+              ok = false;
+              break;
             }
           }
         }
+        (void)ok;
         tc_commit(smem_u32(&bars->drain));
         drain_wait(smem_u32(&bars->drain), 0, P.err_flags);
       }
@@ -780,14 +913,21 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
       // the fp16 stage is free (PV of the tile that used it before is done).
       const int ct = tid - 320;  // 0..63
       constexpr int kS8 = C::kStages8 > 0 ? C::kStages8 : 1;  // (non-FP8 builds never run this)
-      for (int k = 0; k < n; ++k) {
+      int k = 0;  // global tile index
+      bool okc = true;
+      for (int iu = 0; okc; ++iu) {
+        Work w;
+        if (!pair_unit<N>(P, W, iu, pair, npairs, nullptr, &w)) break;
+        if (w.status != 0) continue;
+        const int n = (int)max((int64_t)0, w.t_end - w.t_begin);
+        for (int kk = 0; kk < n; ++kk, ++k) {
         const int s8 = k % kS8, s16 = k % STAGES;
-        bool okc = wait_bar(smem_u32(&bars->full8[s8]), (k / kS8) & 1, abort,
-                            P.err_flags);
+        okc = wait_bar(smem_u32(&bars->full8[s8]), (k / kS8) & 1, abort, P.err_flags);
         if (okc && k >= STAGES)
           okc = wait_bar(smem_u32(&bars->empty[s16]), ((k / STAGES) & 1) ^ 1, abort,
                          P.err_flags);
-        if (!__all_sync(0xffffffffu, okc)) break;
+        okc = __all_sync(0xffffffffu, okc);
+        if (!okc) break;
         const uint8_t* s8p = k8_s + s8 * C::kStage8Bytes;
 #pragma unroll 4
         for (int i = ct; i < N * 20; i += 64) {  // chunk j of row r
@@ -807,11 +947,11 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         fence_proxy_async();
         mbar_arrive(smem_u32(&bars->full[s16]));
         mbar_arrive(smem_u32(&bars->empty8[s8]));
+        }
       }
     }
   }
 
-  if (W.status != 0) grid_dep_launch();
   tc_fence_before();
   cluster_sync_all();  // the peer no longer writes into this CTA's shared memory
   if (warp == 5) {
@@ -889,8 +1029,14 @@ cudaError_t launch_pair_impl(const Geometry& g, Phase ph, const ReadArgs& a, Par
     set_launch_step("query tensor map");
     return cudaErrorInvalidValue;
   }
-  const int64_t units = ph == Phase::kDecode ? (int64_t)P.units : nq;
-  e = launch_pdl(kern, dim3((unsigned)(units * 2)), dim3(C::kThreads), smem, a.stream, map, qmap,
+  // decode: one pair per unit of the plan; prefill: at most one wave of
+  // pairs, each looping over its share of the nq token units
+  int64_t pairs = P.units;
+  if (ph != Phase::kDecode) {
+    P.units = (int)nq;
+    pairs = nq < g.num_sms / 2 ? nq : g.num_sms / 2;
+  }
+  e = launch_pdl(kern, dim3((unsigned)(pairs * 2)), dim3(C::kThreads), smem, a.stream, map, qmap,
                  qmap64, map8b, P);
   if (e != cudaSuccess) {
     set_launch_step("attention kernel launch");
