@@ -506,3 +506,52 @@ def test_gather_probe_reads_the_batch():
         B.pa_latent_gather_probe(p, d.key_cache, d.past, bt, 64, 2, 1, err)
         torch.cuda.synchronize()
         assert int(err.item()) == B.PA_DEVERR_BLOCK
+
+
+def _pair_units_workload(**kw):
+    """DeepSeek dims, H=128, two prefill sequences of 90 tokens: 180 token
+    units over one wave of 76 CTA pairs, so every pair attends two or three
+    tokens in turn (token 179 - u is unit u; pair p takes u = p, p+76, p+152)."""
+    base = dict(q_lens=[90, 90], past_lens=[100, 60], num_heads=128, **W.DSV3, block_size=64,
+                seed=33, scale=W.DSV3_SCALE)
+    base.update(kw)
+    return W.make_workload("pair_units", **base)
+
+
+def _positions(w):
+    cs, past = w.cumseq.tolist(), w.past.tolist()
+    return [past[b] + t - cs[b] for b in range(w.num_seqs) for t in range(cs[b], cs[b + 1])]
+
+
+def test_pair_prefill_invalid_positions_in_later_units():
+    """On the persistent CTA-pair prefill, tokens whose position lies past the
+    cos/sin rows (sequence 0's last 40 tokens, units 90-129: a pair's second
+    token) are flagged and their rows zeroed; every other token matches the
+    oracle. (The invalid tokens write no cache row.)"""
+    w = _pair_units_workload(cos_rows=150)
+    pos = _positions(w)
+    bad = [t for t, p in enumerate(pos) if p >= 150]
+    good = [t for t, p in enumerate(pos) if p < 150]
+    assert len(bad) == 40
+    w.slot_mapping[bad] = -1
+    got = Hn.run_gpu(w)
+    assert got["flags"] == B.PA_DEVERR_POSITION, hex(got["flags"])
+    assert np.all(got["out"][bad] == 0)
+    ref = Hn.run_oracle(w, good)
+    Hn.check_out(w, got["out"], ref["out"], good, ref["scales"])
+
+
+def test_pair_prefill_bad_block_stays_with_its_tokens():
+    """A block-table entry outside the pool in sequence 1 (read by all its
+    tokens, which the pairs attend first) zeroes exactly sequence 1's rows:
+    the tokens of sequence 0 that the same pairs attend afterwards match the
+    oracle (the per-token error bit is cleared between tokens)."""
+    w = _pair_units_workload()
+    w.block_table[1, 0] = w.num_blocks + 3
+    got = Hn.run_gpu(w)
+    assert got["flags"] == B.PA_DEVERR_BLOCK, hex(got["flags"])
+    from oracle import pa_oracle as O
+    assert np.all(O.bits_to_f64(got["out"][90:], "bf16") == 0)  # (+0 or -0: O times 0)
+    good = list(range(90))
+    ref = Hn.run_oracle(w, good)
+    Hn.check_out(w, got["out"], ref["out"], good, ref["scales"])
