@@ -30,13 +30,20 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
   if (g.fp8) {
     // FP8 cache: two fp16 key stages (the converted tiles the MMAs read) and
     // as many E4M3 stages as the rest of shared memory holds (they carry
-    // the copies in flight from HBM).
-    Shape t{g.hs, vg, 1, vg > 128 ? 64 : 128, 2, (ph == Phase::kDecode && g.H <= 64) ? 64 : 128,
-            2, false};
-    if (g.hs == 192 && vg == 128 && t.qr == 64) t.stages = kFp8Stages16;
-    t.stages8 = (kSmemBudget - 1024 - q_bytes(t) - t.stages * stage_bytes(t)) / stage8_bytes(t);
-    if (t.stages8 > 8) t.stages8 = 8;
-    if (g.hs == 192 && vg == 128 && t.qr == 64 && t.stages8 > kFp8Stages8) t.stages8 = kFp8Stages8;
+    // the copies in flight from HBM). 128-key tiles where two E4M3 stages
+    // fit beside them (not for value widths above 128, for the TMEM budget),
+    // else 64-key tiles.
+    auto fp8_shape = [&](int n) {
+      Shape t{g.hs, vg, 1, n, 2, (ph == Phase::kDecode && g.H <= 64) ? 64 : 128, 2, false};
+      const bool glm = g.hs == 192 && vg == 128 && t.qr == 64 && n == 128;
+      if (glm) t.stages = kFp8Stages16;
+      t.stages8 = (kSmemBudget - 1024 - q_bytes(t) - t.stages * stage_bytes(t)) / stage8_bytes(t);
+      if (t.stages8 > 8) t.stages8 = 8;
+      if (glm && t.stages8 > kFp8Stages8) t.stages8 = kFp8Stages8;
+      return t;
+    };
+    Shape t = fp8_shape(vg > 128 ? 64 : 128);
+    if (t.stages8 < 2 && t.n == 128) t = fp8_shape(64);
     if (t.stages8 < 2 || tmem_cols_used(t) > 512) return false;
     *s = t;
     return true;

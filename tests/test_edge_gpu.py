@@ -67,6 +67,11 @@ FP8_VARIANTS = {
     "heads_128": dict(num_heads=128),
     "hs_256_vhs_256": dict(head_size=256, v_head_size=256, rotary_offset=192),
     "hs_80_vhs_48": dict(head_size=80, v_head_size=48, rotary_offset=16),
+    # wide latents with narrow values: 64-key tiles (two E4M3 stages do not
+    # fit beside 128-key ones)
+    "hs_224_vhs_106": dict(head_size=224, v_head_size=106, rotary_offset=160),
+    "hs_256_vhs_128_heads_128": dict(head_size=256, v_head_size=128, rotary_offset=192,
+                                     num_heads=128),
     "k_scale_odd": dict(k_scale=0.0123),
     "saturating_keys": dict(k_scale=2.0 ** -10),
 }
