@@ -69,10 +69,10 @@ NCU_TRAFFIC = {
     # cache rows): the quarter-size capture times four
     "dsv3_prefill": ("tc_pair_kernel", 4 * 1096044800, "b66d85dcac5984e1",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
-    "glm_decode": ("tc_attn_kernel", 54257664, "53e331d2f8ef9cb5", "measured on this workload"),
-    "mixed_serving": ("tc_attn_kernel", 99262208, "53e331d2f8ef9cb5", "measured on this workload"),
+    "glm_decode": ("tc_attn_kernel", 54257664, "e8579a24f94f53ab", "measured on this workload"),
+    "mixed_serving": ("tc_attn_kernel", 99262208, "e8579a24f94f53ab", "measured on this workload"),
     "gqa_decode": ("tc_gqa_kernel", 580619008, "e5fd8ae0e2ff9a81", "measured on this workload"),
-    "glm_decode_fp8": ("tc_attn_kernel", 25967360, "53e331d2f8ef9cb5", "measured on this workload"),
+    "glm_decode_fp8": ("tc_attn_kernel", 25967360, "e8579a24f94f53ab", "measured on this workload"),
 }
 
 
