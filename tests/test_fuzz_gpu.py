@@ -8,6 +8,8 @@ interleaved, or none), a block size, a window and softcap, the cache format
 batch of decode sequences followed by prefill chunks, some slots -1. The
 outputs meet the scale-aware bound and the cache rows the write rules; on
 the geometries the tensor-core kernels cover, both read phases run there.
+The SEPARATE layout gets the same treatment (kv heads, group sizes, widths,
+sink logits and q/k RMSNorm drawn at random).
 """
 import random
 
@@ -81,3 +83,48 @@ def test_random_configuration(seed):
     Hn.check_cache(w, got["cache"], ref["cache"])
     err, ratio = Hn.check_out(w, got["out"], ref["out"], scales=ref["scales"])
     print(f"RATIO fuzz{seed}: {ratio:.3f} of the scale-aware bound ({desc})")
+
+
+SEPARATE_CASES = 16
+
+
+def _draw_separate(seed: int):
+    rng = random.Random(5000 + seed)
+    kvh = rng.choice([1, 2, 3, 4, 8])
+    grp = rng.choice([1, 2, 3, 4, 8, 16]) if kvh > 1 else rng.choice([1, 4, 32, 128])
+    hs = rng.randint(4, 16) * 16
+    vhs = rng.randint(8, hs // 8) * 8
+    rd = rng.choice([0, 16, 32, 64, hs - hs % 32])
+    rd = min(rd, hs)
+    ro = rng.randint(0, (hs - rd) // 8) * 8 if rd else 0
+    nd, npf = rng.randint(0, 3), rng.randint(0, 2)
+    if nd + npf == 0:
+        npf = 1
+    q_lens = [1] * nd + [rng.randint(2, 23) for _ in range(npf)]
+    past = [rng.randint(0, 299) for _ in q_lens]
+    kw = dict(dtype=torch.float16 if rng.random() < 0.35 else torch.bfloat16,
+              num_heads=kvh * grp, kv_num_heads=kvh, head_size=hs, v_head_size=vhs,
+              rotary_offset=ro, rotary_dim=rd, rotary_interleaved=int(rd > 0 and rng.random() < 0.3),
+              block_size=rng.choice([16, 32, 64, 128]),
+              local_window_size=rng.choice([-1, -1, 0, 7, 100]),
+              softcap=rng.choice([0.0, 0.0, 2.0, 30.0]), head_sink=rng.random() < 0.5,
+              qk_norm=rng.random() < 0.5, seed=seed, drop_slots=rng.randint(0, 1),
+              scale=rng.uniform(0.03, 0.2))
+    return q_lens, past, kw
+
+
+@pytest.mark.parametrize("seed", range(SEPARATE_CASES))
+def test_random_separate_configuration(seed):
+    """SEPARATE layout (grouped-query heads over separate key and value
+    caches, optional sink logit and q/k RMSNorm): random geometries within
+    the tensor-core kernels' range (widths 64..256, value width a multiple
+    of 8, up to 128 query heads per kv head), options and ragged batches."""
+    q_lens, past, kw = _draw_separate(seed)
+    w = W.make_separate_workload(f"sepfuzz{seed}", q_lens=q_lens, past_lens=past, **kw)
+    desc = {k: v for k, v in kw.items() if k != "seed"} | dict(q_lens=q_lens, past=past)
+    got = Hn.run_gpu_separate(w)
+    assert got["flags"] == 0, (hex(got["flags"]), desc)
+    ref = Hn.run_oracle_separate(w)
+    Hn.check_separate_caches(w, got, ref)
+    err, ratio = Hn.check_out(w, got["out"], ref["out"], scales=ref["scales"])
+    print(f"RATIO sepfuzz{seed}: {ratio:.3f} of the scale-aware bound ({desc})")
