@@ -7,12 +7,14 @@ interleaved, or none), a block size, a window and softcap, the cache format
 (16-bit or FP8 where the tensor-core kernels read it) and a small ragged
 batch of decode sequences followed by prefill chunks, some slots -1. The
 outputs meet the scale-aware bound and the cache rows the write rules; on
-the geometries the tensor-core kernels cover, both read phases run there.
+the geometries the tensor-core kernels cover, both read phases run there;
+a second run gives the same bits.
 The SEPARATE layout gets the same treatment (kv heads, group sizes, widths,
 sink logits and q/k RMSNorm drawn at random).
 """
 import random
 
+import numpy as np
 import pytest
 import torch
 
@@ -54,7 +56,9 @@ def _draw(seed: int):
     if nd + npf == 0:
         nd = 1
     q_lens = [1] * nd + [rng.randint(2, 23) for _ in range(npf)]
-    past = [rng.randint(0, 299) for _ in q_lens]
+    long_ctx = rng.random() < 0.3  # decode contexts of thousands of keys: many key splits
+    past = [rng.randint(1000, 5000) if long_ctx and q == 1 else rng.randint(0, 299)
+            for q in q_lens]
     default_scale = vhs == hs and rng.random() < 0.5
     kw = dict(dtype=dtype, num_heads=H, head_size=hs, v_head_size=vhs, rotary_offset=ro,
               rotary_dim=rd, rotary_interleaved=inter, block_size=bs,
@@ -79,6 +83,8 @@ def test_random_configuration(seed):
     assert got["flags"] == 0, (hex(got["flags"]), desc)
     if tensor_core:
         assert (got["op"].kernel_family(0), got["op"].kernel_family(1)) == (1, 1), desc
+    again = Hn.run_gpu(w, scale=0.0 if default_scale else None)  # deterministic: same bits
+    assert np.array_equal(got["out"], again["out"]), desc
     ref = Hn.run_oracle(w)
     Hn.check_cache(w, got["cache"], ref["cache"])
     err, ratio = Hn.check_out(w, got["out"], ref["out"], scales=ref["scales"])
