@@ -64,10 +64,10 @@ KERNEL_SOURCES = {
 }
 # workload -> (kernel, bytes per launch, source digest, how the figure was taken)
 NCU_TRAFFIC = {
-    "dsv3_decode": ("tc_pair_kernel", 315180800, "b66d85dcac5984e1", "measured on this workload"),
+    "dsv3_decode": ("tc_pair_kernel", 315180800, "5075f434a37767de", "measured on this workload"),
     # traffic grows with the tokens (query in, output out, each sequence's
     # cache rows): the quarter-size capture times four
-    "dsv3_prefill": ("tc_pair_kernel", 4 * 1096044800, "b66d85dcac5984e1",
+    "dsv3_prefill": ("tc_pair_kernel", 4 * 1096044800, "5075f434a37767de",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
     "glm_decode": ("tc_attn_kernel", 54257664, "e8579a24f94f53ab", "measured on this workload"),
     "mixed_serving": ("tc_attn_kernel", 99262208, "e8579a24f94f53ab", "measured on this workload"),

@@ -25,7 +25,9 @@
 //
 // Roles: warps 0-3 softmax/epilogue (thread = head row = TMEM lane), warp 4
 // TMA producer, warp 5 TMEM allocation + the MMA-issuing thread, warps 6-9
-// score exchange. Key tiles of 64 keys, 3 stages; every wait is bounded.
+// score exchange (FP8 cache: warps 10-11 convert E4M3 tiles to fp16). Key
+// tiles of 64 keys in 3 stages (FP8 cache: 2 fp16 stages fed from 2 E4M3
+// stages); every wait is bounded.
 //
 // Work units: decode runs one pair per unit of the device plan (a sequence's
 // key split). Prefill is persistent: at most one wave of pairs, each looping
