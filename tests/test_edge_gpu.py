@@ -560,3 +560,71 @@ def test_pair_prefill_bad_block_stays_with_its_tokens():
     good = list(range(90))
     ref = Hn.run_oracle(w, good)
     Hn.check_out(w, got["out"], ref["out"], good, ref["scales"])
+
+
+def _prefill_units_workload(**kw):
+    """GLM dims, H=64 (two tokens per unit of the single-CTA kernel),
+    prefill sequences of 1200 and 700 tokens on pasts 0 and 300: 950 units,
+    three waves and more of the two-CTAs-per-SM prefill shape."""
+    base = dict(q_lens=[1200, 700], past_lens=[0, 300], num_heads=64, **W.GLM, block_size=16,
+                seed=41, scale=0.07)
+    base.update(kw)
+    return W.make_workload("prefill_units", **base)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "fp16"])
+def test_prefill_many_units(dtype):
+    """A long chunked prefill on the half-SM prefill shape (units of two
+    tokens, contexts up to 1000 keys): every token against the oracle, and a
+    second run gives the same bits."""
+    w = _prefill_units_workload(dtype=dtype)
+    got = _check(w, family=1)
+    again = Hn.run_gpu(w)
+    assert np.array_equal(got["out"], again["out"])
+
+
+def test_mixed_many_units():
+    """A mixed batch in one grid: 40 decode sequences (long contexts,
+    several key splits each) ahead of 1500 prefill tokens, with a window and
+    a softcap."""
+    q_lens = [1] * 40 + [900, 600]
+    past = [2000 + 37 * i for i in range(40)] + [0, 450]
+    w = W.make_workload("mixed_units", q_lens=q_lens, past_lens=past, num_heads=64, **W.GLM,
+                        block_size=16, seed=42, scale=0.07, dtype=torch.float16,
+                        local_window_size=700, softcap=30.0, num_decode_seqs=40, drop_frac=0.05)
+    _check(w, family=1)
+
+
+def test_prefill_invalid_positions_among_valid_units():
+    """Tokens past the cos/sin rows (sequence 0's last 200) are flagged and
+    their rows zeroed; every other token matches the oracle."""
+    w = _prefill_units_workload(cos_rows=1000)
+    pos = _positions(w)
+    bad = [t for t, p in enumerate(pos) if p >= 1000]
+    good = [t for t, p in enumerate(pos) if p < 1000]
+    assert len(bad) == 200
+    w.slot_mapping[bad] = -1
+    got = Hn.run_gpu(w)
+    assert got["flags"] == B.PA_DEVERR_POSITION, hex(got["flags"])
+    assert np.all(got["out"][bad] == 0)
+    ref = Hn.run_oracle(w, good)
+    Hn.check_out(w, got["out"], ref["out"], good, ref["scales"])
+
+
+def test_prefill_bad_block_stays_with_its_units():
+    """A block-table entry outside the pool at sequence 0's keys 640-655
+    zeroes exactly the rows of the units that read it (sequence 0's tokens
+    at positions 640 and later; a unit's two tokens share their tiles); every
+    other unit matches the oracle."""
+    w = _prefill_units_workload()
+    w.block_table[0, 40] = w.num_blocks + 3
+    got = Hn.run_gpu(w)
+    assert got["flags"] == B.PA_DEVERR_BLOCK, hex(got["flags"])
+    from oracle import pa_oracle as O
+    pos = _positions(w)
+    bad = [t for t in range(1200) if pos[t] >= 640]
+    bad_set = set(bad)
+    good = [t for t in range(w.num_tokens) if t not in bad_set]
+    assert np.all(O.bits_to_f64(got["out"][bad], "bf16") == 0)  # (+0 or -0: O times 0)
+    ref = Hn.run_oracle(w, good)
+    Hn.check_out(w, got["out"], ref["out"], good, ref["scales"])
