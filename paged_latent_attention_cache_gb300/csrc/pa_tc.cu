@@ -50,10 +50,11 @@ bool pick(const Geometry& g, Phase ph, Shape* s) {
   }
   // Prefill with H <= 64 (units of 128 / H tokens, each a short chain of a
   // few key tiles) runs two CTAs per SM where they fit in half an SM: 64-key
-  // tiles, two stages and a single S/P buffer (97 KB of shared memory and
-  // 224 TMEM columns at 192/128).
+  // tiles, two stages and two S buffers, each tile's P written over its own
+  // S so that QK^T of the next tile runs during the softmax of this one (97
+  // KB of shared memory and 256 TMEM columns at 192/128).
   if (ph == Phase::kPrefill && g.H <= 64) {
-    const Shape u{g.hs, vg, 1, 64, 2, 128, 1, false};
+    const Shape u{g.hs, vg, 1, 64, 2, 128, 2, false, 0, true};
     if (smem_bytes(u) <= kHalfSmemBudget && tmem_alloc_cols(tmem_cols_used(u)) <= 256) {
       *s = u;
       return true;
@@ -80,7 +81,7 @@ cudaError_t launch_single(const Geometry& g, Phase ph, const ReadArgs& a, Params
   if (s.stages8) return launch_fp8<T>(g, ph, a, P, nq, s);
   if (s.n == 128 && s.qr == 64) return launch_shape<T, 128, 64, 2, 0, 0, 0>(g, ph, a, P, nq, s);
   if (s.n == 128) return launch_shape<T, 128, 128, 2, 0, 0, 0>(g, ph, a, P, nq, s);
-  if (s.nb == 1) return launch_shape<T, 64, 128, 1, 0, 0, 0>(g, ph, a, P, nq, s);
+  if (s.pos) return launch_shape<T, 64, 128, 2, 0, 0, 0, false, true>(g, ph, a, P, nq, s);
   if (s.qr == 64) return launch_shape<T, 64, 64, 2, 0, 0, 0>(g, ph, a, P, nq, s);
   return launch_shape<T, 64, 128, 2, 0, 0, 0>(g, ph, a, P, nq, s);
 }

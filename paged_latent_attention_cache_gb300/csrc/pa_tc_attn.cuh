@@ -34,7 +34,8 @@
 //   (With 64 query rows the producer and MMA warps are 6 and 7, on other
 //   scheduler partitions than the two softmax warps that hold rows.)
 // Pipelines: K tiles in a STAGES-deep ring (full/empty mbarriers), S and P
-// in NB TMEM buffers (two, or one where two CTAs share an SM). Every
+// in two TMEM buffers each (where two CTAs share an SM, each tile's P is
+// written over its own S columns instead: POS). Every
 // mbarrier wait is bounded: on expiry the
 // CTA sets PA_DEVERR_TIMEOUT in the error word, drains what it issued and
 // exits without trapping.
@@ -138,14 +139,17 @@ __device__ __noinline__ void issue_pv(uint32_t d, uint32_t a, uint64_t b0, uint3
 // instructions are fetched cold on every launch.
 // FP8: the cache holds E4M3 codes; the MMAs then take fp16 operands (the
 // query rounded to fp16 once, the key tiles converted exactly, P in fp16).
-template <typename T, int N, int QR, int NB, bool CAP, int HSF, int VGF, int STF, bool FP8>
+template <typename T, int N, int QR, int NB, bool CAP, int HSF, int VGF, int STF, bool FP8,
+          bool POS>
 __global__ void __launch_bounds__(Tile<N, QR, NB, FP8>::kThreads, 1)
 tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                const __grid_constant__ Params P) {
   using C = Tile<N, QR, NB, FP8>;
   using TM = typename std::conditional<FP8, __half, T>::type;  // MMA operand type
   constexpr int kSlabsF = (HSF + 63) / 64;
-  constexpr int kTmemColsF = fixed_tmem_cols(VGF + NB * N + NB * N / 2);
+  constexpr int kTmemColsF = fixed_tmem_cols(VGF + NB * N + (POS ? 0 : NB * N / 2));
+  // P (16-bit, N/2 columns per tile) has buffers of its own after the S
+  // buffers, or (POS) is written over its own tile's S columns
   const int hs = HSF ? HSF : P.hs;
   const int slabs = HSF ? kSlabsF : P.slabs;
   const int vg = VGF ? VGF : P.vg;
@@ -153,7 +157,8 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
   const int stage_bytes = HSF ? N * kSlabsF * 128 : P.stage_bytes;
   const int q_bytes = HSF ? QR * kSlabsF * 128 : P.q_bytes;
   const int col_s = VGF ? VGF : P.col_s;          // TMEM: O | S x NB | P x NB
-  const int col_p = VGF ? VGF + NB * N : P.col_p;
+  const int col_p = POS ? col_s : VGF ? VGF + NB * N : P.col_p;
+  constexpr int kPStride = POS ? N : N / 2;  // TMEM columns from one P buffer to the next
   const uint32_t tmem_cols = VGF ? (uint32_t)kTmemColsF : (uint32_t)P.tmem_cols;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Work work;
@@ -463,8 +468,9 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
           fence_proxy_async();
         }
 
-        // P buffer sb is free once PV(k-NB) has completed.
-        if (k >= NB) {
+        // P buffer sb is free once PV(k-NB) has completed. (POS: P goes over
+        // S(k), which QK^T(k) wrote only after PV(k-NB) had completed.)
+        if (!POS && k >= NB) {
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&bars->pv_done[sb]),
                                                 ((k - NB) / NB) & 1, abort, P.err_flags));
           if (!ok) break;
@@ -491,7 +497,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             if (!CAP) lsum += exp_chunk<TM, 0>(r, pk, A);
             else if (mode == 1) lsum += exp_chunk<TM, 1>(r, pk, A);
             else lsum += exp_chunk<TM, 2>(r, pk, A);
-            tmem_st16(lane_addr + col_p + sb * (N / 2) + c / 2, pk);
+            tmem_st16(lane_addr + col_p + sb * kPStride + c / 2, pk);
           }
           if (!dry) l += lsum;
           if (__any_sync(0xffffffffu, rescale)) {
@@ -685,7 +691,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         // commit also tracks them.
         issue_qk<C::kQBox, C::kKBox, HSF / 16>(tmem + col_s + (NB - 1) * N, sdesc(q_base, 16, 1024),
                                      sdesc(k_base, 16, 1024), nk, kIdQK);
-        issue_pv<N>(tmem, tmem + col_p + (NB - 1) * (N / 2), sdesc(k_base, C::kKBox, 1024), 0u,
+        issue_pv<N>(tmem, tmem + col_p + (NB - 1) * kPStride, sdesc(k_base, C::kKBox, 1024), 0u,
                     id_pv);
         bool ok = wait_bar(smem_u32(&bars->q_full), 0, abort, P.err_flags);
         if (ok) {
@@ -705,7 +711,7 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 tc_fence_after();
                 // B = V[keys, channels]: MN-major, 64-channel slabs kKBox apart
                 // (leading offset), 8-key groups 1024 bytes apart (stride).
-                issue_pv<N>(tmem, tmem + col_p + sb * (N / 2),
+                issue_pv<N>(tmem, tmem + col_p + sb * kPStride,
                             sdesc(k_base + stage * stage_bytes, C::kKBox, 1024),
                             kp > 0 ? 1u : 0u, id_pv);
                 tc_commit(smem_u32(&bars->pv_done[sb]));
@@ -714,12 +720,17 @@ tc_attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                 progressed = true;
               }
             }
-            // QK^T(kq): needs its key tile and a free S buffer.
+            // QK^T(kq): needs its key tile and a free S buffer. (POS: P(kq-NB)
+            // lies in that buffer, so PV(kq-NB) must have completed; before
+            // the first reuse, the warm-up PV that read buffer NB-1 has
+            // completed with QK^T(0), whose commit tracks it.)
             if (kq < n && kq < kp + NB) {
               const int stage = kq % stages, sb = kq % NB;
               if (mbar_test_wait(smem_u32(&bars->full[stage]), (kq / stages) & 1) &&
-                  (kq < NB ||
-                   mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NB) / NB) & 1))) {
+                  (kq < NB ? (!POS || kq == 0 || mbar_test_wait(smem_u32(&bars->s_full[0]), 0))
+                           : (mbar_test_wait(smem_u32(&bars->s_free[sb]), ((kq - NB) / NB) & 1) &&
+                              (!POS || mbar_test_wait(smem_u32(&bars->pv_done[sb]),
+                                                      ((kq - NB) / NB) & 1))))) {
                 tc_fence_after();
                 issue_qk<C::kQBox, C::kKBox, HSF / 16>(tmem + col_s + sb * N, sdesc(q_base, 16, 1024),
                                              sdesc(k_base + stage * stage_bytes, 16, 1024), nk,
@@ -821,14 +832,17 @@ inline int stage8_bytes(const Shape& s) { return s.n * s.hs; }
 inline int smem_bytes(const Shape& s) {
   return q_bytes(s) + s.stages * stage_bytes(s) + s.stages8 * stage8_bytes(s) + 1024;
 }
-inline int tmem_cols_used(const Shape& s) { return s.vg + s.nb * s.n + s.nb * s.n / 2; }
+inline int tmem_cols_used(const Shape& s) {
+  return s.vg + s.nb * s.n + (s.pos ? 0 : s.nb * s.n / 2);
+}
 inline int tmem_alloc_cols(int used) {
   int c = 32;
   while (c < used) c <<= 1;
   return c;
 }
 
-template <typename T, int N, int QR, int NB, int HSF, int VGF, int STF, bool FP8 = false>
+template <typename T, int N, int QR, int NB, int HSF, int VGF, int STF, bool FP8 = false,
+          bool POS = false>
 cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params& P, int64_t nq,
                          const Shape& s) {
   using C = Tile<N, QR, NB, FP8>;
@@ -838,7 +852,7 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   P.stage_bytes = stage_bytes(s);
   P.q_bytes = q_bytes(s);
   P.col_s = s.vg;
-  P.col_p = s.vg + NB * N;
+  P.col_p = POS ? s.vg : s.vg + NB * N;
   P.tmem_cols = tmem_alloc_cols(tmem_cols_used(s));
   P.stages8 = s.stages8;
   P.stage8_bytes = stage8_bytes(s);
@@ -848,8 +862,8 @@ cudaError_t launch_shape(const Geometry& g, Phase ph, const ReadArgs& a, Params&
   // maximum less the kernel's static shared memory
   static std::atomic<bool> configured[2][64];
   const int cap = P.softcap_on ? 1 : 0;
-  auto kern = cap ? tc_attn_kernel<T, N, QR, NB, true, HSF, VGF, STF, FP8>
-                  : tc_attn_kernel<T, N, QR, NB, false, HSF, VGF, STF, FP8>;
+  auto kern = cap ? tc_attn_kernel<T, N, QR, NB, true, HSF, VGF, STF, FP8, POS>
+                  : tc_attn_kernel<T, N, QR, NB, false, HSF, VGF, STF, FP8, POS>;
   cudaError_t e = once_per_device(configured[cap], g.device, [&] {
     int optin = 0;
     cudaFuncAttributes fa;
@@ -933,8 +947,8 @@ inline bool fixed_shape(const Shape& s) {
   if (s.stages8)
     return s.n == 128 && s.qr == 64 && s.nb == 2 && s.stages == kFp8Stages16 &&
            s.stages8 == kFp8Stages8;
+  if (s.pos) return s.n == 64 && s.qr == 128 && s.nb == 2 && s.stages == 2;
   return (s.n == 128 && s.qr == 64 && s.nb == 2 && s.stages == 4) ||
-         (s.n == 64 && s.qr == 128 && s.nb == 1 && s.stages == 2) ||
          (s.n == 128 && s.qr == 128 && s.nb == 2 && s.stages == 3);
 }
 template <typename T>

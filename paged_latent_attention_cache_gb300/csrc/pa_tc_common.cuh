@@ -813,6 +813,7 @@ struct Shape {
   int hs, vg, groups, n, stages, qr, nb;
   bool pair;
   int stages8 = 0;  // FP8 cache: E4M3 stages (0: the cache is in the query dtype)
+  bool pos = false;  // P written over its tile's S columns (no TMEM of its own)
 };
 
 // Decode grid: one wave of CTAs (one per SM), at least one unit per sequence.
