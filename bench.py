@@ -69,10 +69,10 @@ NCU_TRAFFIC = {
     # cache rows): the quarter-size capture times four
     "dsv3_prefill": ("tc_pair_kernel", 4 * 1096044800, "5075f434a37767de",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
-    "glm_decode": ("tc_attn_kernel", 54257664, "e8579a24f94f53ab", "measured on this workload"),
-    "mixed_serving": ("tc_attn_kernel", 99262208, "e8579a24f94f53ab", "measured on this workload"),
+    "glm_decode": ("tc_attn_kernel", 54265088, "b623479eada5c5cb", "measured on this workload"),
+    "mixed_serving": ("tc_attn_kernel", 99709440, "b623479eada5c5cb", "measured on this workload"),
     "gqa_decode": ("tc_gqa_kernel", 580619008, "e5fd8ae0e2ff9a81", "measured on this workload"),
-    "glm_decode_fp8": ("tc_attn_kernel", 25967360, "e8579a24f94f53ab", "measured on this workload"),
+    "glm_decode_fp8": ("tc_attn_kernel", 25967616, "b623479eada5c5cb", "measured on this workload"),
 }
 
 
