@@ -542,25 +542,27 @@ tc_gqa_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
           grid_dep_wait();
           waited = true;
         }
-        if (k >= stages) {
-          bool okw = true;
-          if (lane == 0)
-            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / stages) & 1) ^ 1, abort,
-                           P.err_flags);
-          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
-        }
+        // the boxes' rows (block ids loaded) before the wait for the stage,
+        // so that the copies go out as soon as the stage is free
         int y = (int)P.num_slots;  // out of range: TMA fills zeros
         if (lane < nsub) {
           const int64_t key0 = (t_begin + k) * N + (int64_t)lane * P.box_rows;
           if (key0 <= pos_hi && key0 + P.box_rows - 1 >= lo) {
             const int32_t phys = bt[key0 / P.bs];
             if (phys >= 0 && phys < P.num_blocks) {
-              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
+              y = (int)((int64_t)phys * P.bs + (key0 & (int64_t)(P.bs - 1)));
             } else {
               bars->bad = 1;
               raise_flag(P.err_flags, PA_DEVERR_BLOCK);
             }
           }
+        }
+        if (k >= stages) {
+          bool okw = true;
+          if (lane == 0)
+            okw = wait_bar(smem_u32(&bars->empty[stage]), ((k / stages) & 1) ^ 1, abort,
+                           P.err_flags);
+          if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) break;
         }
         if (lane == 0) mbar_expect_tx(smem_u32(&bars->full[stage]), (uint32_t)stage_bytes);
         __syncwarp();

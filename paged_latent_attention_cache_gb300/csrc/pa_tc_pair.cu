@@ -740,6 +740,20 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             grid_dep_wait();  // the write phase's cache rows are complete and visible
             waited = true;
           }
+          // The boxes' rows are worked out before the wait for the stage, so
+          // that the copies go out as soon as the stage is free (block size: a
+          // power of two).
+          int y = (int)P.num_slots;  // out of range: TMA fills zeros
+          const int phys = ids.get(kk * nsub, lane & (nsub - 1), lane);
+          if (lane < nsub && ids.visible(kk * nsub + lane)) {
+            if (phys >= 0 && phys < P.num_blocks) {
+              const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
+              y = (int)((int64_t)phys * P.bs + (key0 & (int64_t)(P.bs - 1)));
+            } else {
+              atomicOr(&bars->bad_mask, 1 << (au & 31));
+              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
+            }
+          }
           if (k >= PST) {
             bool okw = true;
             if (lane == 0)
@@ -747,17 +761,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
             if (!__shfl_sync(0xffffffffu, okw ? 1 : 0, 0)) {
               okp = false;
               break;
-            }
-          }
-          int y = (int)P.num_slots;  // out of range: TMA fills zeros
-          const int phys = ids.get(kk * nsub, lane & (nsub - 1), lane);
-          if (lane < nsub && ids.visible(kk * nsub + lane)) {
-            if (phys >= 0 && phys < P.num_blocks) {
-              const int64_t key0 = (t_begin + kk) * N + (int64_t)lane * P.box_rows;
-              y = (int)((int64_t)phys * P.bs + key0 % P.bs);
-            } else {
-              atomicOr(&bars->bad_mask, 1 << (au & 31));
-              raise_flag(P.err_flags, PA_DEVERR_BLOCK);
             }
           }
           if (lane == 0)
