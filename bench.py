@@ -64,15 +64,15 @@ KERNEL_SOURCES = {
 }
 # workload -> (kernel, bytes per launch, source digest, how the figure was taken)
 NCU_TRAFFIC = {
-    "dsv3_decode": ("tc_pair_kernel", 315074304, "d95f1ac2e59d1d49", "measured on this workload"),
+    "dsv3_decode": ("tc_pair_kernel", 315103744, "73ef4a7681d71ef4", "measured on this workload"),
     # traffic grows with the tokens (query in, output out, each sequence's
     # cache rows): the quarter-size capture times four
-    "dsv3_prefill": ("tc_pair_kernel", 4 * 1096123648, "d95f1ac2e59d1d49",
+    "dsv3_prefill": ("tc_pair_kernel", 4 * 1096469504, "73ef4a7681d71ef4",
                      "dsv3_prefill_small (4 x 1024 tokens) scaled by 4"),
-    "glm_decode": ("tc_attn_kernel", 54364928, "224664b7244fdbc9", "measured on this workload"),
-    "mixed_serving": ("tc_attn_kernel", 99880448, "224664b7244fdbc9", "measured on this workload"),
-    "gqa_decode": ("tc_gqa_kernel", 580324608, "ebaefdf282597a66", "measured on this workload"),
-    "glm_decode_fp8": ("tc_attn_kernel", 25968384, "224664b7244fdbc9", "measured on this workload"),
+    "glm_decode": ("tc_attn_kernel", 54154496, "05afb7237f0565c4", "measured on this workload"),
+    "mixed_serving": ("tc_attn_kernel", 99269120, "05afb7237f0565c4", "measured on this workload"),
+    "gqa_decode": ("tc_gqa_kernel", 579862272, "50f50be27473339b", "measured on this workload"),
+    "glm_decode_fp8": ("tc_attn_kernel", 25967872, "05afb7237f0565c4", "measured on this workload"),
 }
 
 

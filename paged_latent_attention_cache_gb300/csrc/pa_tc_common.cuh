@@ -337,7 +337,8 @@ struct BlockIds {
     return i < nbox && key <= hi && key + box_rows - 1 >= lo;
   }
   __device__ __forceinline__ int fetch(int i) const {
-    return visible(i) ? bt[(key0 + (int64_t)i * box_rows) / bs] : 0;
+    // (block size: a power of two)
+    return visible(i) ? bt[(key0 + (int64_t)i * box_rows) >> (__ffs(bs) - 1)] : 0;
   }
   __device__ __forceinline__ void start(int lane) {
     batch = 0;

@@ -711,6 +711,12 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
         const int32_t b = w.b;
         const int64_t lo = P.window >= 0 ? max((int64_t)0, pos - P.window) : 0;
         const int n = (int)max((int64_t)0, w.t_end - t_begin);
+        // (the unit's first block ids are requested before anything else)
+        BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
+                     P.box_rows, P.bs, n * nsub};
+        ids.start(lane);
+        int dirty_from = 0;
+        if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, w.past / N - t_begin);
         // the query region is free once QK^T of the previous unit's last tile
         // has completed
         if (last_k >= 0) {
@@ -729,11 +735,6 @@ tc_pair_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__
                         (int)(t * P.H), qb);
           tma_load_2d(smem_u32(q_s) + q_half_off, &qmap64, g ? 288 : 256, (int)(t * P.H), qb);
         }
-        int dirty_from = 0;
-        if (P.early && P.own_slots) dirty_from = (int)max((int64_t)0, w.past / N - t_begin);
-        BlockIds ids{P.block_table + (int64_t)b * P.max_blocks, t_begin * N, lo, pos,
-                     P.box_rows, P.bs, n * nsub};
-        ids.start(lane);
         for (int kk = 0; kk < n; ++kk, ++k) {
           const int stage = k % PST;
           if (!waited && kk >= dirty_from) {
